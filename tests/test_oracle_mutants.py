@@ -1,0 +1,63 @@
+"""Planted mistakes in a copy of the oracle, on the CPU: each must fail at least one pin.
+
+Every mutant is the oracle's own source with one plausible mistake
+substituted (a wrong head mapping, an off-by-one mask, a dropped scale, a
+wrong sign, a transposed operand, ...). A pin set that let one of them
+through would not be pinning that part of the oracle.
+"""
+
+import pathlib
+import types
+
+import pytest
+
+import oracle
+import oracle_checks as oc
+from oracle import monoid
+
+SRC = (pathlib.Path(oracle.__file__).parent / "attention.py").read_text()
+
+MUTANTS = {
+    "gqa_head_mapping_modulo": ("return h // (Hq // Hkv)", "return h % Hkv"),
+    "causal_sees_next_key": ("np.where(j <= np.asarray(row_idx)[:, None]", "np.where(j <= np.asarray(row_idx)[:, None] + 1"),
+    "score_scale_dropped": ("s = scale * (q_rows @ k_head.T)", "s = (q_rows @ k_head.T)"),
+    "lse_base2": ("lse = m + np.log(", "lse = m + np.log2("),
+    "dS_sign": ("dS = P * (dP - Dvec[:, None])", "dS = P * (dP + Dvec[:, None])"),
+    "D_from_dO_only": ("Dvec = (dO[b, h] * O).sum(axis=1)", "Dvec = (dO[b, h] * dO[b, h]).sum(axis=1)"),
+    "dQ_transposed_dS": ("dQ[b, h] = scale * (dS @ k[b, g])", "dQ[b, h] = scale * (dS.T @ k[b, g])"),
+    "dK_scale_dropped": ("dK[b, g] += scale * (dS.T @ q[b, h])", "dK[b, g] += (dS.T @ q[b, h])"),
+    "dK_wrong_q_head": ("dK[b, g] += scale * (dS.T @ q[b, h])", "dK[b, g] += scale * (dS.T @ q[b, g])"),
+    "dV_not_summed_over_group": ("dV[b, g] += P.T @ dO[b, h]", "dV[b, g] = P.T @ dO[b, h]"),
+    "dV_untransposed_P": ("dV[b, g] += P.T @ dO[b, h]", "dV[b, g] += P @ dO[b, h]"),
+    "dkdv_rows_skips_rows": ("first = int(J.min()) if causal else 0", "first = int(J.max()) if causal else 0"),
+    "dq_rows_drops_D": ("dP = dO[b, h, rows] @ v[b, g].T\n    Dvec = (dO[b, h, rows] * O).sum(axis=1)",
+                        "dP = dO[b, h, rows] @ v[b, g].T\n    Dvec = 0.0 * (dO[b, h, rows] * O).sum(axis=1)"),
+}
+
+
+def _mutant_module(name):
+    old, new = MUTANTS[name]
+    assert SRC.count(old) >= 1, f"mutation anchor for {name} not found in the oracle source"
+    mod = types.ModuleType(f"oracle_mutant_{name}")
+    exec(compile(SRC.replace(old, new, 1), f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+def _first_failing_check(mod):
+    for check in oc.ALL_CHECKS:
+        fn = getattr(oc, check)
+        try:
+            if check == "check_monoid_regrouping":
+                fn(mod, monoid)
+            else:
+                fn(mod)
+        except (AssertionError, FloatingPointError, ValueError, IndexError):
+            return check
+    return None
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name):
+    mod = _mutant_module(name)
+    caught_by = _first_failing_check(mod)
+    assert caught_by is not None, f"no pin catches the planted mistake {name!r}"
