@@ -1,0 +1,346 @@
+"""Throughput of fused causal GQA attention, forward + backward, on GB300.
+
+One step = one forward (O, LSE) and one backward (dQ, dK, dV) of the whole
+workload through the C ABI, inputs resident in HBM. The default workload is
+long-context training: B=2, Hq=32, Hkv=8, S=16384, D=128, causal, seeded
+synthetic bf16 inputs (Q, K, V ~ N(0,1), dO ~ N(0, 1e-2)).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line. Under torchrun (N > 1) every rank runs its own replica
+of the workload (independent problems, no data-path collective: weak
+scaling); the reported time is the max over ranks.
+
+Throughput is algorithmic: forward 4*D flops per visible (query, key) pair
+per query head, backward 10*D (five contractions, including the recompute of
+Q K^T), i.e. fwd = 4*B*Hq*D*S(S+1)/2 and bwd = 2.5 * fwd. Masked halves of
+diagonal tiles are not counted.
+
+``--impl reference`` times the f64 CPU oracle (the only reference there is)
+on a bounded sample of the same workload, on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal GQA attention fwd+bwd TFLOP/s and % of GB300 BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def flops(B, Hq, S, D):
+    pairs = S * (S + 1) / 2.0
+    fwd = 4.0 * B * Hq * D * pairs
+    return fwd, 2.5 * fwd
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profiled_traffic(kernel_name, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_name}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not m_bytes or not m_hash:
+        return None
+    src = os.path.join(ROOT, "causal_gqa_attention_flash_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(src)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(src, f), "rb").read())
+    if h.hexdigest() != m_hash.group(1):
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(w, budget_s=12.0, prefix=4096):
+    """Time the f64 oracle on causal prefixes of the workload: all G query heads of one KV group over
+    positions [0, prefix) (a self-contained causal sub-problem), forward + backward, repeated over
+    KV groups until budget_s of wall time has passed. Returns (TFLOP/s, description, cores)."""
+    import numpy as np
+
+    import oracle
+    from gqa_inputs import make_inputs, to_f64
+
+    S = min(prefix, w.S)
+    q, k, v, dO = make_inputs(1, w.G, 1, S, w.D, seed=w.seed, do_std=w.do_std)
+    qf, kf, vf, dOf = (to_f64(t) for t in (q, k, v, dO))
+    fwd1, bwd1 = flops(1, w.G, S, w.D)
+    done, t0, units = 0.0, time.perf_counter(), 0
+    while True:
+        oracle.forward(qf, kf, vf, causal=True, scale=w.scale)
+        oracle.backward(qf, kf, vf, dOf, causal=True, scale=w.scale)
+        done += fwd1 + bwd1
+        units += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    desc = (f"{units} x (1 KV group = {w.G} query heads, causal prefix S={S}, D={w.D}) fwd+bwd in f64 numpy, "
+            f"{el:.1f} s")
+    return done / el / 1e12, desc, os.cpu_count()
+
+
+def reference_arm(args, w, rank, world):
+    if rank != 0:
+        return
+    val, desc, cores = cpu_oracle_sample(w, budget_s=max(5.0, min(30.0, 3.0 * args.steps)))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, shapes of the workload)",
+        "config": config_of(w),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": f"{w.name}: causal GQA B={w.B} Hq={w.Hq} Hkv={w.Hkv} S={w.S} D={w.D}",
+            "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": True, "scale": w.scale,
+            "seed": w.seed, "l2": "inputs larger than L2 (Q and dO are each > 129 MB)"
+            if w.B * w.Hq * w.S * w.D * 2 > 129e6 else "inputs smaller than L2 (L2 not flushed)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="long16k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--shape", default=None,
+                    help="B,Hq,Hkv,S,D: override the workload's shape (same seed and value distributions); "
+                         "for profiling smaller cases")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from gqa_inputs import WORKLOADS, Workload
+    w = WORKLOADS[args.workload]
+    if args.shape:
+        B, Hq, Hkv, S, D = (int(x) for x in args.shape.split(","))
+        w = Workload(f"{w.name}-shape{B}x{Hq}x{Hkv}x{S}x{D}", B, Hq, Hkv, S, D, seed=w.seed, do_std=w.do_std)
+
+    if args.impl == "reference":
+        reference_arm(args, w, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import causal_gqa_attention_flash_gb300 as g
+    from gqa_inputs import make_inputs
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # Each rank: its own seeded replica of the workload (independent problems).
+    q_h, k_h, v_h, dO_h = make_inputs(w.B, w.Hq, w.Hkv, w.S, w.D, w.seed + 1000 * rank, do_std=w.do_std)
+    q_h, k_h, v_h, dO_h = (t.pin_memory() for t in (q_h, k_h, v_h, dO_h))
+    q, k, v, dO = (t.cuda() for t in (q_h, k_h, v_h, dO_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.S), device="cuda", dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(g.gqa_attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.S, w.D), device="cuda", dtype=torch.uint8)
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+    stream = torch.cuda.current_stream()
+
+    def step():
+        g.gqa_attn_fwd(q, k, v, causal=True, scale=w.scale, o=o, lse=lse, stream=stream)
+        g.gqa_attn_bwd(q, k, v, o, dO, lse, causal=True, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                       stream=stream)
+
+    def step_e2e():
+        for dst, src in ((q, q_h), (k, k_h), (v, v_h), (dO, dO_h)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(outs_h, (o, lse, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    fwd_fl, bwd_fl = flops(w.B, w.Hq, w.S, w.D)
+    step_fl = fwd_fl + bwd_fl
+
+    # ---- device-resident timing
+    g.gqa_attn_trace_arm()  # creates the trace events during warm-up
+    for _ in range(args.warmup):
+        step()
+    g.gqa_attn_trace_collect()
+    rc = g.gqa_attn_get_error()
+    if rc != 0:
+        raise RuntimeError(f"warm-up failed: {g.gqa_attn_strerror(rc)}")
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        g.gqa_attn_trace_arm()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        trace = g.gqa_attn_trace_collect()
+    barrier()
+    rc = g.gqa_attn_get_error()
+    if rc != 0:
+        raise RuntimeError(f"timed steps failed: {g.gqa_attn_strerror(rc)}")
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+
+    # ---- end to end: pinned host buffers in, results back to pinned host buffers, every step
+    for _ in range(max(1, args.warmup // 2)):
+        step_e2e()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step_e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, dO_h))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    launches = sum(n for n, _ in trace.values())
+    main_n, main_ms = trace["bwd_main"]
+    fwd_n, fwd_ms = trace["fwd"]
+    main_avg = main_ms / max(main_n, 1)
+    fwd_avg = fwd_ms / max(fwd_n, 1)
+    peak_tf = peaks["bf16_tflops_sustained"]
+    achieved = bwd_fl / (main_avg / 1e3) / 1e12
+    traffic = profiled_traffic("bwd_main", w.name)
+    kernels = {name: {"launches": n, "avg_ms": (t / n if n else None), "share": (t / max(sum(
+        tt for _, tt in trace.values()), 1e-12))} for name, (n, t) in trace.items()}
+
+    line = {
+        "metric": METRIC,
+        "value": world * step_fl / (ms / 1e3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V, N(0,1e-2) dO)",
+        "config": config_of(w),
+        "fwd_tflops": fwd_fl / (fwd_avg / 1e3) / 1e12,
+        "bwd_tflops": bwd_fl / ((ms - fwd_avg) / 1e3) / 1e12,
+        "frac_of_peak": world * step_fl / (ms / 1e3) / 1e12 / (world * peak_tf),
+        "kernels": kernels,
+        "roofline": {"kernel": "bwd_main", "bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 dense, sustained (kernel timed inside back-to-back steps)",
+                     "fwd_kernel": {"achieved": fwd_fl / (fwd_avg / 1e3) / 1e12,
+                                    "frac": fwd_fl / (fwd_avg / 1e3) / 1e12 / peak_tf}},
+        "e2e": {"value": world * step_fl / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        val, desc, cores = cpu_oracle_sample(w)
+        line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

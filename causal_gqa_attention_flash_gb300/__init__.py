@@ -1,0 +1,168 @@
+"""Fused causal grouped-query attention (forward + backward) for GB300, sm_103a.
+
+A thin Python binding over the C ABI of ``libgqa_attn.so`` (declared in
+``include/gqa_attn.h``). Every function here only marshals arguments:
+it checks tensor placement, dtype and shape, allocates outputs with torch
+(device memory and streams are the only things torch provides), and calls
+the entry point of the same name. All arithmetic runs in the library's CUDA
+kernels; if the library is missing, the call raises.
+
+    o, lse = gqa_attn_fwd(q, k, v, causal=True)
+    dq, dk, dv = gqa_attn_bwd(q, k, v, o, dO, lse, causal=True)
+
+Layout is BHSD: q, o, dO, dq are [B, Hq, S, D] bf16; k, v, dk, dv are
+[B, Hkv, S, D] bf16; lse is [B, Hq, S] float32. Query head h reads KV head
+h // (Hq // Hkv).
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+
+__all__ = [
+    "GqaAttnError",
+    "gqa_attn_fwd",
+    "gqa_attn_bwd",
+    "gqa_attn_bwd_workspace_size",
+    "gqa_attn_get_error",
+    "gqa_attn_strerror",
+    "gqa_attn_last_cuda_error",
+    "gqa_attn_selftest_wait_timeout",
+    "gqa_attn_trace_arm",
+    "gqa_attn_trace_collect",
+    "KERNEL_NAMES",
+    "lib_path",
+]
+
+KERNEL_NAMES = ("fwd", "bwd_prep", "bwd_main", "bwd_convert")
+
+GQA_OK = 0
+GQA_ERR_INVALID_ARG = -1
+GQA_ERR_UNSUPPORTED = -2
+GQA_ERR_WORKSPACE_TOO_SMALL = -3
+GQA_ERR_CUDA = -4
+GQA_ERR_TIMEOUT = -5
+
+
+class GqaAttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        msg = gqa_attn_strerror(code)
+        if code == GQA_ERR_CUDA:
+            msg += f" (cudaError {gqa_attn_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [{code}]")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _lib.LIB_PATH
+
+
+def gqa_attn_strerror(code: int) -> str:
+    return _lib.load().gqa_attn_strerror(int(code)).decode()
+
+
+def gqa_attn_last_cuda_error() -> int:
+    return int(_lib.load().gqa_attn_last_cuda_error())
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return int(stream.cuda_stream)
+    return int(stream)
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != GQA_OK:
+        raise GqaAttnError(rc, where)
+
+
+def _dims(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D bfloat16 CUDA tensor (BHSD), got "
+                             f"{t.dtype} {tuple(t.shape)} on {t.device}")
+    B, Hq, S, D = q.shape
+    if k.shape[0] != B or k.shape[2] != S or k.shape[3] != D or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    return B, Hq, k.shape[1], S, D
+
+
+def gqa_attn_fwd(q, k, v, causal: bool = True, scale: float | None = None, o=None, lse=None, stream=None):
+    """Forward: returns (o [B,Hq,S,D] bf16, lse [B,Hq,S] f32). ``scale`` defaults to 1/sqrt(D)."""
+    B, Hq, Hkv, S, D = _dims(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), device=q.device, dtype=torch.float32)
+    rc = _lib.load().gqa_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                  B, Hq, Hkv, S, D, int(bool(causal)), float(scale), _stream_handle(stream))
+    _check(rc, "gqa_attn_fwd")
+    return o, lse
+
+
+def gqa_attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, S: int, D: int) -> int:
+    return int(_lib.load().gqa_attn_bwd_workspace_size(B, Hq, Hkv, S, D))
+
+
+def gqa_attn_bwd(q, k, v, o, dO, lse, causal: bool = True, scale: float | None = None,
+                 dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of sum(o * dO): returns (dq, dk, dv), bf16, shaped like q, k, v.
+
+    ``workspace`` (optional) is a uint8 CUDA tensor of at least
+    ``gqa_attn_bwd_workspace_size(...)`` bytes; one is allocated if omitted.
+    """
+    B, Hq, Hkv, S, D = _dims(q, k, v)
+    for name, t in (("o", o), ("dO", dO)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor shaped like q")
+    if lse.shape != (B, Hq, S) or lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, Hq, S]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = gqa_attn_bwd_workspace_size(B, Hq, Hkv, S, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = _lib.load().gqa_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
+                                  lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                  workspace.data_ptr(), nbytes, B, Hq, Hkv, S, D, int(bool(causal)),
+                                  float(scale), _stream_handle(stream))
+    _check(rc, "gqa_attn_bwd")
+    return dq, dk, dv
+
+
+def gqa_attn_get_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status: 0 or a negative code."""
+    return int(_lib.load().gqa_attn_get_error(_stream_handle(stream)))
+
+
+def gqa_attn_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait nothing ends; it gives up after limit_us)."""
+    _check(_lib.load().gqa_attn_selftest_wait_timeout(int(limit_us), _stream_handle(stream)),
+           "gqa_attn_selftest_wait_timeout")
+
+
+def gqa_attn_trace_arm() -> None:
+    """Arm per-kernel event timing for the following calls on this host thread."""
+    _check(_lib.load().gqa_attn_trace_arm(), "gqa_attn_trace_arm")
+
+
+def gqa_attn_trace_collect() -> dict:
+    """Disarm and return {kernel name: (launches, total ms)} of the calls since arming."""
+    import ctypes
+    n = len(KERNEL_NAMES)
+    launches = (ctypes.c_int * n)()
+    total = (ctypes.c_double * n)()
+    _check(_lib.load().gqa_attn_trace_collect(launches, total), "gqa_attn_trace_collect")
+    return {name: (int(launches[i]), float(total[i])) for i, name in enumerate(KERNEL_NAMES)}

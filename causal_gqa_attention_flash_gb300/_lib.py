@@ -1,0 +1,41 @@
+"""ctypes declarations of libgqa_attn.so (the C ABI in include/gqa_attn.h)."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgqa_attn.so")
+
+_c_int, _c_float, _vp, _sz = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+SIGNATURES = {
+    "gqa_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _vp]),
+    "gqa_attn_bwd_workspace_size": (_sz, [_c_int] * 5),
+    "gqa_attn_bwd": (_c_int, [_vp] * 10 + [_sz] + [_c_int] * 6 + [_c_float, _vp]),
+    "gqa_attn_get_error": (_c_int, [_vp]),
+    "gqa_attn_strerror": (ctypes.c_char_p, [_c_int]),
+    "gqa_attn_last_cuda_error": (_c_int, []),
+    "gqa_attn_selftest_wait_timeout": (_c_int, [_c_int, _vp]),
+    "gqa_attn_trace_arm": (_c_int, []),
+    "gqa_attn_trace_collect": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(ctypes.c_double)]),
+}
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the library once. Raises if it has not been built: there is no fallback."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m causal_gqa_attention_flash_gb300.build` "
+                "(the CUDA library is the only implementation; there is no CPU fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib

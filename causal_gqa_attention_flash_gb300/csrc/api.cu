@@ -1,0 +1,326 @@
+// C ABI of libgqa_attn.so: argument checks, tensor-map construction, the
+// device status word and the kernel launches. The contract of every entry
+// point is stated in include/gqa_attn.h.
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+#include <vector>
+
+#include "../../include/gqa_attn.h"
+#include "common.h"
+#include "ptx.cuh"
+
+// Device status word (one per device that loads the library). Kernels OR
+// STATUS_* bits into it; gqa_attn_get_error() reads and clears it.
+__device__ int g_gqa_status;
+
+namespace gqa {
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+int fail_cuda(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return GQA_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+
+// Address of g_gqa_status on the current device (looked up once per device).
+cudaError_t status_ptr(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_gqa_status);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [nheads, S, D] tensor (D innermost) as a 3-D tiled map with box {inner, 128, 1}.
+cudaError_t encode_3d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int elem_bytes, int D, int S,
+                      int nheads, int box_inner, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)nheads};
+  cuuint64_t strides[2] = {(cuuint64_t)D * elem_bytes, (cuuint64_t)S * D * elem_bytes};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)kTile, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_bf16(CUtensorMap* m, const void* ptr, int D, int S, int nheads) {
+  return encode_3d(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, S, nheads, kChunk, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_common(int B, int Hq, int Hkv, int S, int D, float scale) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1) return GQA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return GQA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
+  const long long tiles = (S + kTile - 1) / kTile;
+  if (tiles > 65535) return GQA_ERR_UNSUPPORTED;
+  if ((long long)B * Hq * tiles >= (1ll << 31) || (long long)B * Hq * (long long)S >= (1ll << 31))
+    return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+// ------------------------------------------------------------------ tracing
+
+struct TraceRec {
+  int kind;
+  cudaEvent_t begin, end;
+};
+thread_local bool t_trace_armed = false;
+thread_local std::vector<TraceRec> t_trace;
+thread_local size_t t_trace_used = 0;
+thread_local int t_trace_error = 0;
+
+}  // namespace
+
+void trace_begin(int kind, cudaStream_t s) {
+  if (!t_trace_armed) return;
+  if (t_trace_used == t_trace.size()) {
+    TraceRec r{kind, nullptr, nullptr};
+    if (cudaEventCreate(&r.begin) != cudaSuccess || cudaEventCreate(&r.end) != cudaSuccess) {
+      t_trace_error = 1;
+      t_trace_armed = false;
+      return;
+    }
+    t_trace.push_back(r);
+  }
+  t_trace[t_trace_used].kind = kind;
+  if (cudaEventRecord(t_trace[t_trace_used].begin, s) != cudaSuccess) t_trace_error = 1;
+}
+
+void trace_end(int kind, cudaStream_t s) {
+  if (!t_trace_armed) return;
+  (void)kind;
+  if (cudaEventRecord(t_trace[t_trace_used].end, s) != cudaSuccess) t_trace_error = 1;
+  ++t_trace_used;
+}
+
+}  // namespace gqa
+
+using namespace gqa;
+
+extern "C" {
+
+int gqa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
+                 int D, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse) return GQA_ERR_INVALID_ARG;
+  int rc = check_common(B, Hq, Hkv, S, D, scale);
+  if (rc != GQA_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return GQA_ERR_INVALID_ARG;
+  CUtensorMap mq, mk, mv;
+  cudaError_t e;
+  if ((e = encode_bf16(&mq, q, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mk, k, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mv, v, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
+  int* status = nullptr;
+  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  FwdArgs a;
+  a.map_q = &mq;
+  a.map_k = &mk;
+  a.map_v = &mv;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.S = S;
+  a.D = D;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  a.status = status;
+  if ((e = launch_fwd(a, static_cast<cudaStream_t>(stream))) != cudaSuccess) return fail_cuda(e);
+  return GQA_OK;
+}
+
+size_t gqa_attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D) {
+  if (check_common(B, Hq, Hkv, S, D, 1.0f) != GQA_OK) return 0;
+  return bwd_workspace_layout(B, Hq, S, D).total;
+}
+
+int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S,
+                 int D, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace) return GQA_ERR_INVALID_ARG;
+  int rc = check_common(B, Hq, Hkv, S, D, scale);
+  if (rc != GQA_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
+    return GQA_ERR_INVALID_ARG;
+  const BwdWorkspace ws = bwd_workspace_layout(B, Hq, S, D);
+  if (workspace_bytes < ws.total) return GQA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  CUtensorMap mq, mk, mv, mdo, macc;
+  cudaError_t e;
+  if ((e = encode_bf16(&mq, q, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mk, k, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mv, v, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mdo, dO, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_3d(&macc, wsb + ws.dqacc_off, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, S, B * Hq, 32,
+                     CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return fail_cuda(e);
+  int* status = nullptr;
+  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  BwdArgs a;
+  a.map_q = &mq;
+  a.map_k = &mk;
+  a.map_v = &mv;
+  a.map_do = &mdo;
+  a.map_dqacc = &macc;
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dvec = reinterpret_cast<float*>(wsb + ws.dvec_off);
+  a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
+  a.dq_acc = reinterpret_cast<float*>(wsb + ws.dqacc_off);
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.S = S;
+  a.D = D;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  a.status = status;
+  if ((e = launch_bwd(a, static_cast<cudaStream_t>(stream))) != cudaSuccess) return fail_cuda(e);
+  return GQA_OK;
+}
+
+int gqa_attn_get_error(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  int* status = nullptr;
+  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  int h = 0;
+  if ((e = cudaMemcpyAsync(&h, status, sizeof(int), cudaMemcpyDeviceToHost, s)) != cudaSuccess) return fail_cuda(e);
+  if ((e = cudaMemsetAsync(status, 0, sizeof(int), s)) != cudaSuccess) return fail_cuda(e);
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail_cuda(e);
+  if (h & STATUS_TIMEOUT) return GQA_ERR_TIMEOUT;
+  return GQA_OK;
+}
+
+const char* gqa_attn_strerror(int code) {
+  switch (code) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID_ARG: return "invalid argument";
+    case GQA_ERR_UNSUPPORTED: return "unsupported size (D must be 64 or 128; sizes within index range)";
+    case GQA_ERR_WORKSPACE_TOO_SMALL: return "backward workspace too small";
+    case GQA_ERR_CUDA: return "CUDA error";
+    case GQA_ERR_TIMEOUT: return "device-side wait exceeded its time limit";
+    default: return "unknown error code";
+  }
+}
+
+int gqa_attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gqa_attn_trace_arm(void) {
+  t_trace_armed = true;
+  t_trace_used = 0;
+  t_trace_error = 0;
+  return GQA_OK;
+}
+
+int gqa_attn_trace_collect(int* launches, double* total_ms) {
+  if (!launches || !total_ms) return GQA_ERR_INVALID_ARG;
+  t_trace_armed = false;
+  for (int k = 0; k < kKernelCount; ++k) {
+    launches[k] = 0;
+    total_ms[k] = 0.0;
+  }
+  if (t_trace_error) return GQA_ERR_CUDA;
+  for (size_t i = 0; i < t_trace_used; ++i) {
+    const TraceRec& r = t_trace[i];
+    cudaError_t e = cudaEventSynchronize(r.end);
+    if (e != cudaSuccess) return fail_cuda(e);
+    float ms = 0.f;
+    if ((e = cudaEventElapsedTime(&ms, r.begin, r.end)) != cudaSuccess) return fail_cuda(e);
+    launches[r.kind] += 1;
+    total_ms[r.kind] += ms;
+  }
+  t_trace_used = 0;
+  return GQA_OK;
+}
+
+int gqa_attn_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return GQA_ERR_INVALID_ARG;
+  int* status = nullptr;
+  cudaError_t e;
+  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  if ((e = launch_wait_selftest(status, (uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream))) !=
+      cudaSuccess)
+    return fail_cuda(e);
+  return GQA_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ bounded-wait self-test
+
+namespace gqa {
+namespace {
+
+// One block: thread 0 initialises an mbarrier that expects one arrival nobody
+// makes, then waits on it with the ordinary bounded wait. The wait gives up
+// after limit_ns, sets the TIMEOUT bit and the kernel returns.
+__global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitGuard wg{&abort_flag, status, limit_ns};
+    (void)mbar_wait(&bar, 0, wg);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

@@ -1,0 +1,525 @@
+// Backward of fused causal grouped-query attention on sm_103a.
+//
+// The gradient of a comprehension is itself a comprehension, so the backward
+// writes no S x S intermediate either (aiinsiders.net, "A compiler that
+// derives GPU kernels matches hand-tuned code"); every contraction
+// accumulates in f32 (the same article reports a bf16-accumulating fused
+// backward failing the f32 tolerance). Three kernels on one stream:
+//
+//   bwd_prep      D_i = sum_d dO_id O_id (f32), LSE_i * log2(e) (+inf past S),
+//                 and a zeroed f32 dQ accumulator;                    HBM-bound
+//   bwd_main      one CTA per (batch, KV head, 128-key tile). For every query
+//                 head of the group and every query tile that can see the key
+//                 tile it recomputes S^T = K Q^T, P^T = exp2(S^T c - LSE2),
+//                 dP^T = V dO^T, dS^T = P^T (dP^T - D), and accumulates
+//                 dV += P^T dO and dK += dS^T Q in TMEM (so the GQA reduction
+//                 over the group happens inside the CTA, in a fixed order:
+//                 dK/dV are deterministic), and dQ_i += dS K by a TMA
+//                 reduce-add of the f32 partial into the accumulator;
+//   bwd_convert   dQ = bf16(scale * accumulator);                     HBM-bound
+//
+// bwd_main warp roles: warp 4 = TMA producer, warp 5 = MMA issuer, warps 0..3
+// = element-wise work, thread r owning TMEM lane r (key row r for S^T, dP^T,
+// dK, dV; query row r for the dQ partial).
+// TMEM columns: [0,128) S^T f32, then P^T bf16 in [0,64) and dS^T bf16 in
+// [64,128); [128,256) dP^T f32, then the dQ partial f32 [128, 128+D);
+// [256,256+D) dV; [384,384+D) dK.
+#include "common.h"
+#include "ptx.cuh"
+
+namespace gqa {
+namespace {
+
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ prep
+
+// One group of D/8 threads per row: each thread reads 8 bf16 of dO and of O.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dO,
+                                                       const float* __restrict__ lse, float* __restrict__ dvec,
+                                                       float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                       int rows_total, int S, int S_pad, float log2e,
+                                                       long long acc_vec4) {
+  constexpr int TPR = D / 8;            // threads per row
+  constexpr int RPW = 32 / TPR;          // rows per warp and iteration
+  const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int nthreads = gridDim.x * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % TPR;
+  // Rows of the padded [B*Hq, S_pad] arrays; the loop bound is warp-uniform so
+  // that every lane takes part in the shuffles.
+  for (int r0 = (gtid >> 5) * RPW; r0 < rows_total; r0 += (nthreads >> 5) * RPW) {
+    const int r = r0 + lane / TPR;
+    const int bh = r / S_pad;
+    const int s = r - bh * S_pad;
+    const bool live = r < rows_total;
+    float acc = 0.f;
+    if (live && s < S) {
+      const size_t base = ((size_t)bh * S + s) * D + sub * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(o + base);
+      const uint4 b = *reinterpret_cast<const uint4*>(dO + base);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), acc);
+        acc = fmaf(__uint_as_float(aw[i] & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u), acc);
+      }
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
+    if (live && sub == 0) {
+      dvec[r] = acc;
+      lse2[r] = (s < S) ? lse[(size_t)bh * S + s] * log2e : INFINITY;
+    }
+  }
+  float4* acc4 = reinterpret_cast<float4*>(dq_acc);
+  for (long long i = gtid; i < acc_vec4; i += nthreads) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------ convert
+
+__global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq,
+                                                          long long n8, float scale) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+    uint4 w;
+    w.x = pack_bf16(a.x * scale, a.y * scale);
+    w.y = pack_bf16(a.z * scale, a.w * scale);
+    w.z = pack_bf16(b.x * scale, b.y * scale);
+    w.w = pack_bf16(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4*>(dq)[i] = w;
+  }
+}
+
+// ------------------------------------------------------------------ main
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kChunks = D / kChunk;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStages = (D == 64) ? 2 : 1;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kTileBytes;
+  static constexpr int kQOff = kVOff + kTileBytes;
+  static constexpr int kDOOff = kQOff + kStages * kTileBytes;
+  static constexpr int kDSOff = kDOOff + kStages * kTileBytes;         // dS bf16 [128 kv][128 q], MN-major
+  static constexpr int kDSBytes = kTile * kTile * 2;
+  static constexpr int kStgOff = kDSOff + kDSBytes;                    // 2 x f32 [128][32] dQ staging (128B swizzle)
+  static constexpr int kStgBytes = kTile * 32 * 4;
+  static constexpr int kRowOff = kStgOff + 2 * kStgBytes;              // per stage: lse2[128], dvec[128]
+  static constexpr int kBarOff = kRowOff + kStages * 2 * kTile * 4;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static constexpr int kThreads = 192;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSPCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 384;
+};
+
+template <int ST>
+struct BwdBars {
+  uint64_t kv_full;
+  uint64_t qdo_full[ST];
+  uint64_t qdo_empty[ST];
+  uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free, dkv_done, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct BwdKParams {
+  const float* lse2;
+  const float* dvec;
+  uint16_t* dk;
+  uint16_t* dv;
+  int Hq, Hkv, S, S_pad, causal, n_tiles;
+  float scale, scale_log2;
+  int* status;
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                    const __grid_constant__ CUtensorMap map_acc, const BwdKParams p) {
+  using C = BwdCfg<D>;
+  constexpr int ST = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  auto* bars = reinterpret_cast<BwdBars<ST>*>(smem + C::kBarOff);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int kvh = blockIdx.x;  // b * Hkv + hkv
+  const int jt = blockIdx.y;   // key tile; tile 0 sees the most query tiles when causal
+  const int G = p.Hq / p.Hkv;
+  const int b = kvh / p.Hkv;
+  const int hkv = kvh - b * p.Hkv;
+  const int bhq0 = b * p.Hq + hkv * G;  // first query head of the group
+  const int i_start = p.causal ? jt : 0;
+  const int n_i = p.n_tiles - i_start;
+  const int n_steps = G * n_i;
+  const WaitGuard wg{&bars->abort_flag, p.status, kWaitLimitNs};
+
+  if (tid == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&bars->qdo_full[s], 1);
+      mbar_init(&bars->qdo_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->ds_full, 128);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->dkv_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      tma_prefetch_desc(&map_do);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_3d(smem + C::kKOff + c * kBoxBytes, &map_k, &bars->kv_full, c * kChunk, jt * kTile, kvh);
+        tma_load_3d(smem + C::kVOff + c * kBoxBytes, &map_v, &bars->kv_full, c * kChunk, jt * kTile, kvh);
+      }
+      int issued = 0;
+      for (int t = 0; t < n_steps; ++t) {
+        const int st = t % ST;
+        const int use = t / ST;
+        if (use > 0 && !mbar_wait(&bars->qdo_empty[st], (use - 1) & 1, wg)) break;
+        const int hl = t / n_i;
+        const int i = i_start + (t - hl * n_i);
+        const int bhq = bhq0 + hl;
+        uint64_t* bar = &bars->qdo_full[st];
+        mbar_arrive_expect_tx(bar, 2 * C::kTileBytes + 2 * kTile * 4);
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(smem + C::kQOff + st * C::kTileBytes + c * kBoxBytes, &map_q, bar, c * kChunk, i * kTile, bhq);
+          tma_load_3d(smem + C::kDOOff + st * C::kTileBytes + c * kBoxBytes, &map_do, bar, c * kChunk, i * kTile,
+                      bhq);
+        }
+        float* srow = reinterpret_cast<float*>(smem + C::kRowOff) + st * 2 * kTile;
+        const size_t roff = (size_t)bhq * p.S_pad + (size_t)i * kTile;
+        bulk_load(srow, p.lse2 + roff, kTile * 4, bar);
+        bulk_load(srow + kTile, p.dvec + roff, kTile * 4, bar);
+        issued = t + 1;
+      }
+      if (bars->abort_flag) {
+        mbar_wait_drain(&bars->kv_full, 0, kWaitLimitNs);
+        for (int t = (issued > ST ? issued - ST : 0); t < issued; ++t)
+          mbar_wait_drain(&bars->qdo_full[t % ST], (t / ST) & 1, kWaitLimitNs);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_kk = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both operands K-major
+      constexpr uint32_t idesc_tb = idesc_bf16(128, D, false, true);     // dV, dK: A in TMEM, B MN-major
+      constexpr uint32_t idesc_mm = idesc_bf16(128, D, true, true);      // dQ: A and B MN-major
+      const uint32_t k_addr = smem_addr(smem + C::kKOff);
+      const uint32_t v_addr = smem_addr(smem + C::kVOff);
+      const uint32_t ds_addr = smem_addr(smem + C::kDSOff);
+      bool ok = mbar_wait(&bars->kv_full, 0, wg);
+      for (int t = 0; ok && t < n_steps; ++t) {
+        const int st = t % ST;
+        if (!(ok = mbar_wait(&bars->qdo_full[st], (t / ST) & 1, wg))) break;
+        if (t > 0 && !(ok = mbar_wait(&bars->dq_free, (t - 1) & 1, wg))) break;
+        tc_fence_after();
+        const uint32_t q_addr = smem_addr(smem + C::kQOff + st * C::kTileBytes);
+        const uint32_t do_addr = smem_addr(smem + C::kDOOff + st * C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
+          umma_ss(tbase + C::kSPCol, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
+                  idesc_kk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->s_full);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
+          umma_ss(tbase + C::kDPCol, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
+                  idesc_kk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->dp_full);
+        if (!(ok = mbar_wait(&bars->p_full, t & 1, wg))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(tbase + C::kDVCol, tbase + C::kSPCol + (uint32_t)kk * 8u,
+                  sdesc_sw128(do_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_tb, (t > 0 || kk > 0) ? 1u : 0u);
+        if (!(ok = mbar_wait(&bars->ds_full, t & 1, wg))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(tbase + C::kDKCol, tbase + C::kSPCol + 64u + (uint32_t)kk * 8u,
+                  sdesc_sw128(q_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_tb, (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ss(tbase + C::kDPCol, sdesc_sw128(ds_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024),
+                  sdesc_sw128(k_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_mm, kk > 0 ? 1u : 0u);
+        umma_commit(&bars->dq_full);
+        umma_commit(&bars->qdo_empty[st]);
+      }
+      umma_commit(&bars->dkv_done);
+      umma_commit(&bars->drain);
+      mbar_wait_drain(&bars->drain, 0, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise warps 0..3
+    const int row = tid;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t sp_tmem = tbase + lane_off + C::kSPCol;
+    const uint32_t dp_tmem = tbase + lane_off + C::kDPCol;
+    const float c = p.scale_log2;
+    const int kv_row = jt * kTile + row;
+    const bool kv_valid = kv_row < p.S;
+    uint8_t* sds = smem + C::kDSOff;
+    float* stg = reinterpret_cast<float*>(smem + C::kStgOff);
+    bool ok = true;
+    int stg_i = 0;
+    for (int t = 0; t < n_steps; ++t) {
+      const int st = t % ST;
+      const int hl = t / n_i;
+      const int i = i_start + (t - hl * n_i);
+      const int bhq = bhq0 + hl;
+      const float* slse = reinterpret_cast<const float*>(smem + C::kRowOff) + st * 2 * kTile;
+      const float* sdv = slse + kTile;
+      // visible iff key (jt*128 + row) <= query (i*128 + col): on the diagonal tile, col >= row
+      const int first_visible = (p.causal && i == jt) ? row : 0;
+
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, t & 1, wg));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t r[128];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        tmem_ld_32x32b_x32(sp_tmem + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * q]));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[32 * q]));
+      float P[128];
+#pragma unroll
+      for (int col = 0; col < 128; ++col) {
+        const float e = ex2_approx(fmaf(__uint_as_float(r[col]), c, -slse[col]));
+        P[col] = (kv_valid && col >= first_visible) ? e : 0.f;
+      }
+      {
+        uint32_t pk[64];
+#pragma unroll
+        for (int x = 0; x < 64; ++x) pk[x] = pack_bf16(P[2 * x], P[2 * x + 1]);
+        tmem_st_32x32b_x32(sp_tmem + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st_32x32b_x32(sp_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->dp_full, t & 1, wg));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t d[32];
+        tmem_ld_32x32b_x32(dp_tmem + q * 32, d);
+        tmem_wait_ld_x32(d);
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int c0 = q * 32 + 2 * x;
+          const float ds0 = P[c0] * (__uint_as_float(d[2 * x]) - sdv[c0]);
+          const float ds1 = P[c0 + 1] * (__uint_as_float(d[2 * x + 1]) - sdv[c0 + 1]);
+          pk[x] = pack_bf16(ds0, ds1);
+        }
+        tmem_st_32x32b_x16(sp_tmem + 64 + q * 16, pk);
+        // dS[row = key][col = query] into the MN-major (query-contiguous) 128B-swizzled tile.
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int qc = q * 32 + u * 8;  // first query column of this 16-byte unit
+          const int unit = (qc & 63) >> 3;
+          uint8_t* dst = sds + (qc >> 6) * kBoxBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((unit ^ (row & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_full);
+
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, t & 1, wg));
+      if (!ok) break;
+      tc_fence_after();
+      // dQ partial: TMEM lane = query row. Staged in 32-column f32 slices, reduce-added by TMA.
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t d[32];
+        tmem_ld_32x32b_x32(dp_tmem + q * 32, d);
+        tmem_wait_ld_x32(d);
+        float* buf = stg + (stg_i & 1) * (kTile * 32);
+        if (tid == 0) bulk_wait_group_read<1>();
+        named_barrier_sync(1, 128);
+        // 128-byte swizzled slice (the accumulator map's swizzle): 16-byte unit u of row r
+        // sits at position u ^ (r % 8), so 8 consecutive rows hit distinct banks.
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          *reinterpret_cast<float4*>(buf + row * 32 + ((u ^ (row & 7)) << 2)) =
+              make_float4(__uint_as_float(d[4 * u]), __uint_as_float(d[4 * u + 1]), __uint_as_float(d[4 * u + 2]),
+                          __uint_as_float(d[4 * u + 3]));
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (tid == 0) {
+          tma_reduce_add_3d(&map_acc, buf, q * 32, i * kTile, bhq);
+          bulk_commit_group();
+        }
+        ++stg_i;
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);
+    }
+    if (tid == 0) bulk_wait_group<0>();
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->dkv_done, 0, wg));
+    if (ok) {
+      tc_fence_after();
+      const size_t orow = ((size_t)kvh * p.S + kv_row) * D;
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t d[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kDVCol + q * 32, d);
+        tmem_wait_ld_x32(d);
+        uint32_t w[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) w[x] = pack_bf16(__uint_as_float(d[2 * x]), __uint_as_float(d[2 * x + 1]));
+        if (kv_valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dv + orow + q * 32);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t d[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kDKCol + q * 32, d);
+        tmem_wait_ld_x32(d);
+        uint32_t w[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          w[x] = pack_bf16(__uint_as_float(d[2 * x]) * p.scale, __uint_as_float(d[2 * x + 1]) * p.scale);
+        if (kv_valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dk + orow + q * 32);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::kTmemCols);
+  }
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
+                                                  cudaSuccess)
+      n = v;
+    else
+      n = 148;
+  }
+  return n;
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const int n_tiles = ceil_div(a.S, kTile);
+  const int S_pad = n_tiles * kTile;
+  const int rows_total = a.B * a.Hq * S_pad;
+  const long long acc_elems = (long long)a.B * a.Hq * a.S * D;
+  const int sms = num_sms();
+  {
+    const int threads = 256;
+    long long want = ((long long)rows_total * (D / 8) + threads - 1) / threads;
+    const int blocks = (int)(want < (long long)sms * 8 ? (want < 1 ? 1 : want) : (long long)sms * 8);
+    trace_begin(kKernelBwdPrep, stream);
+    bwd_prep_kernel<D><<<blocks, threads, 0, stream>>>(
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse, a.dvec, a.lse2, a.dq_acc,
+        rows_total, a.S, S_pad, 1.4426950408889634f, acc_elems / 4);
+    cudaError_t e = cudaGetLastError();
+    trace_end(kKernelBwdPrep, stream);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    BwdKParams p;
+    p.lse2 = a.lse2;
+    p.dvec = a.dvec;
+    p.dk = static_cast<uint16_t*>(a.dk);
+    p.dv = static_cast<uint16_t*>(a.dv);
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.S = a.S;
+    p.S_pad = S_pad;
+    p.causal = a.causal;
+    p.n_tiles = n_tiles;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale_log2;
+    p.status = a.status;
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(a.B * a.Hkv), (unsigned)n_tiles);
+    trace_begin(kKernelBwdMain, stream);
+    bwd_main_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_do,
+                                                                     *a.map_dqacc, p);
+    e = cudaGetLastError();
+    trace_end(kKernelBwdMain, stream);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const long long n8 = acc_elems / 8;
+    const int threads = 256;
+    long long want = (n8 + threads - 1) / threads;
+    const int blocks = (int)(want < (long long)sms * 8 ? (want < 1 ? 1 : want) : (long long)sms * 8);
+    trace_begin(kKernelBwdConvert, stream);
+    bwd_convert_kernel<<<blocks, threads, 0, stream>>>(a.dq_acc, static_cast<uint16_t*>(a.dq), n8, a.scale);
+    cudaError_t e = cudaGetLastError();
+    trace_end(kKernelBwdConvert, stream);
+    return e;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+  if (a.D == 64) return launch_bwd_d<64>(a, stream);
+  return launch_bwd_d<128>(a, stream);
+}
+
+}  // namespace gqa

@@ -1,0 +1,81 @@
+// Definitions shared by the kernels and the host-side launchers of libgqa_attn.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace gqa {
+
+// Tile edge along the sequence for queries and keys (one tcgen05 M=128 tile).
+constexpr int kTile = 128;
+// Columns of one 128-byte swizzle row of bf16 (the TMA box's inner extent).
+constexpr int kChunk = 64;
+// Bytes of one [128 rows x 64 bf16] swizzled box.
+constexpr int kBoxBytes = kTile * kChunk * 2;
+
+// Time limit of one device-side wait before the kernel gives up (ns).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+struct FwdArgs {
+  const CUtensorMap* map_q;  // [B*Hq, S, D] bf16, box {64, 128, 1}, 128B swizzle
+  const CUtensorMap* map_k;  // [B*Hkv, S, D]
+  const CUtensorMap* map_v;
+  void* o;                   // bf16 [B, Hq, S, D]
+  float* lse;                // f32 [B, Hq, S]
+  int B, Hq, Hkv, S, D, causal;
+  float scale_log2;          // scale * log2(e)
+  int* status;               // device status word
+};
+
+struct BwdArgs {
+  const CUtensorMap* map_q;    // [B*Hq, S, D] bf16
+  const CUtensorMap* map_k;    // [B*Hkv, S, D] bf16
+  const CUtensorMap* map_v;
+  const CUtensorMap* map_do;   // [B*Hq, S, D] bf16
+  const CUtensorMap* map_dqacc;// [B*Hq, S, D] f32, box {32, 128, 1}, 128B swizzle
+  const void* o;               // bf16 [B, Hq, S, D]
+  const void* dO;              // bf16 [B, Hq, S, D]
+  const float* lse;            // f32 [B, Hq, S]
+  void* dq;                    // bf16 [B, Hq, S, D]
+  void* dk;                    // bf16 [B, Hkv, S, D]
+  void* dv;
+  float* dvec;                 // f32 [B*Hq, S_pad]: D_i = rowsum(dO * O)
+  float* lse2;                 // f32 [B*Hq, S_pad]: LSE * log2(e), +inf past S
+  float* dq_acc;               // f32 [B*Hq, S, D]
+  int B, Hq, Hkv, S, D, causal;
+  float scale, scale_log2;
+  int* status;
+};
+
+// Workspace sections of the backward (byte offsets, each 256-aligned).
+struct BwdWorkspace {
+  size_t dvec_off, lse2_off, dqacc_off, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline BwdWorkspace bwd_workspace_layout(int B, int Hq, int S, int D) {
+  BwdWorkspace w;
+  const size_t rows_pad = (size_t)B * Hq * (size_t)ceil_div(S, kTile) * kTile;
+  w.dvec_off = 0;
+  w.lse2_off = align256(w.dvec_off + rows_pad * sizeof(float));
+  w.dqacc_off = align256(w.lse2_off + rows_pad * sizeof(float));
+  w.total = align256(w.dqacc_off + (size_t)B * Hq * S * D * sizeof(float));
+  return w;
+}
+
+// Tracing hooks (api.cu): no-ops unless the calling host thread armed tracing.
+enum KernelKind { kKernelFwd = 0, kKernelBwdPrep = 1, kKernelBwdMain = 2, kKernelBwdConvert = 3, kKernelCount = 4 };
+void trace_begin(int kind, cudaStream_t s);
+void trace_end(int kind, cudaStream_t s);
+
+// Host launchers (fwd.cu, bwd.cu). Return a cudaError_t.
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace gqa

@@ -1,0 +1,150 @@
+/*
+ * gqa_attn.h -- C ABI of libgqa_attn.so: fused causal grouped-query attention,
+ * forward and backward, for NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes
+ *   Attention as the tang page states it ("How tang works", section 3,
+ *   "Optimizations are derived, not written", equations (5)-(6)): the row
+ *   softmax of scale * Q K^T over the visible keys, applied to V, evaluated
+ *   as the streaming reduction whose three running values (row max m, sum l,
+ *   accumulator) form an associative combine, so that no S x S score matrix
+ *   is ever written. Grouped-query heads as in the RustingBrain docs ("GQA
+ *   12/4 heads", ".heads(8, 2, 64)"): Hq query heads share Hkv key/value
+ *   heads, query head h reads KV head h / (Hq / Hkv). The backward is the
+ *   gradient of sum(O * dO), itself a comprehension with no S x S
+ *   intermediates (aiinsiders.net, "A compiler that derives GPU kernels
+ *   matches hand-tuned code"), with f32 accumulation throughout (the same
+ *   article reports a bf16-accumulating fused backward missing the f32
+ *   tolerance).
+ *
+ * Layout (every tensor dense, row-major, "BHSD"):
+ *   q, o, dO, dq : bf16 [B, Hq,  S, D]
+ *   k, v, dk, dv : bf16 [B, Hkv, S, D]
+ *   lse          : f32  [B, Hq,  S]      natural-log log-sum-exp of the scaled scores
+ * Every pointer is a DEVICE pointer, 16-byte aligned (TMA requirement).
+ * Causal: key j is visible to query i iff j <= i (queries and keys share the
+ * length S). causal = 0 makes every key visible.
+ * Supported: D in {64, 128}; any S >= 1; B, Hq, Hkv >= 1 with Hq % Hkv == 0;
+ * B * Hq * ceil(S / 128) and B * Hkv * ceil(S / 128) below 2^31.
+ *
+ * Ownership: the caller allocates and owns every buffer (device memory and
+ * the stream). The library never allocates or frees device memory and never
+ * synchronises the stream, except gqa_attn_get_error(). All work is enqueued
+ * on `stream` (a cudaStream_t; NULL means the legacy default stream) and runs
+ * asynchronously with respect to the host.
+ *
+ * Errors: every entry point returns GQA_OK (0) or a negative code. Invalid
+ * arguments are rejected on the host before anything is enqueued. A CUDA
+ * launch failure returns GQA_ERR_CUDA (the CUDA error code is kept, per host
+ * thread, for gqa_attn_last_cuda_error()). A device-side wait that exceeds
+ * its time limit makes the kernel give up cleanly and sets a device status
+ * bit that gqa_attn_get_error() reports as GQA_ERR_TIMEOUT. There is no CPU
+ * fallback of any kind: a failure is an error code.
+ *
+ * Thread safety: entry points may be called concurrently from several host
+ * threads. The device status word is shared by every call on a device.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQA_OK 0
+#define GQA_ERR_INVALID_ARG (-1)         /* null/misaligned pointer, bad size, Hq % Hkv != 0, scale not finite */
+#define GQA_ERR_UNSUPPORTED (-2)         /* D not in {64, 128}, sizes beyond the index range */
+#define GQA_ERR_WORKSPACE_TOO_SMALL (-3) /* backward workspace smaller than gqa_attn_bwd_workspace_size() */
+#define GQA_ERR_CUDA (-4)                /* a CUDA runtime/driver call failed; see gqa_attn_last_cuda_error() */
+#define GQA_ERR_TIMEOUT (-5)             /* a device-side wait gave up (reported by gqa_attn_get_error) */
+
+/*
+ * Forward: O = softmax(scale * Q K^T + causal mask) V and LSE per query row.
+ *   q [B,Hq,S,D], k, v [B,Hkv,S,D] (inputs, bf16, device)
+ *   o [B,Hq,S,D] (output, bf16, device), lse [B,Hq,S] (output, f32, device;
+ *   lse = ln sum_j exp(scale * q_i . k_j) over the visible keys)
+ *   scale: multiplies the scores (usually 1/sqrt(D)); must be finite and >= 0.
+ * Passage: tang, "How tang works" section 3, equations (5)-(6) (attention as
+ * written vs. the derived streaming reduction: same answer, no score matrix).
+ */
+int gqa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
+                 int D, int causal, float scale, void* stream);
+
+/*
+ * Size in bytes of the device workspace gqa_attn_bwd needs (256-byte aligned
+ * sections: the per-row D = rowsum(dO * O) and the scaled LSE, f32
+ * [B,Hq,ceil(S/128)*128] each, and the f32 dQ accumulator [B,Hq,S,D]).
+ * Returns 0 for arguments gqa_attn_bwd would reject.
+ */
+size_t gqa_attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D);
+
+/*
+ * Backward of gqa_attn_fwd for the loss sum(O * dO).
+ *   q, k, v, o, dO (bf16, device) and lse (f32, device) as produced/consumed by
+ *   gqa_attn_fwd with the same causal and scale;
+ *   dq [B,Hq,S,D], dk, dv [B,Hkv,S,D] (outputs, bf16, device). dk and dv are
+ *   summed over the Hq/Hkv query heads that share each KV head; they are
+ *   bitwise deterministic. dq is accumulated in f32 by reduce-add, so its
+ *   last bits may differ between runs.
+ *   workspace: device memory of at least gqa_attn_bwd_workspace_size() bytes,
+ *   256-byte aligned, owned by the caller, not read before being written; it
+ *   may be reused once the stream has passed this call.
+ * Steps: D = rowsum(dO * O); recompute P from Q, K and LSE; dV = P^T dO;
+ * dP = dO V^T; dS = P * (dP - D); dK = scale dS^T Q; dQ = scale dS K.
+ * Passage: aiinsiders.net, "A compiler that derives GPU kernels matches
+ * hand-tuned code" (the gradient through a comprehension is a comprehension;
+ * the fused backward must meet the f32 tolerance).
+ */
+int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S,
+                 int D, int causal, float scale, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device. Returns GQA_OK, GQA_ERR_TIMEOUT if a kernel gave up on a
+ * wait since the last call, or GQA_ERR_CUDA if the stream reports an error.
+ */
+int gqa_attn_get_error(void* stream);
+
+/* Static, human-readable text of an error code. Never NULL. */
+const char* gqa_attn_strerror(int code);
+
+/* The CUDA error code behind the last GQA_ERR_CUDA returned on this host thread (0 if none). */
+int gqa_attn_last_cuda_error(void);
+
+/*
+ * Self-test of the bounded device wait (no counterpart on the pages): launches
+ * one block that waits on an mbarrier nothing ever arrives at, with a limit of
+ * limit_us microseconds (1..10^6). The kernel gives up, records the TIMEOUT
+ * status bit and returns; a following gqa_attn_get_error() reports
+ * GQA_ERR_TIMEOUT. It faults, traps or hangs nothing.
+ */
+int gqa_attn_selftest_wait_timeout(int limit_us, void* stream);
+
+/*
+ * Per-kernel tracing (no counterpart on the pages; used to time each kernel
+ * of a call live, e.g. for a roofline). gqa_attn_trace_arm() arms the calling
+ * host thread: every kernel that gqa_attn_fwd / gqa_attn_bwd then launch from
+ * this thread is bracketed by two CUDA events recorded on the call's stream.
+ * gqa_attn_trace_collect() disarms, waits for the last recorded event, and
+ * writes, for each kernel kind k (GQA_KERNEL_*), launches[k] and total_ms[k]
+ * (arrays of GQA_KERNEL_COUNT entries, host memory, owned by the caller).
+ * Events are created on first use on the device current at that time and
+ * reused afterwards; no device memory is allocated.
+ */
+#define GQA_KERNEL_FWD 0
+#define GQA_KERNEL_BWD_PREP 1
+#define GQA_KERNEL_BWD_MAIN 2
+#define GQA_KERNEL_BWD_CONVERT 3
+#define GQA_KERNEL_COUNT 4
+int gqa_attn_trace_arm(void);
+int gqa_attn_trace_collect(int* launches, double* total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

@@ -1,0 +1,89 @@
+"""The C ABI without a GPU: the library builds, loads, exports every declared entry point,
+and rejects bad arguments on the host before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa_attn.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_attn_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from causal_gqa_attention_flash_gb300.build import build_library
+    from causal_gqa_attention_flash_gb300 import _lib
+    build_library()
+    return _lib.load()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("gqa_attn_fwd", "gqa_attn_bwd", "gqa_attn_bwd_workspace_size", "gqa_attn_get_error",
+              "gqa_attn_strerror"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in gqa_attn.h but not exported"
+
+
+def test_binding_declares_every_symbol():
+    from causal_gqa_attention_flash_gb300 import _lib
+    assert sorted(_lib.SIGNATURES) == _declared_functions()
+
+
+def test_strerror_and_workspace_size(lib):
+    for code in (0, -1, -2, -3, -4, -5, -99):
+        assert isinstance(lib.gqa_attn_strerror(code), bytes)
+    assert lib.gqa_attn_bwd_workspace_size(1, 4, 2, 128, 96) == 0
+    assert lib.gqa_attn_bwd_workspace_size(1, 4, 3, 128, 64) == 0
+    n = lib.gqa_attn_bwd_workspace_size(2, 32, 8, 16384, 128)
+    # D and LSE2 rows (f32, padded to 128) + f32 dQ accumulator, 256-byte aligned sections
+    assert n == 2 * 2 * 32 * 16384 * 4 + 2 * 32 * 16384 * 128 * 4
+    n = lib.gqa_attn_bwd_workspace_size(1, 4, 2, 130, 64)
+    rows_pad = 4 * 256
+    assert n >= 2 * rows_pad * 4 + 4 * 130 * 64 * 4 and n % 256 == 0
+
+
+def test_host_argument_checks_need_no_gpu(lib):
+    """Arguments the host rejects return their code before any CUDA call (fake aligned addresses)."""
+    A = 1 << 20  # an aligned, never-dereferenced address
+    assert lib.gqa_attn_fwd(None, A, A, A, A, 1, 4, 2, 128, 64, 1, 0.125, None) == -1
+    assert lib.gqa_attn_fwd(A, A, A, A, A, 1, 4, 3, 128, 64, 1, 0.125, None) == -1
+    assert lib.gqa_attn_fwd(A, A, A, A, A, 1, 4, 2, 128, 80, 1, 0.125, None) == -2
+    assert lib.gqa_attn_fwd(A + 8, A, A, A, A, 1, 4, 2, 128, 64, 1, 0.125, None) == -1
+    assert lib.gqa_attn_fwd(A, A, A, A, A, 1, 4, 2, 128, 64, 1, float("inf"), None) == -1
+    assert lib.gqa_attn_fwd(A, A, A, A, A, 0, 4, 2, 128, 64, 1, 0.125, None) == -1
+    assert lib.gqa_attn_fwd(A, A, A, A, A, 1, 4, 2, 128 * 65536, 64, 1, 0.125, None) == -2
+    args = [A] * 10
+    assert lib.gqa_attn_bwd(*args, 0, 1, 4, 2, 128, 64, 1, 0.125, None) == -3
+    assert lib.gqa_attn_bwd(*args[:9], A + 128, 1 << 30, 1, 4, 2, 128, 64, 1, 0.125, None) == -1
+    assert lib.gqa_attn_selftest_wait_timeout(0, None) == -1
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    from causal_gqa_attention_flash_gb300 import _lib
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _lib.load()
+
+
+def test_product_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "causal_gqa_attention_flash_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "oracle/" not in src, f

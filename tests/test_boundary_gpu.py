@@ -1,0 +1,72 @@
+"""Boundary behaviour on a GPU: error codes, the bounded-wait timeout path, stream use."""
+
+import ctypes
+
+import pytest
+import torch
+
+from gpu_helpers import full_case, gqa
+
+pytestmark = pytest.mark.gpu
+
+
+def _raw(g):
+    from causal_gqa_attention_flash_gb300 import _lib
+    return _lib.load()
+
+
+def test_wait_timeout_selftest_reports_and_recovers():
+    """A wait that nothing ends gives up after its limit; the status says TIMEOUT once; the context stays usable."""
+    g = gqa()
+    assert g.gqa_attn_get_error() == 0
+    g.gqa_attn_selftest_wait_timeout(2000)
+    assert g.gqa_attn_get_error() == g.GQA_ERR_TIMEOUT
+    assert g.gqa_attn_get_error() == 0  # read-and-clear
+    full_case(g, 1, 4, 2, 129, 64, seed=3)  # kernels still run correctly afterwards
+
+
+def test_invalid_arguments_rejected_before_launch():
+    g = gqa()
+    lib = _raw(g)
+    q = torch.zeros(1, 4, 128, 64, device="cuda", dtype=torch.bfloat16)
+    k = torch.zeros(1, 2, 128, 64, device="cuda", dtype=torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 4, 128, device="cuda", dtype=torch.float32)
+    s = torch.cuda.current_stream().cuda_stream
+    P = lambda t: t.data_ptr()
+    ok = lib.gqa_attn_fwd(P(q), P(k), P(k), P(o), P(lse), 1, 4, 2, 128, 64, 1, 0.125, s)
+    assert ok == 0
+    assert lib.gqa_attn_fwd(P(q), P(k), P(k), P(o), P(lse), 1, 4, 3, 128, 64, 1, 0.125, s) == g.GQA_ERR_INVALID_ARG
+    assert lib.gqa_attn_fwd(P(q), P(k), P(k), P(o), P(lse), 1, 4, 2, 128, 96, 1, 0.125, s) == g.GQA_ERR_UNSUPPORTED
+    assert lib.gqa_attn_fwd(P(q) + 2, P(k), P(k), P(o), P(lse), 1, 4, 2, 128, 64, 1, 0.125, s) == g.GQA_ERR_INVALID_ARG
+    assert lib.gqa_attn_fwd(None, P(k), P(k), P(o), P(lse), 1, 4, 2, 128, 64, 1, 0.125, s) == g.GQA_ERR_INVALID_ARG
+    assert lib.gqa_attn_fwd(P(q), P(k), P(k), P(o), P(lse), 1, 4, 2, 0, 64, 1, 0.125, s) == g.GQA_ERR_INVALID_ARG
+    assert lib.gqa_attn_fwd(P(q), P(k), P(k), P(o), P(lse), 1, 4, 2, 128, 64, 1, float("nan"), s) == g.GQA_ERR_INVALID_ARG
+    assert lib.gqa_attn_fwd(P(q), P(k), P(k), P(o), P(lse), 1, 4, 2, 128, 64, 1, -1.0, s) == g.GQA_ERR_INVALID_ARG
+    need = lib.gqa_attn_bwd_workspace_size(1, 4, 2, 128, 64)
+    ws = torch.empty(need, device="cuda", dtype=torch.uint8)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
+    args = [P(q), P(k), P(k), P(o), P(q), P(lse), P(dq), P(dk), P(dv), P(ws)]
+    assert lib.gqa_attn_bwd(*args, need - 1, 1, 4, 2, 128, 64, 1, 0.125, s) == g.GQA_ERR_WORKSPACE_TOO_SMALL
+    bad_ws = args[:9] + [P(ws) + 16]
+    assert lib.gqa_attn_bwd(*bad_ws, need, 1, 4, 2, 128, 64, 1, 0.125, s) == g.GQA_ERR_INVALID_ARG
+    assert lib.gqa_attn_bwd(*args, need, 1, 4, 2, 128, 64, 1, 0.125, s) == 0
+    assert g.gqa_attn_get_error() == 0
+
+
+def test_runs_on_a_side_stream():
+    """Work is enqueued on the caller's stream; results match the default-stream run."""
+    g = gqa()
+    from gqa_inputs import make_inputs
+    q, k, v, dO = (t.cuda() for t in make_inputs(2, 8, 2, 300, 128, seed=77))
+    o0, l0 = g.gqa_attn_fwd(q, k, v)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        o1, l1 = g.gqa_attn_fwd(q, k, v, stream=side)
+        r1 = g.gqa_attn_bwd(q, k, v, o1, dO, l1, stream=side)
+    side.synchronize()
+    r0 = g.gqa_attn_bwd(q, k, v, o0, dO, l0)
+    torch.cuda.synchronize()
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    assert torch.equal(r0[1], r1[1]) and torch.equal(r0[2], r1[2])
