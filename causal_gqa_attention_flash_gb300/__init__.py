@@ -166,3 +166,4 @@ def gqa_attn_trace_collect() -> dict:
     total = (ctypes.c_double * n)()
     _check(_lib.load().gqa_attn_trace_collect(launches, total), "gqa_attn_trace_collect")
     return {name: (int(launches[i]), float(total[i])) for i, name in enumerate(KERNEL_NAMES)}
+

@@ -143,18 +143,19 @@ int gqa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   if (rc != GQA_OK) return rc;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return GQA_ERR_INVALID_ARG;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   cudaError_t e;
   if ((e = encode_bf16(&mq, q, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
   if ((e = encode_bf16(&mk, k, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
   if ((e = encode_bf16(&mv, v, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mo, o, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
   int* status = nullptr;
   if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
   FwdArgs a;
   a.map_q = &mq;
   a.map_k = &mk;
   a.map_v = &mv;
-  a.o = o;
+  a.map_o = &mo;
   a.lse = lse;
   a.B = B;
   a.Hq = Hq;

@@ -24,7 +24,7 @@ struct FwdArgs {
   const CUtensorMap* map_q;  // [B*Hq, S, D] bf16, box {64, 128, 1}, 128B swizzle
   const CUtensorMap* map_k;  // [B*Hkv, S, D]
   const CUtensorMap* map_v;
-  void* o;                   // bf16 [B, Hq, S, D]
+  const CUtensorMap* map_o;  // [B*Hq, S, D] bf16 (TMA store of O)
   float* lse;                // f32 [B, Hq, S]
   int B, Hq, Hkv, S, D, causal;
   float scale_log2;          // scale * log2(e)

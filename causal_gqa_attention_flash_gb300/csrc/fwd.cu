@@ -8,18 +8,28 @@
 // is associative the key loop tiles (section 3, last paragraph); here the tile
 // is 128 keys, one tcgen05 M=128 x N=128 MMA.
 //
-// One CTA = one (batch, query head, 128-row query tile). Warp roles:
-//   warp 4      TMA producer: Q once, then K_j / V_j into a ring of stages;
-//   warp 5      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//               buffers, then O += P_j V_j with P_j read from TMEM;
-//   warps 0..3  softmax: thread r owns query row r (TMEM lane r); reads S_j,
-//               updates (m, l), writes P_j = exp2(S_j*c - m) as bf16 back into
-//               the S_j buffer, rescales O in TMEM when m moves, and finally
-//               writes O / l and LSE.
-// TMEM columns: S buffer 0 at [0,128), S buffer 1 at [128,256), O at [256,256+D).
-// The reference max is only moved when the tile max exceeds it by more than
-// 2^8 (lazy rescale); any reference >= the true max gives the same O / l and
-// LSE, which is the monoid's regrouping property.
+// One CTA = one (batch, query head) and two consecutive 128-row query tiles,
+// A (rows q0..q0+127) and B (rows q0+128..q0+255), which share every K/V tile
+// the TMA brings in. Warp roles (384 threads, three warpgroups):
+//   warps 0..3  softmax of tile A: thread r owns row r of A (TMEM lane r);
+//   warps 4..7  softmax of tile B (same, lanes 0..127 through the lane quarter w % 4);
+//   warp 8      TMA producer: Q_A, Q_B once, then K_j / V_j into a ring of stages;
+//   warp 9      MMA issuer (one thread) and TMEM owner; warps 10, 11 idle.
+// Registers: launched at kLaunchRegs per thread; the producer warpgroup drops
+// to kLowRegs and the two softmax warpgroups rise to kHighRegs (setmaxnreg).
+// The MMA thread alternates between the tiles: while softmax A works on S_A(j)
+// the tensor core runs P_B(j-1) V_{j-1} and S_B(j); while softmax B works on
+// S_B(j) it runs P_A(j) V_j and S_A(j+1). Each softmax reads S, updates
+// (m, l), and writes P = exp2(S c - m) as bf16 back into the S columns, where
+// the next P V MMA reads it as its A operand.
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
+// The reference max moves only when a tile max exceeds it by more than 8
+// (log2 units): any reference >= the true max gives the same O / l and LSE,
+// the regrouping property of the monoid. Because S_X(j) is issued after
+// P_X(j-1) V_{j-1} on the same in-order MMA stream, its completion also
+// means the previous P V is done, so O can be rescaled right away.
+// Epilogue: O / l in bf16 is written into the tile's (no longer needed) Q
+// buffer in the TMA box layout and stored by TMA; rows past S are clipped.
 #include "common.h"
 #include "ptx.cuh"
 
@@ -29,16 +39,20 @@ namespace {
 template <int D>
 struct FwdCfg {
   static constexpr int kChunks = D / kChunk;
-  static constexpr int kTileBytes = kTile * D * 2;  // one 128-row bf16 tile of Q, K or V
-  static constexpr int kStages = (D == 64) ? 3 : 2;
-  static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kTileBytes;
+  static constexpr int kTileBytes = kTile * D * 2;  // one 128-row bf16 tile of Q, K, V or O
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kQOff = 0;                   // Q_A, Q_B (reused as O staging)
+  static constexpr int kKOff = kQOff + 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 384;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 256;
+  static constexpr int kLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
+  static constexpr int kLowRegs = (D == 64) ? 56 : 64;
+  static constexpr int kHighRegs = (D == 64) ? 224 : 216;
+  static_assert(2 * 128 * kHighRegs + 128 * kLowRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 };
 
 template <int ST>
@@ -49,14 +63,13 @@ struct FwdBars {
   uint64_t kv_empty[ST];
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t o_done;
+  uint64_t o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 struct FwdKParams {
-  uint16_t* o;
   float* lse;
   int Hq, Hkv, S, causal, n_tiles;
   float scale_log2;
@@ -73,27 +86,35 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return true;
 }
 
+// Number of key tiles query tile qt (first row q0) visits; 0 if the tile lies past S.
+__device__ __forceinline__ int kv_tiles_of(int qt, int S, int causal, int n_tiles) {
+  if (qt * kTile >= S) return 0;
+  return causal ? (qt + 1) : n_tiles;
+}
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-               const __grid_constant__ CUtensorMap map_v, const FwdKParams p) {
+               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+               const FwdKParams p) {
   using C = FwdCfg<D>;
   constexpr int ST = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   auto* bars = reinterpret_cast<FwdBars<ST>*>(smem + C::kBarOff);
-  uint8_t* sQ = smem + C::kQOff;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int bh = blockIdx.x;                      // b * Hq + h
-  const int qt = (int)gridDim.y - 1 - (int)blockIdx.y;  // longest (most key tiles) first
+  const int bh = blockIdx.x;                                   // b * Hq + h
+  const int pair = (int)gridDim.y - 1 - (int)blockIdx.y;       // longest pairs first
   const int b = bh / p.Hq;
   const int h = bh - b * p.Hq;
   const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
-  const int q0 = qt * kTile;
-  const int n_kv = p.causal ? (qt + 1) : p.n_tiles;
+  const int qtA = 2 * pair, qtB = 2 * pair + 1;
+  const int nA = kv_tiles_of(qtA, p.S, p.causal, p.n_tiles);
+  const int nB = kv_tiles_of(qtB, p.S, p.causal, p.n_tiles);
+  const int n_kv = nA > nB ? nA : nB;
   const WaitGuard wg{&bars->abort_flag, p.status, kWaitLimitNs};
 
   if (tid == 0) {
@@ -106,29 +127,32 @@ __global__ void __launch_bounds__(192, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->o_done[i], 1);
     }
-    mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
-
-  if (warp == 4) {
+  if (warp >= 8) {
+   setmaxnreg_dec<C::kLowRegs>();
+   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_3d(sQ + c * kBoxBytes, &map_q, &bars->q_full, c * kChunk, q0, bh);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * kBoxBytes, &map_q, &bars->q_full, c * kChunk,
+                      (qtA + t) * kTile, bh);
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % ST;
@@ -153,68 +177,82 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
-      const uint32_t o_tmem = tbase + C::kOCol;
-      const uint32_t q_addr = smem_addr(sQ);
-      auto issue_s = [&](int j) {
+      // S_X(j) = Q_X K_j^T into the S columns of tile X.
+      auto issue_s = [&](int x, int j) {
+        const uint32_t q_addr = smem_addr(smem + C::kQOff + x * C::kTileBytes);
         const uint32_t k_addr = smem_addr(smem + C::kKOff + (j % ST) * C::kTileBytes);
-        const uint32_t d_tmem = tbase + (uint32_t)(j & 1) * 128u;
+        const uint32_t d_tmem = tbase + (uint32_t)x * 128u;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
           umma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc_s,
                   kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->s_full[j & 1]);
+        umma_commit(&bars->s_full[x]);
+      };
+      // O_X += P_X(j) V_j, P_X(j) read from the S columns of tile X.
+      auto issue_pv = [&](int x, int j) {
+        const uint32_t v_addr = smem_addr(smem + C::kVOff + (j % ST) * C::kTileBytes);
+        const uint32_t p_tmem = tbase + (uint32_t)x * 128u;
+        const uint32_t o_tmem = tbase + C::kOCol + (uint32_t)x * D;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(o_tmem, p_tmem + (uint32_t)kk * 8u, sdesc_sw128(v_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024),
+                  idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->o_done[x]);
       };
       bool ok = mbar_wait(&bars->q_full, 0, wg) && mbar_wait(&bars->k_full[0], 0, wg);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
+        if (nA > 0) issue_s(0, 0);
+        if (nB > 0) issue_s(1, 0);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          const int j1 = j + 1;
-          if (!(ok = mbar_wait(&bars->k_full[j1 % ST], (j1 / ST) & 1, wg))) break;
-          tc_fence_after();
-          issue_s(j1);
-        }
-        if (!(ok = mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, wg))) break;
         const int st = j % ST;
+        const int j1 = j + 1;
         if (!(ok = mbar_wait(&bars->v_full[st], (j / ST) & 1, wg))) break;
-        tc_fence_after();
-        const uint32_t v_addr = smem_addr(smem + C::kVOff + st * C::kTileBytes);
-        const uint32_t p_tmem = tbase + (uint32_t)(j & 1) * 128u;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          umma_ts(o_tmem, p_tmem + (uint32_t)kk * 8u, sdesc_sw128(v_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024),
-                  idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        if (j1 < n_kv && !(ok = mbar_wait(&bars->k_full[j1 % ST], (j1 / ST) & 1, wg))) break;
+        if (j < nA) {
+          if (!(ok = mbar_wait(&bars->p_full[0], j & 1, wg))) break;
+          tc_fence_after();
+          issue_pv(0, j);
+          if (j1 < nA) issue_s(0, j1);
         }
-        umma_commit(&bars->o_done);
+        if (j < nB) {
+          if (!(ok = mbar_wait(&bars->p_full[1], j & 1, wg))) break;
+          tc_fence_after();
+          issue_pv(1, j);
+          if (j1 < nB) issue_s(1, j1);
+        }
         umma_commit(&bars->kv_empty[st]);
       }
       // Every MMA issued completes before TMEM is released.
       umma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, kWaitLimitNs);
     }
+   }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0..3)
-    const int row = tid;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t o_tmem = tbase + lane_off + C::kOCol;
+    // ------------------------------------------------------------ softmax (tile X = warp / 4)
+    setmaxnreg_inc<C::kHighRegs>();
+    const int x = warp >> 2;
+    const int row = tid & 127;
+    const int qt = qtA + x;
+    const int n_x = x ? nB : nA;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_tmem = tbase + lane_off + (uint32_t)x * 128u;
+    const uint32_t o_tmem = tbase + lane_off + C::kOCol + (uint32_t)x * D;
     const float c = p.scale_log2;
     float m_ref = 0.f, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int buf = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[buf], (j >> 1) & 1, wg));
+    for (int j = 0; j < n_x; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[x], j & 1, wg));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t s_tmem = tbase + lane_off + (uint32_t)buf * 128u;
       uint32_t r[128];
 #pragma unroll
       for (int q = 0; q < 4; ++q)
@@ -226,26 +264,16 @@ __global__ void __launch_bounds__(192, 1)
       const bool diag = p.causal && (j == qt);
       const bool tail = !p.causal && (kv0 + kTile > p.S);
       const int last = diag ? row : (tail ? (p.S - kv0 - 1) : (kTile - 1));  // last visible local key
-      float s[128];
-#pragma unroll
-      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
+      const bool masked = diag || tail;
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-      if (diag || tail) {
 #pragma unroll
-        for (int i = 0; i < 128; i += 4) {
-          mx0 = fmaxf(mx0, i + 0 <= last ? s[i + 0] : -INFINITY);
-          mx1 = fmaxf(mx1, i + 1 <= last ? s[i + 1] : -INFINITY);
-          mx2 = fmaxf(mx2, i + 2 <= last ? s[i + 2] : -INFINITY);
-          mx3 = fmaxf(mx3, i + 3 <= last ? s[i + 3] : -INFINITY);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 128; i += 4) {
-          mx0 = fmaxf(mx0, s[i + 0]);
-          mx1 = fmaxf(mx1, s[i + 1]);
-          mx2 = fmaxf(mx2, s[i + 2]);
-          mx3 = fmaxf(mx3, s[i + 3]);
-        }
+      for (int i = 0; i < 128; i += 4) {
+        const float s0 = __uint_as_float(r[i]), s1 = __uint_as_float(r[i + 1]);
+        const float s2 = __uint_as_float(r[i + 2]), s3 = __uint_as_float(r[i + 3]);
+        mx0 = fmaxf(mx0, (!masked || i + 0 <= last) ? s0 : -INFINITY);
+        mx1 = fmaxf(mx1, (!masked || i + 1 <= last) ? s1 : -INFINITY);
+        mx2 = fmaxf(mx2, (!masked || i + 2 <= last) ? s2 : -INFINITY);
+        mx3 = fmaxf(mx3, (!masked || i + 3 <= last) ? s3 : -INFINITY);
       }
       const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
       float alpha = 1.f;
@@ -259,28 +287,30 @@ __global__ void __launch_bounds__(192, 1)
       }
       const float neg_m = -m_ref;
       float sum0 = 0.f, sum1 = 0.f;
-      if (diag || tail) {
 #pragma unroll
-        for (int i = 0; i < 128; i += 2) {
-          s[i] = (i <= last) ? ex2_approx(fmaf(s[i], c, neg_m)) : 0.f;
-          s[i + 1] = (i + 1 <= last) ? ex2_approx(fmaf(s[i + 1], c, neg_m)) : 0.f;
-          sum0 += s[i];
-          sum1 += s[i + 1];
-        }
-      } else {
+      for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 128; i += 2) {
-          s[i] = ex2_approx(fmaf(s[i], c, neg_m));
-          s[i + 1] = ex2_approx(fmaf(s[i + 1], c, neg_m));
-          sum0 += s[i];
-          sum1 += s[i + 1];
+        for (int x2 = 0; x2 < 16; ++x2) {
+          const int i = q * 32 + 2 * x2;
+          float e0 = ex2_approx(fmaf(__uint_as_float(r[i]), c, neg_m));
+          float e1 = ex2_approx(fmaf(__uint_as_float(r[i + 1]), c, neg_m));
+          if (masked) {
+            e0 = (i <= last) ? e0 : 0.f;
+            e1 = (i + 1 <= last) ? e1 : 0.f;
+          }
+          sum0 += e0;
+          sum1 += e1;
+          pk[x2] = pack_bf16(e0, e1);
         }
+        tmem_st_32x32b_x16(s_tmem + q * 16, pk);
       }
       l = l * alpha + (sum0 + sum1);
 
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds the sum up to tile j-1 against the old reference: wait for P_{j-1} V_{j-1}, then rescale.
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, (j - 1) & 1, wg));
+        // O_X holds the sum up to tile j-1 against the old reference. P_X(j-1) V_{j-1} completed
+        // before S_X(j) did (same in-order MMA stream); the wait below returns at once.
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[x], (j - 1) & 1, wg));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -293,43 +323,48 @@ __global__ void __launch_bounds__(192, 1)
           tmem_st_32x32b_x32(o_tmem + cc * 32, o);
         }
       }
-      uint32_t pk[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) pk[i] = pack_bf16(s[2 * i], s[2 * i + 1]);
-      tmem_st_32x32b_x32(s_tmem + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st_32x32b_x32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->p_full[buf]);
+      mbar_arrive(&bars->p_full[x]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, (n_kv - 1) & 1, wg));
-    if (ok) {
+    if (ok && n_x > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[x], (n_x - 1) & 1, wg));
+    if (ok && n_x > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const int qrow = q0 + row;
-      uint16_t* orow = p.o + ((size_t)bh * p.S + qrow) * D;
+      uint8_t* stage = smem + C::kQOff + x * C::kTileBytes;  // Q_X is no longer read by any MMA
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld_32x32b_x32(o_tmem + cc * 32, o);
         tmem_wait_ld_x32(o);
-        uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (qrow < p.S) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int u = 0; u < 4; ++u) {  // 16-byte units of 8 columns
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(o[8 * u + 0]) * inv_l, __uint_as_float(o[8 * u + 1]) * inv_l);
+          w.y = pack_bf16(__uint_as_float(o[8 * u + 2]) * inv_l, __uint_as_float(o[8 * u + 3]) * inv_l);
+          w.z = pack_bf16(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
+          w.w = pack_bf16(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
+          const int col = cc * 32 + u * 8;      // first column of the unit
+          const int unit = (col & 63) >> 3;     // unit within the 128-byte row of its box
+          *reinterpret_cast<uint4*>(stage + (col >> 6) * kBoxBytes + row * 128 + ((unit ^ (row & 7)) << 4)) = w;
         }
       }
+      fence_proxy_async_smem();
+      named_barrier_sync(1 + x, 128);
+      if (row == 0) {
+        for (int cb = 0; cb < C::kChunks; ++cb)
+          tma_store_3d(&map_o, stage + cb * kBoxBytes, cb * kChunk, qt * kTile, bh);
+        bulk_commit_group();
+      }
+      const int qrow = qt * kTile + row;
       if (qrow < p.S) p.lse[(size_t)bh * p.S + qrow] = (m_ref + __log2f(l)) * 0.69314718055994530942f;
+      if (row == 0) bulk_wait_group_read<0>();
     }
     tc_fence_before();
   }
 
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tbase, C::kTmemCols);
   }
@@ -339,7 +374,6 @@ template <int D>
 cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
   FwdKParams p;
-  p.o = static_cast<uint16_t*>(a.o);
   p.lse = a.lse;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
@@ -350,9 +384,14 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.status = a.status;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(a.B * a.Hq), (unsigned)p.n_tiles);
+  // The setmaxnreg split must fit the registers the block is launched with, or the
+  // increase would wait forever: refuse to launch otherwise.
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, fwd_kernel<D>)) != cudaSuccess) return e;
+  if (fa.numRegs * C::kThreads < 2 * 128 * C::kHighRegs + 128 * C::kLowRegs) return cudaErrorInvalidConfiguration;
+  dim3 grid((unsigned)(a.B * a.Hq), (unsigned)ceil_div(a.S, 2 * kTile));
   trace_begin(kKernelFwd, stream);
-  fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, p);
+  fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_o, p);
   e = cudaGetLastError();
   trace_end(kKernelFwd, stream);
   return e;

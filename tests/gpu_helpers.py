@@ -46,8 +46,15 @@ def max_abs(a, b):
     return float(np.max(np.abs(np.asarray(a) - np.asarray(b)))) if np.size(a) else 0.0
 
 
+def bf16_round(x):
+    """Round f64 values to the nearest bf16 (ties to even), back as f64."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
 def assert_fwd_close(O, L, O_ref, L_ref, where=""):
-    eo, el = max_abs(O, O_ref), max_abs(L, L_ref)
+    # O is delivered in bf16, whose half-ulp is 0.0156 for |O| in [4, 8): the 1e-2 bound is
+    # applied against the correctly rounded bf16 oracle value, the best answer the format holds.
+    eo, el = max_abs(O, bf16_round(O_ref)), max_abs(L, L_ref)
     assert np.all(np.isfinite(O)) and np.all(np.isfinite(L)), where
     assert eo <= TOL_O, f"{where} O max-abs err {eo:.3e} > {TOL_O}"
     assert el <= TOL_LSE, f"{where} LSE max-abs err {el:.3e} > {TOL_LSE}"
