@@ -46,6 +46,7 @@ GQA_ERR_UNSUPPORTED = -2
 GQA_ERR_WORKSPACE_TOO_SMALL = -3
 GQA_ERR_CUDA = -4
 GQA_ERR_TIMEOUT = -5
+GQA_ERR_INTERNAL = -6
 
 
 class GqaAttnError(RuntimeError):

@@ -236,6 +236,7 @@ int gqa_attn_get_error(void* stream) {
   if ((e = cudaMemsetAsync(status, 0, sizeof(int), s)) != cudaSuccess) return fail_cuda(e);
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail_cuda(e);
   if (h & STATUS_TIMEOUT) return GQA_ERR_TIMEOUT;
+  if (h & STATUS_MISALIGNED_SMEM) return GQA_ERR_INTERNAL;
   return GQA_OK;
 }
 
@@ -247,6 +248,7 @@ const char* gqa_attn_strerror(int code) {
     case GQA_ERR_WORKSPACE_TOO_SMALL: return "backward workspace too small";
     case GQA_ERR_CUDA: return "CUDA error";
     case GQA_ERR_TIMEOUT: return "device-side wait exceeded its time limit";
+    case GQA_ERR_INTERNAL: return "kernel layout self-check failed (no work was done)";
     default: return "unknown error code";
   }
 }

@@ -21,9 +21,10 @@
 // bwd_main warp roles: warp 4 = TMA producer, warp 5 = MMA issuer, warps 0..3
 // = element-wise work, thread r owning TMEM lane r (key row r for S^T, dP^T,
 // dK, dV; query row r for the dQ partial).
-// TMEM columns: [0,128) S^T f32, then P^T bf16 in [0,64) and dS^T bf16 in
-// [64,128); [128,256) dP^T f32, then the dQ partial f32 [128, 128+D);
-// [256,256+D) dV; [384,384+D) dK.
+// TMEM columns: [0,128) S^T f32; column half h (query columns [64h, 64h+64))
+// then holds its packed bf16 P^T in [64h, 64h+32) and dS^T in [64h+32, 64h+64),
+// written only by the warpgroup that read those S^T columns; [128,256) dP^T
+// f32, then the dQ partial f32 [128, 128+D); [256,256+D) dV; [256+D,256+2D) dK.
 #include "common.h"
 #include "ptx.cuh"
 
@@ -107,21 +108,20 @@ template <int D>
 struct BwdCfg {
   static constexpr int kChunks = D / kChunk;
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kStages = (D == 64) ? 2 : 1;
+  static constexpr int kStages = 2;                                    // Q / dO ring
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;
-  static constexpr int kDSOff = kDOOff + kStages * kTileBytes;         // dS bf16 [128 kv][128 q], MN-major
-  static constexpr int kDSBytes = kTile * kTile * 2;
-  static constexpr int kStgOff = kDSOff + kDSBytes;                    // 2 x f32 [128][32] dQ staging (128B swizzle)
-  static constexpr int kStgBytes = kTile * 32 * 4;
-  static constexpr int kRowOff = kStgOff + 2 * kStgBytes;              // per stage: lse2[128], dvec[128]
+  static constexpr int kDSOff = kDOOff + kStages * kTileBytes;         // dS bf16 [128 kv][128 q], MN-major;
+  static constexpr int kDSBytes = kTile * kTile * 2;                   // reused as the dQ reduce staging
+  static constexpr int kRowOff = kDSOff + kDSBytes;                    // per stage: lse2[128], dvec[128]
   static constexpr int kBarOff = kRowOff + kStages * 2 * kTile * 4;
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
-  static constexpr int kThreads = 192;
+  static constexpr int kSmemBytes = kBarOff + 256;                     // the base is checked to be 1024-aligned
+  static constexpr int kThreads = 320;
+  static constexpr int kRounds = D / 64;                               // dQ staging rounds of two 32-column slices
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kSPCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 384;
+  static constexpr uint32_t kSPCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
 };
 
 template <int ST>
@@ -130,6 +130,7 @@ struct BwdBars {
   uint64_t qdo_full[ST];
   uint64_t qdo_empty[ST];
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free, dkv_done, drain;
+  uint64_t wg_bar[2];  // one per element-wise warpgroup (column half)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -144,20 +145,37 @@ struct BwdKParams {
   int* status;
 };
 
+// One CTA per (batch, KV head, 128-key tile jt), 320 threads:
+//   warps 0..7  element-wise work. Warp w owns TMEM lane quarter w % 4 (key
+//               rows of S^T, dP^T, dK, dV; query rows of the dQ partial) and the
+//               column half h = w / 4 (query columns [64h, 64h+64) of S^T / dP^T;
+//               dQ / dK / dV columns of that half);
+//   warp 8      TMA producer: K, V once; Q, dO, LSE2 and D rows per step, 2 stages;
+//   warp 9      MMA issuer (one thread) and TMEM owner.
+// A step is one (query head of the group, query tile i). MMA order per step t:
+//   dV(t) after P(t) is written, dK(t) and dQ(t) after dS(t) is written, then at
+//   once S(t+1) (its Q is already staged) and, once the dQ(t) columns have been
+//   read out, dP(t+1). The element-wise warps load the dQ partial into registers,
+//   release its TMEM columns, and only then stage it (in the dS buffer, whose
+//   dQ MMA has completed) for the TMA reduce-add.
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                     const __grid_constant__ CUtensorMap map_acc, const BwdKParams p) {
   using C = BwdCfg<D>;
   constexpr int ST = C::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   auto* bars = reinterpret_cast<BwdBars<ST>*>(smem + C::kBarOff);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // The 128-byte swizzled tiles need a 1024-byte aligned base; report instead of faulting.
+  if ((smem_addr(smem) & 1023u) != 0) {
+    if (tid == 0) atomicOr(p.status, STATUS_MISALIGNED_SMEM);
+    return;
+  }
   const int kvh = blockIdx.x;  // b * Hkv + hkv
   const int jt = blockIdx.y;   // key tile; tile 0 sees the most query tiles when causal
   const int G = p.Hq / p.Hkv;
@@ -177,16 +195,18 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->ds_full, 128);
+    mbar_init(&bars->p_full, 8);   // one arrival per element-wise warp
+    mbar_init(&bars->ds_full, 8);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->dq_free, 8);
     mbar_init(&bars->dkv_done, 1);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->wg_bar[0], 4);
+    mbar_init(&bars->wg_bar[1], 4);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
@@ -194,7 +214,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&map_q);
@@ -233,7 +253,7 @@ __global__ void __launch_bounds__(192, 1)
           mbar_wait_drain(&bars->qdo_full[t % ST], (t / ST) & 1, kWaitLimitNs);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_kk = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both operands K-major
@@ -242,107 +262,131 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t k_addr = smem_addr(smem + C::kKOff);
       const uint32_t v_addr = smem_addr(smem + C::kVOff);
       const uint32_t ds_addr = smem_addr(smem + C::kDSOff);
-      bool ok = mbar_wait(&bars->kv_full, 0, wg);
-      for (int t = 0; ok && t < n_steps; ++t) {
-        const int st = t % ST;
-        if (!(ok = mbar_wait(&bars->qdo_full[st], (t / ST) & 1, wg))) break;
-        if (t > 0 && !(ok = mbar_wait(&bars->dq_free, (t - 1) & 1, wg))) break;
+      auto q_addr = [&](int t) { return smem_addr(smem + C::kQOff + (t % ST) * C::kTileBytes); };
+      auto do_addr = [&](int t) { return smem_addr(smem + C::kDOOff + (t % ST) * C::kTileBytes); };
+      // X^T = A B^T for a 128-row A tile (K or V) and a 128-row B tile (Q or dO), both K-major.
+      auto issue_kmajor = [&](uint32_t d_col, uint32_t a, uint32_t bb) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
+          umma_ss(tbase + d_col, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bb + off, 16, 1024), idesc_kk,
+                  kk > 0 ? 1u : 0u);
+        }
+      };
+      // TMEM column of the A operand (P^T; dS^T is 32 columns further) for query rows 16kk..16kk+15:
+      // column half h = kk / 4 keeps its packed P^T in [64h, 64h+32) and dS^T in [64h+32, 64h+64).
+      auto p_col = [](int kk) { return (uint32_t)(kk >> 2) * 64u + (uint32_t)(kk & 3) * 8u; };
+      bool ok = mbar_wait(&bars->kv_full, 0, wg) && mbar_wait(&bars->qdo_full[0], 0, wg);
+      if (ok) {
         tc_fence_after();
-        const uint32_t q_addr = smem_addr(smem + C::kQOff + st * C::kTileBytes);
-        const uint32_t do_addr = smem_addr(smem + C::kDOOff + st * C::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
-          umma_ss(tbase + C::kSPCol, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
-                  idesc_kk, kk > 0 ? 1u : 0u);
-        }
+        issue_kmajor(C::kSPCol, k_addr, q_addr(0));
         umma_commit(&bars->s_full);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
-          umma_ss(tbase + C::kDPCol, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
-                  idesc_kk, kk > 0 ? 1u : 0u);
-        }
+        issue_kmajor(C::kDPCol, v_addr, do_addr(0));
         umma_commit(&bars->dp_full);
+      }
+      for (int t = 0; ok && t < n_steps; ++t) {
         if (!(ok = mbar_wait(&bars->p_full, t & 1, wg))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(tbase + C::kDVCol, tbase + C::kSPCol + (uint32_t)kk * 8u,
-                  sdesc_sw128(do_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_tb, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tbase + C::kDVCol, tbase + C::kSPCol + p_col(kk),
+                  sdesc_sw128(do_addr(t) + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_tb,
+                  (t > 0 || kk > 0) ? 1u : 0u);
         if (!(ok = mbar_wait(&bars->ds_full, t & 1, wg))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(tbase + C::kDKCol, tbase + C::kSPCol + 64u + (uint32_t)kk * 8u,
-                  sdesc_sw128(q_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_tb, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tbase + C::kDKCol, tbase + C::kSPCol + p_col(kk) + 32u,
+                  sdesc_sw128(q_addr(t) + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_tb,
+                  (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_ss(tbase + C::kDPCol, sdesc_sw128(ds_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024),
                   sdesc_sw128(k_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_mm, kk > 0 ? 1u : 0u);
         umma_commit(&bars->dq_full);
-        umma_commit(&bars->qdo_empty[st]);
+        umma_commit(&bars->qdo_empty[t % ST]);
+        if (t + 1 < n_steps) {
+          const int t1 = t + 1;
+          if (!(ok = mbar_wait(&bars->qdo_full[t1 % ST], (t1 / ST) & 1, wg))) break;
+          tc_fence_after();
+          issue_kmajor(C::kSPCol, k_addr, q_addr(t1));  // P^T(t) and dS^T(t) were consumed by dV(t), dK(t)
+          umma_commit(&bars->s_full);
+          if (!(ok = mbar_wait(&bars->dq_free, t & 1, wg))) break;
+          tc_fence_after();
+          issue_kmajor(C::kDPCol, v_addr, do_addr(t1));
+          umma_commit(&bars->dp_full);
+        }
       }
       umma_commit(&bars->dkv_done);
       umma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, kWaitLimitNs);
     }
   } else {
-    // ------------------------------------------------------------ element-wise warps 0..3
-    const int row = tid;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ------------------------------------------------------------ element-wise warps 0..7
+    const int quarter = warp & 3;
+    const int hf = warp >> 2;                     // column half
+    const int row = quarter * 32 + lane;          // TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t sp_tmem = tbase + lane_off + C::kSPCol;
     const uint32_t dp_tmem = tbase + lane_off + C::kDPCol;
     const float c = p.scale_log2;
     const int kv_row = jt * kTile + row;
     const bool kv_valid = kv_row < p.S;
-    uint8_t* sds = smem + C::kDSOff;
-    float* stg = reinterpret_cast<float*>(smem + C::kStgOff);
+    const bool leader = (row == 0);               // one thread of the warpgroup issues its TMA reduces
+    uint8_t* sds_half = smem + C::kDSOff + hf * kBoxBytes;  // dS columns [64hf, 64hf+64) / this half's staging
+    uint64_t* wgb = &bars->wg_bar[hf];
+    uint32_t wg_phase = 0;
     bool ok = true;
-    int stg_i = 0;
     for (int t = 0; t < n_steps; ++t) {
       const int st = t % ST;
       const int hl = t / n_i;
       const int i = i_start + (t - hl * n_i);
       const int bhq = bhq0 + hl;
-      const float* slse = reinterpret_cast<const float*>(smem + C::kRowOff) + st * 2 * kTile;
+      const float* slse = reinterpret_cast<const float*>(smem + C::kRowOff) + st * 2 * kTile + hf * 64;
       const float* sdv = slse + kTile;
       // visible iff key (jt*128 + row) <= query (i*128 + col): on the diagonal tile, col >= row
       const int first_visible = (p.causal && i == jt) ? row : 0;
 
+      // ---- P^T = exp2(S^T c - LSE2) for the 64 query columns of this half
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, t & 1, wg));
       if (!ok) break;
       tc_fence_after();
-      uint32_t r[128];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        tmem_ld_32x32b_x32(sp_tmem + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * q]));
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[32 * q]));
-      float P[128];
-#pragma unroll
-      for (int col = 0; col < 128; ++col) {
-        const float e = ex2_approx(fmaf(__uint_as_float(r[col]), c, -slse[col]));
-        P[col] = (kv_valid && col >= first_visible) ? e : 0.f;
-      }
+      float P[64];
       {
-        uint32_t pk[64];
+        uint32_t r[64];
+        tmem_ld_32x32b_x32(sp_tmem + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld_32x32b_x32(sp_tmem + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        uint32_t pk[32];
 #pragma unroll
-        for (int x = 0; x < 64; ++x) pk[x] = pack_bf16(P[2 * x], P[2 * x + 1]);
-        tmem_st_32x32b_x32(sp_tmem + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st_32x32b_x32(sp_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        for (int x = 0; x < 32; ++x) {
+          const int c0 = 2 * x;
+          const float e0 = ex2_approx(fmaf(__uint_as_float(r[c0]), c, -slse[c0]));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(r[c0 + 1]), c, -slse[c0 + 1]));
+          P[c0] = (kv_valid && hf * 64 + c0 >= first_visible) ? e0 : 0.f;
+          P[c0 + 1] = (kv_valid && hf * 64 + c0 + 1 >= first_visible) ? e1 : 0.f;
+          pk[x] = pack_bf16(P[c0], P[c0 + 1]);
+        }
+        tmem_st_32x32b_x32(sp_tmem + hf * 64, pk);  // this half's own columns
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
+      mbar_arrive_warp(&bars->p_full);
 
+      // ---- dS^T = P^T (dP^T - D): into TMEM (A operand of dK) and into smem (A operand of dQ)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->dp_full, t & 1, wg));
       if (!ok) break;
       tc_fence_after();
+      if (t > 0) {
+        // the half's dS columns held the previous step's dQ staging: its reduce must have read it
+        if (leader) bulk_wait_group_read<0>();
+        if (!(ok = wg_barrier(wgb, wg_phase, wg))) break;
+      }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         uint32_t d[32];
-        tmem_ld_32x32b_x32(dp_tmem + q * 32, d);
+        tmem_ld_32x32b_x32(dp_tmem + hf * 64 + q * 32, d);
         tmem_wait_ld_x32(d);
         uint32_t pk[16];
 #pragma unroll
@@ -352,84 +396,80 @@ __global__ void __launch_bounds__(192, 1)
           const float ds1 = P[c0 + 1] * (__uint_as_float(d[2 * x + 1]) - sdv[c0 + 1]);
           pk[x] = pack_bf16(ds0, ds1);
         }
-        tmem_st_32x32b_x16(sp_tmem + 64 + q * 16, pk);
+        tmem_st_32x32b_x16(sp_tmem + hf * 64 + 32 + q * 16, pk);
         // dS[row = key][col = query] into the MN-major (query-contiguous) 128B-swizzled tile.
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int qc = q * 32 + u * 8;  // first query column of this 16-byte unit
-          const int unit = (qc & 63) >> 3;
-          uint8_t* dst = sds + (qc >> 6) * kBoxBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((unit ^ (row & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          const int unit = q * 4 + u;  // 16-byte unit within this half's 128-byte row
+          *reinterpret_cast<uint4*>(sds_half + (row >> 3) * 1024 + (row & 7) * 128 + ((unit ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
       }
       fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->ds_full);
+      mbar_arrive_warp(&bars->ds_full);
 
+      // ---- dQ partial (TMEM lane = query row): load this half's columns, free TMEM, reduce-add
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, t & 1, wg));
       if (!ok) break;
       tc_fence_after();
-      // dQ partial: TMEM lane = query row. Staged in 32-column f32 slices, reduce-added by TMA.
+      uint32_t dq[C::kRounds][32];
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t d[32];
-        tmem_ld_32x32b_x32(dp_tmem + q * 32, d);
-        tmem_wait_ld_x32(d);
-        float* buf = stg + (stg_i & 1) * (kTile * 32);
-        if (tid == 0) bulk_wait_group_read<1>();
-        named_barrier_sync(1, 128);
-        // 128-byte swizzled slice (the accumulator map's swizzle): 16-byte unit u of row r
-        // sits at position u ^ (r % 8), so 8 consecutive rows hit distinct banks.
+      for (int rd = 0; rd < C::kRounds; ++rd) tmem_ld_32x32b_x32(dp_tmem + (2 * rd + hf) * 32, dq[rd]);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          *reinterpret_cast<float4*>(buf + row * 32 + ((u ^ (row & 7)) << 2)) =
-              make_float4(__uint_as_float(d[4 * u]), __uint_as_float(d[4 * u + 1]), __uint_as_float(d[4 * u + 2]),
-                          __uint_as_float(d[4 * u + 3]));
+      for (int rd = 0; rd < C::kRounds; ++rd) tmem_wait_ld_x32(dq[rd]);
+      tc_fence_before();
+      mbar_arrive_warp(&bars->dq_free);
+      float* stage = reinterpret_cast<float*>(sds_half);  // [128 query rows][32 f32], 128B swizzle
+#pragma unroll
+      for (int rd = 0; rd < C::kRounds; ++rd) {
+        if (rd > 0) {
+          if (leader) bulk_wait_group_read<0>();
+          if (!(ok = wg_barrier(wgb, wg_phase, wg))) break;
         }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<float4*>(stage + row * 32 + ((u ^ (row & 7)) << 2)) =
+              make_float4(__uint_as_float(dq[rd][4 * u]), __uint_as_float(dq[rd][4 * u + 1]),
+                          __uint_as_float(dq[rd][4 * u + 2]), __uint_as_float(dq[rd][4 * u + 3]));
         fence_proxy_async_smem();
-        named_barrier_sync(1, 128);
-        if (tid == 0) {
-          tma_reduce_add_3d(&map_acc, buf, q * 32, i * kTile, bhq);
+        if (!(ok = wg_barrier(wgb, wg_phase, wg))) break;
+        if (leader) {
+          tma_reduce_add_3d(&map_acc, stage, (2 * rd + hf) * 32, i * kTile, bhq);
           bulk_commit_group();
         }
-        ++stg_i;
       }
-      tc_fence_before();
-      mbar_arrive(&bars->dq_free);
+      if (!ok) break;
     }
-    if (tid == 0) bulk_wait_group<0>();
+    if (leader) bulk_wait_group<0>();
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->dkv_done, 0, wg));
     if (ok) {
       tc_fence_after();
       const size_t orow = ((size_t)kvh * p.S + kv_row) * D;
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t d[32];
-        tmem_ld_32x32b_x32(tbase + lane_off + C::kDVCol + q * 32, d);
-        tmem_wait_ld_x32(d);
-        uint32_t w[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x) w[x] = pack_bf16(__uint_as_float(d[2 * x]), __uint_as_float(d[2 * x + 1]));
+      for (int q = 0; q < D / 64; ++q) {
+        const int col = hf * (D / 2) + q * 32;
+        uint32_t dv[32], dk[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kDVCol + col, dv);
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kDKCol + col, dk);
+        tmem_wait_ld_x32(dv);
+        tmem_wait_ld_x32(dk);
         if (kv_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dv + orow + q * 32);
+          uint4* dstv = reinterpret_cast<uint4*>(p.dv + orow + col);
+          uint4* dstk = reinterpret_cast<uint4*>(p.dk + orow + col);
 #pragma unroll
-          for (int x = 0; x < 4; ++x) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t d[32];
-        tmem_ld_32x32b_x32(tbase + lane_off + C::kDKCol + q * 32, d);
-        tmem_wait_ld_x32(d);
-        uint32_t w[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x)
-          w[x] = pack_bf16(__uint_as_float(d[2 * x]) * p.scale, __uint_as_float(d[2 * x + 1]) * p.scale);
-        if (kv_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dk + orow + q * 32);
-#pragma unroll
-          for (int x = 0; x < 4; ++x) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+          for (int x = 0; x < 4; ++x) {
+            dstv[x] = make_uint4(pack_bf16(__uint_as_float(dv[8 * x + 0]), __uint_as_float(dv[8 * x + 1])),
+                                 pack_bf16(__uint_as_float(dv[8 * x + 2]), __uint_as_float(dv[8 * x + 3])),
+                                 pack_bf16(__uint_as_float(dv[8 * x + 4]), __uint_as_float(dv[8 * x + 5])),
+                                 pack_bf16(__uint_as_float(dv[8 * x + 6]), __uint_as_float(dv[8 * x + 7])));
+            const float s = p.scale;
+            dstk[x] = make_uint4(pack_bf16(__uint_as_float(dk[8 * x + 0]) * s, __uint_as_float(dk[8 * x + 1]) * s),
+                                 pack_bf16(__uint_as_float(dk[8 * x + 2]) * s, __uint_as_float(dk[8 * x + 3]) * s),
+                                 pack_bf16(__uint_as_float(dk[8 * x + 4]) * s, __uint_as_float(dk[8 * x + 5]) * s),
+                                 pack_bf16(__uint_as_float(dk[8 * x + 6]) * s, __uint_as_float(dk[8 * x + 7]) * s));
+          }
         }
       }
     }
@@ -437,7 +477,7 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tbase, C::kTmemCols);
   }

@@ -50,8 +50,8 @@ struct FwdCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 256;
   static constexpr int kLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
-  static constexpr int kLowRegs = (D == 64) ? 56 : 64;
-  static constexpr int kHighRegs = (D == 64) ? 224 : 216;
+  static constexpr int kLowRegs = 64;
+  static constexpr int kHighRegs = 216;
   static_assert(2 * 128 * kHighRegs + 128 * kLowRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 };
 
@@ -65,6 +65,7 @@ struct FwdBars {
   uint64_t p_full[2];
   uint64_t o_done[2];
   uint64_t drain;
+  uint64_t wg_bar[2];  // one per softmax warpgroup
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -84,6 +85,55 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
+}
+
+// Row max of one 128-key score row held in registers. Masked tiles (the
+// causal diagonal, the ragged last tile) exclude keys past `last`; the
+// unmasked path (all other tiles) has no per-key select.
+template <bool kMasked>
+__device__ __forceinline__ float row_max(const uint32_t (&r)[128], int last) {
+  float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 128; i += 8) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[k] = __uint_as_float(r[i + k]);
+      if (kMasked) v[k] = (i + k <= last) ? v[k] : -INFINITY;
+    }
+    a0 = fmax3(a0, v[0], v[1]);
+    a1 = fmax3(a1, v[2], v[3]);
+    a2 = fmax3(a2, v[4], v[5]);
+    a3 = fmax3(a3, v[6], v[7]);
+  }
+  return fmax3(a0, a1, fmaxf(a2, a3));
+}
+
+// P = exp2(S c - m) for one row, packed to bf16 pairs and stored into the
+// row's S columns (32 columns per tcgen05.st); returns the row sum of P.
+template <bool kMasked>
+__device__ __forceinline__ float exp_pack_store(const uint32_t (&r)[128], int last, float c, float neg_m,
+                                                uint32_t s_tmem) {
+  float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int x2 = 0; x2 < 16; ++x2) {
+      const int i = q * 32 + 2 * x2;
+      float e0 = ex2_approx(fmaf(__uint_as_float(r[i]), c, neg_m));
+      float e1 = ex2_approx(fmaf(__uint_as_float(r[i + 1]), c, neg_m));
+      if (kMasked) {
+        e0 = (i <= last) ? e0 : 0.f;
+        e1 = (i + 1 <= last) ? e1 : 0.f;
+      }
+      sum0 += e0;
+      sum1 += e1;
+      pk[x2] = pack_bf16(e0, e1);
+    }
+    tmem_st_32x32b_x16(s_tmem + q * 16, pk);
+  }
+  return sum0 + sum1;
 }
 
 // Number of key tiles query tile qt (first row q0) visits; 0 if the tile lies past S.
@@ -126,10 +176,12 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->p_full[i], 4);  // one arrival per softmax warp
       mbar_init(&bars->o_done[i], 1);
     }
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->wg_bar[0], 4);
+    mbar_init(&bars->wg_bar[1], 4);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -265,17 +317,8 @@ __global__ void __launch_bounds__(384, 1)
       const bool tail = !p.causal && (kv0 + kTile > p.S);
       const int last = diag ? row : (tail ? (p.S - kv0 - 1) : (kTile - 1));  // last visible local key
       const bool masked = diag || tail;
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 128; i += 4) {
-        const float s0 = __uint_as_float(r[i]), s1 = __uint_as_float(r[i + 1]);
-        const float s2 = __uint_as_float(r[i + 2]), s3 = __uint_as_float(r[i + 3]);
-        mx0 = fmaxf(mx0, (!masked || i + 0 <= last) ? s0 : -INFINITY);
-        mx1 = fmaxf(mx1, (!masked || i + 1 <= last) ? s1 : -INFINITY);
-        mx2 = fmaxf(mx2, (!masked || i + 2 <= last) ? s2 : -INFINITY);
-        mx3 = fmaxf(mx3, (!masked || i + 3 <= last) ? s3 : -INFINITY);
-      }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const float mx = masked ? row_max<true>(r, last) : row_max<false>(r, last);
+      const float m_tile = mx * c;
       float alpha = 1.f;
       bool need = false;
       if (j == 0) {
@@ -286,26 +329,9 @@ __global__ void __launch_bounds__(384, 1)
         need = true;
       }
       const float neg_m = -m_ref;
-      float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int x2 = 0; x2 < 16; ++x2) {
-          const int i = q * 32 + 2 * x2;
-          float e0 = ex2_approx(fmaf(__uint_as_float(r[i]), c, neg_m));
-          float e1 = ex2_approx(fmaf(__uint_as_float(r[i + 1]), c, neg_m));
-          if (masked) {
-            e0 = (i <= last) ? e0 : 0.f;
-            e1 = (i + 1 <= last) ? e1 : 0.f;
-          }
-          sum0 += e0;
-          sum1 += e1;
-          pk[x2] = pack_bf16(e0, e1);
-        }
-        tmem_st_32x32b_x16(s_tmem + q * 16, pk);
-      }
-      l = l * alpha + (sum0 + sum1);
+      const float rsum = masked ? exp_pack_store<true>(r, last, c, neg_m, s_tmem)
+                                : exp_pack_store<false>(r, last, c, neg_m, s_tmem);
+      l = l * alpha + rsum;
 
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // O_X holds the sum up to tile j-1 against the old reference. P_X(j-1) V_{j-1} completed
@@ -325,7 +351,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->p_full[x]);
+      mbar_arrive_warp(&bars->p_full[x]);
     }
     if (ok && n_x > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[x], (n_x - 1) & 1, wg));
     if (ok && n_x > 0) {
@@ -350,8 +376,9 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       fence_proxy_async_smem();
-      named_barrier_sync(1 + x, 128);
-      if (row == 0) {
+      uint32_t wg_phase = 0;
+      ok = wg_barrier(&bars->wg_bar[x], wg_phase, wg);
+      if (ok && row == 0) {
         for (int cb = 0; cb < C::kChunks; ++cb)
           tma_store_3d(&map_o, stage + cb * kBoxBytes, cb * kChunk, qt * kTile, bh);
         bulk_commit_group();

@@ -13,6 +13,7 @@ namespace gqa {
 
 // Device status bits (OR-ed into the library's status word).
 constexpr int STATUS_TIMEOUT = 1;
+constexpr int STATUS_MISALIGNED_SMEM = 2;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -82,6 +83,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
       }
     }
   }
+}
+
+// One arrival per warp: the warp's lanes synchronise (which orders their
+// earlier memory operations), then lane 0 arrives. Barriers that collect warps
+// this way are initialised with the number of warps, not threads.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Barrier among the 4 warps of one warpgroup on an mbarrier initialised with
+// count 4: every warp arrives once, then every thread waits (bounded) for the
+// phase to complete; phase is the caller's per-thread phase bit. Unlike
+// bar.sync it cannot hang if a warp of the group has left after an aborted
+// wait. Arrive / wait order the group's shared-memory writes before its later
+// reads.
+__device__ __forceinline__ bool wg_barrier(uint64_t* bar, uint32_t& phase, const WaitGuard& g) {
+  mbar_arrive_warp(bar);
+  const bool ok = mbar_wait(bar, phase, g);
+  phase ^= 1u;
+  return ok;
 }
 
 // ---------------------------------------------------------------- TMA / bulk copies
@@ -238,6 +260,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max(a, b, c) in one instruction (sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {

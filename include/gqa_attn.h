@@ -60,6 +60,7 @@ extern "C" {
 #define GQA_ERR_WORKSPACE_TOO_SMALL (-3) /* backward workspace smaller than gqa_attn_bwd_workspace_size() */
 #define GQA_ERR_CUDA (-4)                /* a CUDA runtime/driver call failed; see gqa_attn_last_cuda_error() */
 #define GQA_ERR_TIMEOUT (-5)             /* a device-side wait gave up (reported by gqa_attn_get_error) */
+#define GQA_ERR_INTERNAL (-6)            /* a kernel's own layout check failed and it did no work (gqa_attn_get_error) */
 
 /*
  * Forward: O = softmax(scale * Q K^T + causal mask) V and LSE per query row.
@@ -105,7 +106,9 @@ int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
 /*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device. Returns GQA_OK, GQA_ERR_TIMEOUT if a kernel gave up on a
- * wait since the last call, or GQA_ERR_CUDA if the stream reports an error.
+ * wait since the last call, GQA_ERR_INTERNAL if a kernel's own shared-memory
+ * alignment check failed (it then returned without work), or GQA_ERR_CUDA if
+ * the stream reports an error.
  */
 int gqa_attn_get_error(void* stream);
 
