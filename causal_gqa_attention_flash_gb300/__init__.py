@@ -34,6 +34,8 @@ __all__ = [
     "gqa_attn_selftest_wait_timeout",
     "gqa_attn_trace_arm",
     "gqa_attn_trace_collect",
+    "gqa_attn_bwd_noalloc",
+    "NOALLOC_SCRATCH_BYTES",
     "KERNEL_NAMES",
     "lib_path",
 ]
@@ -47,6 +49,7 @@ GQA_ERR_WORKSPACE_TOO_SMALL = -3
 GQA_ERR_CUDA = -4
 GQA_ERR_TIMEOUT = -5
 GQA_ERR_INTERNAL = -6
+NOALLOC_SCRATCH_BYTES = 64 << 20  # GQA_NOALLOC_SCRATCH_BYTES of include/gqa_attn.h
 
 
 class GqaAttnError(RuntimeError):
@@ -168,3 +171,21 @@ def gqa_attn_trace_collect() -> dict:
     _check(_lib.load().gqa_attn_trace_collect(launches, total), "gqa_attn_trace_collect")
     return {name: (int(launches[i]), float(total[i])) for i, name in enumerate(KERNEL_NAMES)}
 
+
+def gqa_attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, causal: bool = True, scale: float | None = None,
+                         stream=None):
+    """Backward into caller-provided dq, dk, dv using the library's static scratch array.
+
+    For callers that cannot allocate device memory: nothing is allocated here
+    or in the library (the outputs must be given). The scratch array holds
+    NOALLOC_SCRATCH_BYTES; larger problems raise GqaAttnError (workspace too
+    small). Calls that overlap on the GPU race on the shared array.
+    """
+    B, Hq, Hkv, S, D = _dims(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = _lib.load().gqa_attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
+                                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                          B, Hq, Hkv, S, D, int(bool(causal)), float(scale), _stream_handle(stream))
+    _check(rc, "gqa_attn_bwd_noalloc")
+    return dq, dk, dv

@@ -19,6 +19,7 @@ SIGNATURES = {
     "gqa_attn_selftest_wait_timeout": (_c_int, [_c_int, _vp]),
     "gqa_attn_trace_arm": (_c_int, []),
     "gqa_attn_trace_collect": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(ctypes.c_double)]),
+    "gqa_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_c_float, _vp]),
 }
 
 _lib = None

@@ -108,6 +108,8 @@ thread_local int t_trace_error = 0;
 
 }  // namespace
 
+int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
+
 void trace_begin(int kind, cudaStream_t s) {
   if (!t_trace_armed) return;
   if (t_trace_used == t_trace.size()) {

@@ -73,6 +73,9 @@ enum KernelKind { kKernelFwd = 0, kKernelBwdPrep = 1, kKernelBwdMain = 2, kKerne
 void trace_begin(int kind, cudaStream_t s);
 void trace_end(int kind, cudaStream_t s);
 
+// Keeps e as this host thread's last CUDA error and returns GQA_ERR_CUDA (api.cu).
+int record_cuda_error(cudaError_t e);
+
 // Host launchers (fwd.cu, bwd.cu). Return a cudaError_t.
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);

@@ -146,6 +146,34 @@ int gqa_attn_selftest_wait_timeout(int limit_us, void* stream);
 int gqa_attn_trace_arm(void);
 int gqa_attn_trace_collect(int* launches, double* total_ms);
 
+/*
+ * Backward without caller-provided workspace and without any allocation (the
+ * paper has no counterpart; this is a convenience of this library).
+ *
+ * For callers that cannot call cudaMalloc: code running where device
+ * allocation is forbidden or unsafe (inside an allocator's own callbacks, in
+ * a framework that owns all device memory and hands out only tensors, on
+ * hosts that must not allocate after start-up). The backward's scratch
+ * memory (D and scaled-LSE rows, f32 dQ accumulator) lives instead in one
+ * file-scope device array of GQA_NOALLOC_SCRATCH_BYTES (64 MiB) that every
+ * device which loads the library holds until the process exits.
+ * Arguments, layout, outputs and errors are those of gqa_attn_bwd without the
+ * workspace pair. Problems whose workspace (gqa_attn_bwd_workspace_size)
+ * exceeds the array are rejected with GQA_ERR_WORKSPACE_TOO_SMALL; invalid
+ * sizes with GQA_ERR_INVALID_ARG / GQA_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.
+ * Every call on a device shares the array and it keeps the last call's
+ * contents; each call rewrites everything it reads (the dQ accumulator is
+ * zeroed by the call itself). Calls that overlap on the GPU (concurrent
+ * streams or host threads on the same device) race on the array.
+ * Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES (64u << 20)
+int gqa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int D,
+                         int causal, float scale, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
