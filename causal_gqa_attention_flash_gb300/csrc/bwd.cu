@@ -113,13 +113,13 @@ struct BwdCfg {
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;
-  static constexpr int kDSOff = kDOOff + kStages * kTileBytes;         // dS bf16 [128 kv][128 q], MN-major;
-  static constexpr int kDSBytes = kTile * kTile * 2;                   // reused as the dQ reduce staging
+  static constexpr int kDSOff = kDOOff + kStages * kTileBytes;         // dS bf16 [128 kv][128 q], MN-major
+  static constexpr int kDSBytes = kTile * kTile * 2;
   static constexpr int kRowOff = kDSOff + kDSBytes;                    // per stage: lse2[128], dvec[128]
   static constexpr int kBarOff = kRowOff + kStages * 2 * kTile * 4;
   static constexpr int kSmemBytes = kBarOff + 256;                     // the base is checked to be 1024-aligned
   static constexpr int kThreads = 320;
-  static constexpr int kRounds = D / 64;                               // dQ staging rounds of two 32-column slices
+  static constexpr int kRounds = D / 64;                               // 32-column dQ slices per warpgroup
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSPCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
 };
@@ -156,8 +156,11 @@ struct BwdKParams {
 //   dV(t) after P(t) is written, dK(t) and dQ(t) after dS(t) is written, then at
 //   once S(t+1) (its Q is already staged) and, once the dQ(t) columns have been
 //   read out, dP(t+1). The element-wise warps load the dQ partial into registers,
-//   release its TMEM columns, and only then stage it (in the dS buffer, whose
-//   dQ MMA has completed) for the TMA reduce-add.
+//   release its TMEM columns, and only then stage it for the TMA reduce-add, in
+//   one round, into this step's Q and dO tiles (free once dQ(t) has completed).
+//   The reduce streams out while the next step runs; the Q/dO stage goes back to
+//   the producer at the next step's dQ phase, after the two warpgroup leaders
+//   have seen their reduces read it.
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&bars->qdo_full[s], 1);
-      mbar_init(&bars->qdo_empty[s], 1);
+      mbar_init(&bars->qdo_empty[s], 2);  // the two warpgroup leaders, once their dQ reduces read it
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
@@ -304,7 +307,6 @@ __global__ void __launch_bounds__(320, 1)
           umma_ss(tbase + C::kDPCol, sdesc_sw128(ds_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024),
                   sdesc_sw128(k_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_mm, kk > 0 ? 1u : 0u);
         umma_commit(&bars->dq_full);
-        umma_commit(&bars->qdo_empty[t % ST]);
         if (t + 1 < n_steps) {
           const int t1 = t + 1;
           if (!(ok = mbar_wait(&bars->qdo_full[t1 % ST], (t1 / ST) & 1, wg))) break;
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(320, 1)
     const int kv_row = jt * kTile + row;
     const bool kv_valid = kv_row < p.S;
     const bool leader = (row == 0);               // one thread of the warpgroup issues its TMA reduces
-    uint8_t* sds_half = smem + C::kDSOff + hf * kBoxBytes;  // dS columns [64hf, 64hf+64) / this half's staging
+    uint8_t* sds_half = smem + C::kDSOff + hf * kBoxBytes;  // dS columns [64hf, 64hf+64)
     uint64_t* wgb = &bars->wg_bar[hf];
     uint32_t wg_phase = 0;
     bool ok = true;
@@ -359,14 +361,25 @@ __global__ void __launch_bounds__(320, 1)
         tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
         tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         uint32_t pk[32];
+        const bool masked = first_visible > hf * 64 || !kv_valid;  // causal diagonal or keys past S
+        if (masked) {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const int c0 = 2 * x;
-          const float e0 = ex2_approx(fmaf(__uint_as_float(r[c0]), c, -slse[c0]));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(r[c0 + 1]), c, -slse[c0 + 1]));
-          P[c0] = (kv_valid && hf * 64 + c0 >= first_visible) ? e0 : 0.f;
-          P[c0 + 1] = (kv_valid && hf * 64 + c0 + 1 >= first_visible) ? e1 : 0.f;
-          pk[x] = pack_bf16(P[c0], P[c0 + 1]);
+          for (int x = 0; x < 32; ++x) {
+            const int c0 = 2 * x;
+            const float e0 = ex2_approx(fmaf(__uint_as_float(r[c0]), c, -slse[c0]));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(r[c0 + 1]), c, -slse[c0 + 1]));
+            P[c0] = (kv_valid && hf * 64 + c0 >= first_visible) ? e0 : 0.f;
+            P[c0 + 1] = (kv_valid && hf * 64 + c0 + 1 >= first_visible) ? e1 : 0.f;
+            pk[x] = pack_bf16(P[c0], P[c0 + 1]);
+          }
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int c0 = 2 * x;
+            P[c0] = ex2_approx(fmaf(__uint_as_float(r[c0]), c, -slse[c0]));
+            P[c0 + 1] = ex2_approx(fmaf(__uint_as_float(r[c0 + 1]), c, -slse[c0 + 1]));
+            pk[x] = pack_bf16(P[c0], P[c0 + 1]);
+          }
         }
         tmem_st_32x32b_x32(sp_tmem + hf * 64, pk);  // this half's own columns
       }
@@ -378,11 +391,6 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->dp_full, t & 1, wg));
       if (!ok) break;
       tc_fence_after();
-      if (t > 0) {
-        // the half's dS columns held the previous step's dQ staging: its reduce must have read it
-        if (leader) bulk_wait_group_read<0>();
-        if (!(ok = wg_barrier(wgb, wg_phase, wg))) break;
-      }
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         uint32_t d[32];
@@ -411,6 +419,12 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive_warp(&bars->ds_full);
 
       // ---- dQ partial (TMEM lane = query row): load this half's columns, free TMEM, reduce-add
+      if (t > 0 && leader) {
+        // Step t-1's reduces staged in the Q / dO tiles of stage (t-1) % ST; once they have read
+        // them (they had a whole step to drain), hand the stage back to the producer.
+        bulk_wait_group_read<0>();
+        mbar_arrive(&bars->qdo_empty[(t - 1) % ST]);
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, t & 1, wg));
       if (!ok) break;
       tc_fence_after();
@@ -421,24 +435,30 @@ __global__ void __launch_bounds__(320, 1)
       for (int rd = 0; rd < C::kRounds; ++rd) tmem_wait_ld_x32(dq[rd]);
       tc_fence_before();
       mbar_arrive_warp(&bars->dq_free);
-      float* stage = reinterpret_cast<float*>(sds_half);  // [128 query rows][32 f32], 128B swizzle
+      // Staging, all slices at once, into this step's Q and dO tiles (their last readers, dK(t)
+      // and dV(t), completed before dQ(t)): slice 2rd + hf goes to box 2rd + hf of [Q boxes, dO boxes].
+      auto stage_of = [&](int rd) -> float* {
+        const int box = 2 * rd + hf;
+        return reinterpret_cast<float*>(box < C::kChunks
+                                            ? smem + C::kQOff + st * C::kTileBytes + box * kBoxBytes
+                                            : smem + C::kDOOff + st * C::kTileBytes + (box - C::kChunks) * kBoxBytes);
+      };
 #pragma unroll
       for (int rd = 0; rd < C::kRounds; ++rd) {
-        if (rd > 0) {
-          if (leader) bulk_wait_group_read<0>();
-          if (!(ok = wg_barrier(wgb, wg_phase, wg))) break;
-        }
+        float* stage = stage_of(rd);
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           *reinterpret_cast<float4*>(stage + row * 32 + ((u ^ (row & 7)) << 2)) =
               make_float4(__uint_as_float(dq[rd][4 * u]), __uint_as_float(dq[rd][4 * u + 1]),
                           __uint_as_float(dq[rd][4 * u + 2]), __uint_as_float(dq[rd][4 * u + 3]));
-        fence_proxy_async_smem();
-        if (!(ok = wg_barrier(wgb, wg_phase, wg))) break;
-        if (leader) {
-          tma_reduce_add_3d(&map_acc, stage, (2 * rd + hf) * 32, i * kTile, bhq);
-          bulk_commit_group();
-        }
+      }
+      fence_proxy_async_smem();
+      if (!(ok = wg_barrier(wgb, wg_phase, wg))) break;
+      if (leader) {
+#pragma unroll
+        for (int rd = 0; rd < C::kRounds; ++rd)
+          tma_reduce_add_3d(&map_acc, stage_of(rd), (2 * rd + hf) * 32, i * kTile, bhq);
+        bulk_commit_group();
       }
       if (!ok) break;
     }

@@ -13,8 +13,9 @@
 // the TMA brings in. Warp roles (384 threads, three warpgroups):
 //   warps 0..3  softmax of tile A: thread r owns row r of A (TMEM lane r);
 //   warps 4..7  softmax of tile B (same, lanes 0..127 through the lane quarter w % 4);
-//   warp 8      TMA producer: Q_A, Q_B once, then K_j / V_j into a ring of stages;
-//   warp 9      MMA issuer (one thread) and TMEM owner; warps 10, 11 idle.
+//   warp 8      TMA producer: Q_A, Q_B once, then K_j into a ring of stages;
+//   warp 9      MMA issuer (one thread) and TMEM owner;
+//   warp 10     TMA producer: V_j into a ring of stages; warp 11 idle.
 // Registers: launched at kLaunchRegs per thread; the producer warpgroup drops
 // to kLowRegs and the two softmax warpgroups rise to kHighRegs (setmaxnreg).
 // The MMA thread alternates between the tiles: while softmax A works on S_A(j)
@@ -60,7 +61,8 @@ struct FwdBars {
   uint64_t q_full;
   uint64_t k_full[ST];
   uint64_t v_full[ST];
-  uint64_t kv_empty[ST];
+  uint64_t k_empty[ST];
+  uint64_t v_empty[ST];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
@@ -172,7 +174,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < ST; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -195,11 +198,10 @@ __global__ void __launch_bounds__(384, 1)
   if (warp >= 8) {
    setmaxnreg_dec<C::kLowRegs>();
    if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer: Q, then the K ring
     if (lane == 0) {
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
-      tma_prefetch_desc(&map_v);
       mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTileBytes);
       for (int t = 0; t < 2; ++t)
         for (int c = 0; c < C::kChunks; ++c)
@@ -209,24 +211,38 @@ __global__ void __launch_bounds__(384, 1)
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % ST;
         const int use = j / ST;
-        if (use > 0 && !mbar_wait(&bars->kv_empty[st], (use - 1) & 1, wg)) break;
-        uint8_t* sK = smem + C::kKOff + st * C::kTileBytes;
-        uint8_t* sV = smem + C::kVOff + st * C::kTileBytes;
+        if (use > 0 && !mbar_wait(&bars->k_empty[st], (use - 1) & 1, wg)) break;
         mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sK + c * kBoxBytes, &map_k, &bars->k_full[st], c * kChunk, j * kTile, kvh);
-        mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sV + c * kBoxBytes, &map_v, &bars->v_full[st], c * kChunk, j * kTile, kvh);
+          tma_load_3d(smem + C::kKOff + st * C::kTileBytes + c * kBoxBytes, &map_k, &bars->k_full[st], c * kChunk,
+                      j * kTile, kvh);
         issued = j + 1;
       }
       if (bars->abort_flag) {
         // Let every copy already issued land before the CTA's shared memory goes away.
         mbar_wait_drain(&bars->q_full, 0, kWaitLimitNs);
-        for (int j = (issued > ST ? issued - ST : 0); j < issued; ++j) {
+        for (int j = (issued > ST ? issued - ST : 0); j < issued; ++j)
           mbar_wait_drain(&bars->k_full[j % ST], (j / ST) & 1, kWaitLimitNs);
+      }
+    }
+   } else if (warp == 10) {
+    // ------------------------------------------------------------ TMA producer: the V ring
+    if (lane == 0) {
+      tma_prefetch_desc(&map_v);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % ST;
+        const int use = j / ST;
+        if (use > 0 && !mbar_wait(&bars->v_empty[st], (use - 1) & 1, wg)) break;
+        mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kVOff + st * C::kTileBytes + c * kBoxBytes, &map_v, &bars->v_full[st], c * kChunk,
+                      j * kTile, kvh);
+        issued = j + 1;
+      }
+      if (bars->abort_flag) {
+        for (int j = (issued > ST ? issued - ST : 0); j < issued; ++j)
           mbar_wait_drain(&bars->v_full[j % ST], (j / ST) & 1, kWaitLimitNs);
-        }
       }
     }
   } else if (warp == 9) {
@@ -235,7 +251,7 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
       // S_X(j) = Q_X K_j^T into the S columns of tile X.
-      auto issue_s = [&](int x, int j) {
+      auto issue_s = [=](int x, int j) {
         const uint32_t q_addr = smem_addr(smem + C::kQOff + x * C::kTileBytes);
         const uint32_t k_addr = smem_addr(smem + C::kKOff + (j % ST) * C::kTileBytes);
         const uint32_t d_tmem = tbase + (uint32_t)x * 128u;
@@ -248,7 +264,7 @@ __global__ void __launch_bounds__(384, 1)
         umma_commit(&bars->s_full[x]);
       };
       // O_X += P_X(j) V_j, P_X(j) read from the S columns of tile X.
-      auto issue_pv = [&](int x, int j) {
+      auto issue_pv = [=](int x, int j) {
         const uint32_t v_addr = smem_addr(smem + C::kVOff + (j % ST) * C::kTileBytes);
         const uint32_t p_tmem = tbase + (uint32_t)x * 128u;
         const uint32_t o_tmem = tbase + C::kOCol + (uint32_t)x * D;
@@ -258,30 +274,42 @@ __global__ void __launch_bounds__(384, 1)
                   idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars->o_done[x]);
       };
+      // K_j is released once the last S MMA reading it completes, V_j once both P V MMAs do:
+      // the K ring refills a full key tile earlier than a shared K/V stage would.
       bool ok = mbar_wait(&bars->q_full, 0, wg) && mbar_wait(&bars->k_full[0], 0, wg);
       if (ok) {
         tc_fence_after();
         if (nA > 0) issue_s(0, 0);
         if (nB > 0) issue_s(1, 0);
+        umma_commit(&bars->k_empty[0]);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         const int st = j % ST;
         const int j1 = j + 1;
+        const int st1 = j1 % ST;
         if (!(ok = mbar_wait(&bars->v_full[st], (j / ST) & 1, wg))) break;
-        if (j1 < n_kv && !(ok = mbar_wait(&bars->k_full[j1 % ST], (j1 / ST) & 1, wg))) break;
         if (j < nA) {
           if (!(ok = mbar_wait(&bars->p_full[0], j & 1, wg))) break;
           tc_fence_after();
           issue_pv(0, j);
-          if (j1 < nA) issue_s(0, j1);
+          if (j1 < nA) {
+            if (!(ok = mbar_wait(&bars->k_full[st1], (j1 / ST) & 1, wg))) break;
+            tc_fence_after();
+            issue_s(0, j1);
+          }
         }
         if (j < nB) {
           if (!(ok = mbar_wait(&bars->p_full[1], j & 1, wg))) break;
           tc_fence_after();
           issue_pv(1, j);
-          if (j1 < nB) issue_s(1, j1);
+          if (j1 < nB) {
+            if (!(ok = mbar_wait(&bars->k_full[st1], (j1 / ST) & 1, wg))) break;
+            tc_fence_after();
+            issue_s(1, j1);
+          }
         }
-        umma_commit(&bars->kv_empty[st]);
+        if (j1 < n_kv) umma_commit(&bars->k_empty[st1]);
+        umma_commit(&bars->v_empty[st]);
       }
       // Every MMA issued completes before TMEM is released.
       umma_commit(&bars->drain);
