@@ -118,7 +118,7 @@ struct BwdCfg {
   static constexpr int kRowOff = kDSOff + kDSBytes;                    // per stage: lse2[128], dvec[128]
   static constexpr int kBarOff = kRowOff + kStages * 2 * kTile * 4;
   static constexpr int kSmemBytes = kBarOff + 256;                     // the base is checked to be 1024-aligned
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
   static constexpr int kRounds = D / 64;                               // 32-column dQ slices per warpgroup
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSPCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
@@ -129,8 +129,7 @@ struct BwdBars {
   uint64_t kv_full;
   uint64_t qdo_full[ST];
   uint64_t qdo_empty[ST];
-  uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free, dkv_done, drain;
-  uint64_t wg_bar[2];  // one per element-wise warpgroup (column half)
+  uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free, stage_full, dkv_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -145,24 +144,24 @@ struct BwdKParams {
   int* status;
 };
 
-// One CTA per (batch, KV head, 128-key tile jt), 320 threads:
+// One CTA per (batch, KV head, 128-key tile jt), 352 threads:
 //   warps 0..7  element-wise work. Warp w owns TMEM lane quarter w % 4 (key
 //               rows of S^T, dP^T, dK, dV; query rows of the dQ partial) and the
 //               column half h = w / 4 (query columns [64h, 64h+64) of S^T / dP^T;
 //               dQ / dK / dV columns of that half);
 //   warp 8      TMA producer: K, V once; Q, dO, LSE2 and D rows per step, 2 stages;
-//   warp 9      MMA issuer (one thread) and TMEM owner.
+//   warp 9      MMA issuer (one thread) and TMEM owner;
+//   warp 10     dQ reduce: TMA reduce-add of each step's staged dQ partial.
 // A step is one (query head of the group, query tile i). MMA order per step t:
 //   dV(t) after P(t) is written, dK(t) and dQ(t) after dS(t) is written, then at
 //   once S(t+1) (its Q is already staged) and, once the dQ(t) columns have been
 //   read out, dP(t+1). The element-wise warps load the dQ partial into registers,
-//   release its TMEM columns, and only then stage it for the TMA reduce-add, in
-//   one round, into this step's Q and dO tiles (free once dQ(t) has completed).
-//   The reduce streams out while the next step runs; the Q/dO stage goes back to
-//   the producer at the next step's dQ phase, after the two warpgroup leaders
-//   have seen their reduces read it.
+//   release its TMEM columns, and only then stage it, in one round, into this
+//   step's Q and dO tiles (free once dQ(t) has completed). Warp 10 issues the TMA
+//   reduce-adds, waits until they have read the staging and hands the Q/dO stage
+//   back to the producer; the reduce streams out while the next step runs.
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                     const __grid_constant__ CUtensorMap map_acc, const BwdKParams p) {
@@ -194,7 +193,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&bars->qdo_full[s], 1);
-      mbar_init(&bars->qdo_empty[s], 2);  // the two warpgroup leaders, once their dQ reduces read it
+      mbar_init(&bars->qdo_empty[s], 1);  // the reduce warp, once its dQ reduces have read the stage
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
@@ -202,10 +201,9 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(&bars->ds_full, 8);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 8);
+    mbar_init(&bars->stage_full, 8);
     mbar_init(&bars->dkv_done, 1);
     mbar_init(&bars->drain, 1);
-    mbar_init(&bars->wg_bar[0], 4);
-    mbar_init(&bars->wg_bar[1], 4);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -262,29 +260,35 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idesc_kk = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both operands K-major
       constexpr uint32_t idesc_tb = idesc_bf16(128, D, false, true);     // dV, dK: A in TMEM, B MN-major
       constexpr uint32_t idesc_mm = idesc_bf16(128, D, true, true);      // dQ: A and B MN-major
-      const uint32_t k_addr = smem_addr(smem + C::kKOff);
-      const uint32_t v_addr = smem_addr(smem + C::kVOff);
-      const uint32_t ds_addr = smem_addr(smem + C::kDSOff);
-      auto q_addr = [&](int t) { return smem_addr(smem + C::kQOff + (t % ST) * C::kTileBytes); };
-      auto do_addr = [&](int t) { return smem_addr(smem + C::kDOOff + (t % ST) * C::kTileBytes); };
+      // Descriptors are built once; an MMA only adds a compile-time offset (the start-address field
+      // is the low 14 bits of the descriptor and never carries).
+      constexpr uint64_t kTileDesc = (uint64_t)(C::kTileBytes >> 4);
+      const uint64_t dk_k = sdesc_sw128(smem_addr(smem + C::kKOff), 16, 1024);          // K as K-major A
+      const uint64_t dv_k = sdesc_sw128(smem_addr(smem + C::kVOff), 16, 1024);          // V as K-major A
+      const uint64_t dk_mn = sdesc_sw128(smem_addr(smem + C::kKOff), kBoxBytes, 1024);  // K as MN-major B
+      const uint64_t dq_k0 = sdesc_sw128(smem_addr(smem + C::kQOff), 16, 1024);
+      const uint64_t dq_mn0 = sdesc_sw128(smem_addr(smem + C::kQOff), kBoxBytes, 1024);
+      const uint64_t ddo_k0 = sdesc_sw128(smem_addr(smem + C::kDOOff), 16, 1024);
+      const uint64_t ddo_mn0 = sdesc_sw128(smem_addr(smem + C::kDOOff), kBoxBytes, 1024);
+      const uint64_t dds_mn = sdesc_sw128(smem_addr(smem + C::kDSOff), kBoxBytes, 1024);
       // X^T = A B^T for a 128-row A tile (K or V) and a 128-row B tile (Q or dO), both K-major.
-      auto issue_kmajor = [&](uint32_t d_col, uint32_t a, uint32_t bb) {
+      auto issue_kmajor = [=](uint32_t d_col, uint64_t a, uint64_t bb) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
-          umma_ss(tbase + d_col, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bb + off, 16, 1024), idesc_kk,
-                  kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+          umma_ss(tbase + d_col, a + off, bb + off, idesc_kk, kk > 0 ? 1u : 0u);
         }
       };
+      auto stage_desc = [=](uint64_t base, int t) { return base + (uint64_t)(t % ST) * kTileDesc; };
       // TMEM column of the A operand (P^T; dS^T is 32 columns further) for query rows 16kk..16kk+15:
       // column half h = kk / 4 keeps its packed P^T in [64h, 64h+32) and dS^T in [64h+32, 64h+64).
       auto p_col = [](int kk) { return (uint32_t)(kk >> 2) * 64u + (uint32_t)(kk & 3) * 8u; };
       bool ok = mbar_wait(&bars->kv_full, 0, wg) && mbar_wait(&bars->qdo_full[0], 0, wg);
       if (ok) {
         tc_fence_after();
-        issue_kmajor(C::kSPCol, k_addr, q_addr(0));
+        issue_kmajor(C::kSPCol, dk_k, stage_desc(dq_k0, 0));
         umma_commit(&bars->s_full);
-        issue_kmajor(C::kDPCol, v_addr, do_addr(0));
+        issue_kmajor(C::kDPCol, dv_k, stage_desc(ddo_k0, 0));
         umma_commit(&bars->dp_full);
       }
       for (int t = 0; ok && t < n_steps; ++t) {
@@ -293,29 +297,27 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_ts(tbase + C::kDVCol, tbase + C::kSPCol + p_col(kk),
-                  sdesc_sw128(do_addr(t) + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_tb,
-                  (t > 0 || kk > 0) ? 1u : 0u);
+                  stage_desc(ddo_mn0, t) + (uint64_t)((kk * 2048) >> 4), idesc_tb, (t > 0 || kk > 0) ? 1u : 0u);
         if (!(ok = mbar_wait(&bars->ds_full, t & 1, wg))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_ts(tbase + C::kDKCol, tbase + C::kSPCol + p_col(kk) + 32u,
-                  sdesc_sw128(q_addr(t) + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_tb,
-                  (t > 0 || kk > 0) ? 1u : 0u);
+                  stage_desc(dq_mn0, t) + (uint64_t)((kk * 2048) >> 4), idesc_tb, (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ss(tbase + C::kDPCol, sdesc_sw128(ds_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024),
-                  sdesc_sw128(k_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc_mm, kk > 0 ? 1u : 0u);
+          umma_ss(tbase + C::kDPCol, dds_mn + (uint64_t)((kk * 2048) >> 4), dk_mn + (uint64_t)((kk * 2048) >> 4),
+                  idesc_mm, kk > 0 ? 1u : 0u);
         umma_commit(&bars->dq_full);
         if (t + 1 < n_steps) {
           const int t1 = t + 1;
           if (!(ok = mbar_wait(&bars->qdo_full[t1 % ST], (t1 / ST) & 1, wg))) break;
           tc_fence_after();
-          issue_kmajor(C::kSPCol, k_addr, q_addr(t1));  // P^T(t) and dS^T(t) were consumed by dV(t), dK(t)
+          issue_kmajor(C::kSPCol, dk_k, stage_desc(dq_k0, t1));  // P^T(t), dS^T(t) were consumed by dV(t), dK(t)
           umma_commit(&bars->s_full);
           if (!(ok = mbar_wait(&bars->dq_free, t & 1, wg))) break;
           tc_fence_after();
-          issue_kmajor(C::kDPCol, v_addr, do_addr(t1));
+          issue_kmajor(C::kDPCol, dv_k, stage_desc(ddo_k0, t1));
           umma_commit(&bars->dp_full);
         }
       }
@@ -323,7 +325,31 @@ __global__ void __launch_bounds__(320, 1)
       umma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, kWaitLimitNs);
     }
-  } else {
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ dQ reduce warp
+    // Issues the TMA reduce-adds of each step's staged dQ partial, waits until they have read
+    // the staging (the step's Q and dO tiles), and hands the stage back to the producer.
+    if (lane == 0) {
+      tma_prefetch_desc(&map_acc);
+      for (int t = 0; t < n_steps; ++t) {
+        if (!mbar_wait(&bars->stage_full, t & 1, wg)) break;
+        const int st = t % ST;
+        const int hl = t / n_i;
+        const int i = i_start + (t - hl * n_i);
+        const int bhq = bhq0 + hl;
+#pragma unroll
+        for (int s2 = 0; s2 < D / 32; ++s2) {
+          const uint8_t* stage = s2 < C::kChunks ? smem + C::kQOff + st * C::kTileBytes + s2 * kBoxBytes
+                                                 : smem + C::kDOOff + st * C::kTileBytes + (s2 - C::kChunks) * kBoxBytes;
+          tma_reduce_add_3d(&map_acc, stage, s2 * 32, i * kTile, bhq);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read<0>();
+        mbar_arrive(&bars->qdo_empty[st]);
+      }
+      bulk_wait_group<0>();
+    }
+  } else if (warp < 8) {
     // ------------------------------------------------------------ element-wise warps 0..7
     const int quarter = warp & 3;
     const int hf = warp >> 2;                     // column half
@@ -334,16 +360,11 @@ __global__ void __launch_bounds__(320, 1)
     const float c = p.scale_log2;
     const int kv_row = jt * kTile + row;
     const bool kv_valid = kv_row < p.S;
-    const bool leader = (row == 0);               // one thread of the warpgroup issues its TMA reduces
     uint8_t* sds_half = smem + C::kDSOff + hf * kBoxBytes;  // dS columns [64hf, 64hf+64)
-    uint64_t* wgb = &bars->wg_bar[hf];
-    uint32_t wg_phase = 0;
     bool ok = true;
     for (int t = 0; t < n_steps; ++t) {
       const int st = t % ST;
-      const int hl = t / n_i;
-      const int i = i_start + (t - hl * n_i);
-      const int bhq = bhq0 + hl;
+      const int i = i_start + (t % n_i);
       const float* slse = reinterpret_cast<const float*>(smem + C::kRowOff) + st * 2 * kTile + hf * 64;
       const float* sdv = slse + kTile;
       // visible iff key (jt*128 + row) <= query (i*128 + col): on the diagonal tile, col >= row
@@ -418,16 +439,10 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive_warp(&bars->ds_full);
 
-      // ---- dQ partial (TMEM lane = query row): load this half's columns, free TMEM, reduce-add
-      if (t > 0 && leader) {
-        // Step t-1's reduces staged in the Q / dO tiles of stage (t-1) % ST; once they have read
-        // them (they had a whole step to drain), hand the stage back to the producer.
-        bulk_wait_group_read<0>();
-        mbar_arrive(&bars->qdo_empty[(t - 1) % ST]);
-      }
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, t & 1, wg));
       if (!ok) break;
       tc_fence_after();
+      // ---- dQ partial (TMEM lane = query row): load this half's columns, free TMEM, stage it
       uint32_t dq[C::kRounds][32];
 #pragma unroll
       for (int rd = 0; rd < C::kRounds; ++rd) tmem_ld_32x32b_x32(dp_tmem + (2 * rd + hf) * 32, dq[rd]);
@@ -436,16 +451,14 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive_warp(&bars->dq_free);
       // Staging, all slices at once, into this step's Q and dO tiles (their last readers, dK(t)
-      // and dV(t), completed before dQ(t)): slice 2rd + hf goes to box 2rd + hf of [Q boxes, dO boxes].
-      auto stage_of = [&](int rd) -> float* {
-        const int box = 2 * rd + hf;
-        return reinterpret_cast<float*>(box < C::kChunks
-                                            ? smem + C::kQOff + st * C::kTileBytes + box * kBoxBytes
-                                            : smem + C::kDOOff + st * C::kTileBytes + (box - C::kChunks) * kBoxBytes);
-      };
+      // and dV(t), completed before dQ(t)): slice 2rd + hf goes to box 2rd + hf of [Q boxes,
+      // dO boxes]; the reduce warp sends them on.
 #pragma unroll
       for (int rd = 0; rd < C::kRounds; ++rd) {
-        float* stage = stage_of(rd);
+        const int box = 2 * rd + hf;
+        float* stage = reinterpret_cast<float*>(
+            box < C::kChunks ? smem + C::kQOff + st * C::kTileBytes + box * kBoxBytes
+                             : smem + C::kDOOff + st * C::kTileBytes + (box - C::kChunks) * kBoxBytes);
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           *reinterpret_cast<float4*>(stage + row * 32 + ((u ^ (row & 7)) << 2)) =
@@ -453,16 +466,9 @@ __global__ void __launch_bounds__(320, 1)
                           __uint_as_float(dq[rd][4 * u + 2]), __uint_as_float(dq[rd][4 * u + 3]));
       }
       fence_proxy_async_smem();
-      if (!(ok = wg_barrier(wgb, wg_phase, wg))) break;
-      if (leader) {
-#pragma unroll
-        for (int rd = 0; rd < C::kRounds; ++rd)
-          tma_reduce_add_3d(&map_acc, stage_of(rd), (2 * rd + hf) * 32, i * kTile, bhq);
-        bulk_commit_group();
-      }
+      mbar_arrive_warp(&bars->stage_full);
       if (!ok) break;
     }
-    if (leader) bulk_wait_group<0>();
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->dkv_done, 0, wg));
     if (ok) {
       tc_fence_after();

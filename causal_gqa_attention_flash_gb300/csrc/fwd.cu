@@ -51,8 +51,8 @@ struct FwdCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 256;
   static constexpr int kLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
-  static constexpr int kLowRegs = 64;
-  static constexpr int kHighRegs = 216;
+  static constexpr int kLowRegs = 80;
+  static constexpr int kHighRegs = 208;
   static_assert(2 * 128 * kHighRegs + 128 * kLowRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 };
 
@@ -251,27 +251,34 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
       // S_X(j) = Q_X K_j^T into the S columns of tile X.
+      // Descriptors are built once; an MMA only adds a compile-time offset (the start-address field
+      // is the low 14 bits of the descriptor and never carries). The issuing thread shares its SMSP
+      // with softmax warps, so the fewer instructions per MMA, the closer the tensor core runs to its rate.
+      const uint64_t dq0 = sdesc_sw128(smem_addr(smem + C::kQOff), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_addr(smem + C::kKOff), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(smem_addr(smem + C::kVOff), kBoxBytes, 1024);
+      constexpr uint64_t kTileDesc = (uint64_t)(C::kTileBytes >> 4);  // descriptor step of one tile
+      // S_X(j) = Q_X K_j^T into the S columns of tile X.
       auto issue_s = [=](int x, int j) {
-        const uint32_t q_addr = smem_addr(smem + C::kQOff + x * C::kTileBytes);
-        const uint32_t k_addr = smem_addr(smem + C::kKOff + (j % ST) * C::kTileBytes);
+        const uint64_t a = dq0 + (uint64_t)x * kTileDesc;
+        const uint64_t bk = dk0 + (uint64_t)(j % ST) * kTileDesc;
         const uint32_t d_tmem = tbase + (uint32_t)x * 128u;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
-          umma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc_s,
-                  kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+          umma_ss(d_tmem, a + off, bk + off, idesc_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bars->s_full[x]);
       };
       // O_X += P_X(j) V_j, P_X(j) read from the S columns of tile X.
       auto issue_pv = [=](int x, int j) {
-        const uint32_t v_addr = smem_addr(smem + C::kVOff + (j % ST) * C::kTileBytes);
+        const uint64_t bv = dv0 + (uint64_t)(j % ST) * kTileDesc;
         const uint32_t p_tmem = tbase + (uint32_t)x * 128u;
         const uint32_t o_tmem = tbase + C::kOCol + (uint32_t)x * D;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(o_tmem, p_tmem + (uint32_t)kk * 8u, sdesc_sw128(v_addr + (uint32_t)kk * 2048u, kBoxBytes, 1024),
-                  idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(o_tmem, p_tmem + (uint32_t)kk * 8u, bv + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                  (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars->o_done[x]);
       };
       // K_j is released once the last S MMA reading it completes, V_j once both P V MMAs do:
