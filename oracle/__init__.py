@@ -10,13 +10,15 @@ anything here, and nothing here imports the product.
   for workloads too large to evaluate whole.
 * ``oracle.monoid``    -- the online-softmax (m, l, acc) monoid, used to pin
   the regrouping property the flash form rests on.
+* ``oracle.decode``    -- a few new queries against a key/value cache
+  (Sq <= Sk, bottom-right causal alignment).
 
 Pins (in ``tests/``): decimal brute force, central finite differences,
 closed forms, invariants, torch f64 SDPA, monoid regrouping and a stored
 golden file. Every function here is pinned; none is "parity unpinned".
 """
 
-from . import attention, monoid  # noqa: F401
+from . import attention, decode, monoid  # noqa: F401
 from .attention import (  # noqa: F401
     backward,
     backward_dkdv_rows,
@@ -25,3 +27,4 @@ from .attention import (  # noqa: F401
     forward_rows,
     kv_head_of,
 )
+from .decode import forward_cached  # noqa: F401

@@ -334,6 +334,68 @@ def check_golden(orc):
         assert _relerr(x, a[name]) <= 1e-13, ("golden", name, _relerr(x, a[name]))
 
 
+# ---------------------------------------------------------------------------
+# 9. Cached (decode) attention: bottom-right alignment, against the full
+#    sequence, a decimal brute force with explicit positions, and torch SDPA
+#    with an explicit mask.
+# ---------------------------------------------------------------------------
+
+def brute_cached_decimal(q, k, v, causal, scale, prec=50):
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    O = np.zeros((B, Hq, Sq, D))
+    L = np.zeros((B, Hq, Sq))
+    with localcontext() as ctx:
+        ctx.prec = prec
+        sc = Decimal(float(scale))
+        for b in range(B):
+            for h in range(Hq):
+                for i in range(Sq):
+                    pos = Sk - Sq + i  # absolute position of new query i
+                    w = []
+                    for j in range(Sk):
+                        if causal and j > pos:
+                            continue
+                        dot = sum(Decimal(float(q[b, h, i, d])) * Decimal(float(k[b, h // G, j, d])) for d in range(D))
+                        w.append((j, (sc * dot).exp()))
+                    Z = sum(x for _, x in w)
+                    for d in range(D):
+                        O[b, h, i, d] = float(sum(x * Decimal(float(v[b, h // G, j, d])) for j, x in w) / Z)
+                    L[b, h, i] = float(Z.ln())
+    return O, L
+
+
+def check_decode(orc):
+    rng = _rng(18)
+    # decimal brute force, tiny
+    for (B, Hq, Hkv, Sq, Sk, D, causal) in [(1, 4, 2, 2, 5, 3, True), (1, 2, 1, 3, 3, 2, True), (1, 2, 2, 1, 4, 3, False)]:
+        q = _dyadic(rng, (B, Hq, Sq, D))
+        k = _dyadic(rng, (B, Hkv, Sk, D))
+        v = _dyadic(rng, (B, Hkv, Sk, D))
+        O, L = orc.forward_cached(q, k, v, causal=causal, scale=0.6)
+        Ob, Lb = brute_cached_decimal(q, k, v, causal, 0.6)
+        assert _relerr(O, Ob) <= 1e-14 and np.max(np.abs(L - Lb)) <= 1e-13, "cached vs decimal"
+    # the last Sq rows of the full-sequence forward
+    B, Hq, Hkv, Sk, Sq, D = 2, 6, 2, 33, 5, 8
+    qf = rng.standard_normal((B, Hq, Sk, D))
+    k = rng.standard_normal((B, Hkv, Sk, D))
+    v = rng.standard_normal((B, Hkv, Sk, D))
+    for causal in (True, False):
+        Of, Lf = orc.forward(qf, k, v, causal=causal, scale=0.4)
+        O, L = orc.forward_cached(qf[:, :, -Sq:], k, v, causal=causal, scale=0.4)
+        assert _relerr(O, Of[:, :, -Sq:]) <= 1e-14 and np.max(np.abs(L - Lf[:, :, -Sq:])) <= 1e-14, "cached = tail"
+    # torch f64 SDPA with an explicit bottom-right mask
+    q = rng.standard_normal((B, Hq, Sq, D))
+    G = Hq // Hkv
+    mask = torch.arange(Sk)[None, :] <= (Sk - Sq + torch.arange(Sq))[:, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.tensor(q), torch.tensor(k).repeat_interleave(G, dim=1), torch.tensor(v).repeat_interleave(G, dim=1),
+        attn_mask=mask, scale=0.4)
+    O, _ = orc.forward_cached(q, k, v, causal=True, scale=0.4)
+    assert _relerr(O, ref.numpy()) <= 1e-12, "cached vs torch SDPA"
+
+
 ALL_CHECKS = [
     "check_decimal_bruteforce",
     "check_finite_differences",
@@ -343,4 +405,5 @@ ALL_CHECKS = [
     "check_monoid_regrouping",
     "check_row_variants",
     "check_golden",
+    "check_decode",
 ]

@@ -16,6 +16,7 @@ import oracle_checks as oc
 from oracle import monoid
 
 SRC = (pathlib.Path(oracle.__file__).parent / "attention.py").read_text()
+DECODE_SRC = (pathlib.Path(oracle.__file__).parent / "decode.py").read_text()
 
 MUTANTS = {
     "gqa_head_mapping_modulo": ("return h // (Hq // Hkv)", "return h % Hkv"),
@@ -35,11 +36,32 @@ MUTANTS = {
 }
 
 
+DECODE_MUTANTS = {
+    "decode_top_left_alignment": ("rows = (Sk - Sq) + np.arange(Sq)", "rows = np.arange(Sq)"),
+    "decode_off_by_one_position": ("rows = (Sk - Sq) + np.arange(Sq)", "rows = (Sk - Sq - 1) + np.arange(Sq)"),
+}
+
+
 def _mutant_module(name):
     old, new = MUTANTS[name]
     assert SRC.count(old) >= 1, f"mutation anchor for {name} not found in the oracle source"
     mod = types.ModuleType(f"oracle_mutant_{name}")
     exec(compile(SRC.replace(old, new, 1), f"<mutant {name}>", "exec"), mod.__dict__)
+    mod.forward_cached = oracle.forward_cached
+    return mod
+
+
+def _decode_mutant_module(name):
+    """The real attention oracle with a mutated copy of the cached (decode) oracle."""
+    old, new = DECODE_MUTANTS[name]
+    assert DECODE_SRC.count(old) == 1
+    src = DECODE_SRC.replace(old, new, 1).replace("from .attention import", "from oracle.attention import")
+    dmod = types.ModuleType(f"oracle_decode_mutant_{name}")
+    exec(compile(src, f"<mutant {name}>", "exec"), dmod.__dict__)
+    mod = types.ModuleType(f"oracle_with_{name}")
+    mod.__dict__.update({k: getattr(oracle, k) for k in ("forward", "backward", "forward_rows",
+                                                          "backward_dq_rows", "backward_dkdv_rows")})
+    mod.forward_cached = dmod.forward_cached
     return mod
 
 
@@ -61,3 +83,10 @@ def test_planted_mistake_is_caught(name):
     mod = _mutant_module(name)
     caught_by = _first_failing_check(mod)
     assert caught_by is not None, f"no pin catches the planted mistake {name!r}"
+
+
+@pytest.mark.parametrize("name", sorted(DECODE_MUTANTS))
+def test_planted_decode_mistake_is_caught(name):
+    mod = _decode_mutant_module(name)
+    with pytest.raises(AssertionError):
+        oc.check_decode(mod)

@@ -40,6 +40,10 @@ def test_row_variants():
     oc.check_row_variants(oracle)
 
 
+def test_decode_cached_attention():
+    oc.check_decode(oracle)
+
+
 def test_golden_file():
     oc.check_golden(oracle)
 
