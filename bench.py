@@ -54,6 +54,18 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = {"bwd_main": ("bwd.cu", "ptx.cuh", "common.h"), "fwd": ("fwd.cu", "ptx.cuh", "common.h")}
+
+
+def kernel_source_hash(kernel_name):
+    """sha256 over the source files a kernel is built from (its .cu file and the shared headers)."""
+    src = os.path.join(ROOT, "causal_gqa_attention_flash_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel_name]:
+        h.update(open(os.path.join(src, f), "rb").read())
+    return h.hexdigest()
+
+
 def profiled_traffic(kernel_name, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", f"{kernel_name}_{workload}.md")
@@ -62,14 +74,7 @@ def profiled_traffic(kernel_name, workload):
     text = open(path).read()
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    if not m_bytes or not m_hash:
-        return None
-    src = os.path.join(ROOT, "causal_gqa_attention_flash_gb300", "csrc")
-    h = hashlib.sha256()
-    for f in sorted(os.listdir(src)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(src, f), "rb").read())
-    if h.hexdigest() != m_hash.group(1):
+    if not m_bytes or not m_hash or kernel_source_hash(kernel_name) != m_hash.group(1):
         return None
     return float(m_bytes.group(1))
 
@@ -167,6 +172,54 @@ def reference_arm(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+DECODE = dict(B=8, Hq=32, Hkv=8, Sq=1, Sk=16384, D=128, seed=5)
+
+
+def decode_measurement(g, torch, peaks, peak_src, steps=20, warmup=3):
+    """Split-KV decode (one new token per sequence against a 16k-token cache): HBM-bound, so the
+    metric is the cache bytes read per second against the measured HBM peak."""
+    from gqa_inputs import make_inputs
+    c = DECODE
+    _, k, v, _ = make_inputs(c["B"], c["Hq"], c["Hkv"], c["Sk"], c["D"], c["seed"], with_do=False)
+    q = make_inputs(c["B"], c["Hq"], c["Hkv"], c["Sq"], c["D"], c["seed"] + 1, with_do=False)[0]
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((c["B"], c["Hq"], c["Sq"]), device="cuda", dtype=torch.float32)
+    ws = torch.empty(g.gqa_attn_decode_workspace_size(c["B"], c["Hq"], c["Hkv"], c["Sq"], c["Sk"], c["D"], 0),
+                     device="cuda", dtype=torch.uint8)
+    # a buffer larger than L2, written between timed calls so that every call reads the cache from HBM
+    flush = torch.empty(256 << 20, device="cuda", dtype=torch.uint8)
+    for _ in range(warmup):
+        g.gqa_attn_decode_fwd(q, k, v, o=o, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    total = 0.0
+    g.gqa_attn_trace_arm()
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.gqa_attn_decode_fwd(q, k, v, o=o, lse=lse, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    tr = g.gqa_attn_trace_collect()
+    if g.gqa_attn_get_error() != 0:
+        raise RuntimeError("decode failed")
+    ms = total / steps
+    cache_bytes = 2 * k.numel() * k.element_size()
+    algo = cache_bytes + q.numel() * 2 + o.numel() * 2 + lse.numel() * 4
+    n, t = tr["decode_split"]
+    split_ms = t / max(n, 1)
+    gbs = algo / (ms * 1e-3) / 1e9
+    split_gbs = cache_bytes / (split_ms * 1e-3) / 1e9
+    peak = peaks["hbm_gbs"]
+    return {"workload": "decode: B=8 Hq=32 Hkv=8 Sq=1 Sk=16384 D=128 (one new token against a 16k cache)",
+            "value": gbs, "unit": "GB/s", "us_per_call": ms * 1e3, "l2": "256 MB buffer written between calls",
+            "kernels": {k_: {"launches": n_, "avg_ms": (t_ / n_ if n_ else None)} for k_, (n_, t_) in tr.items() if n_},
+            "roofline": {"kernel": "decode_split", "bound": "hbm", "achieved": split_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": split_gbs / peak, "traffic": None, "peak_source": f"{peak_src} HBM copy"}}
+
+
 def config_of(w):
     return {"workload": f"{w.name}: causal GQA B={w.B} Hq={w.Hq} Hkv={w.Hkv} S={w.S} D={w.D}",
             "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": True, "scale": w.scale,
@@ -185,6 +238,7 @@ def main():
                     help="B,Hq,Hkv,S,D: override the workload's shape (same seed and value distributions); "
                          "for profiling smaller cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode measurement")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -328,12 +382,15 @@ def main():
                      "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16 dense, sustained (kernel timed inside back-to-back steps)",
                      "fwd_kernel": {"achieved": fwd_fl / (fwd_avg / 1e3) / 1e12,
-                                    "frac": fwd_fl / (fwd_avg / 1e3) / 1e12 / peak_tf}},
+                                    "frac": fwd_fl / (fwd_avg / 1e3) / 1e12 / peak_tf,
+                                    "traffic": profiled_traffic("fwd", w.name)}},
         "e2e": {"value": world * step_fl / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
+    if world == 1 and not args.no_decode:
+        line["decode"] = decode_measurement(g, torch, peaks, peak_src)
     if world == 1 and not args.no_cpu_baseline:
         val, desc, cores = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}

@@ -35,12 +35,14 @@ __all__ = [
     "gqa_attn_trace_arm",
     "gqa_attn_trace_collect",
     "gqa_attn_bwd_noalloc",
+    "gqa_attn_decode_fwd",
+    "gqa_attn_decode_workspace_size",
     "NOALLOC_SCRATCH_BYTES",
     "KERNEL_NAMES",
     "lib_path",
 ]
 
-KERNEL_NAMES = ("fwd", "bwd_prep", "bwd_main", "bwd_convert")
+KERNEL_NAMES = ("fwd", "bwd_prep", "bwd_main", "bwd_convert", "decode_split", "decode_combine")
 
 GQA_OK = 0
 GQA_ERR_INVALID_ARG = -1
@@ -189,3 +191,33 @@ def gqa_attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, causal: bool = True, s
                                           B, Hq, Hkv, S, D, int(bool(causal)), float(scale), _stream_handle(stream))
     _check(rc, "gqa_attn_bwd_noalloc")
     return dq, dk, dv
+
+
+def gqa_attn_decode_workspace_size(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, D: int, num_splits: int = 0) -> int:
+    return int(_lib.load().gqa_attn_decode_workspace_size(B, Hq, Hkv, Sq, Sk, D, num_splits))
+
+
+def gqa_attn_decode_fwd(q, k_cache, v_cache, causal: bool = True, scale: float | None = None, num_splits: int = 0,
+                        o=None, lse=None, workspace=None, stream=None):
+    """Attention of q [B,Hq,Sq,D] against a cache k/v [B,Hkv,Sk,D] (Sq <= Sk, query i at position
+    Sk - Sq + i). Returns (o [B,Hq,Sq,D] bf16, lse [B,Hq,Sq] f32)."""
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D bfloat16 CUDA tensor (BHSD)")
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape != (B, Hkv, Sk, D) or v_cache.shape != k_cache.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k_cache.shape)}, v {tuple(v_cache.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32) if lse is None else lse
+    need = gqa_attn_decode_workspace_size(B, Hq, Hkv, Sq, Sk, D, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = _lib.load().gqa_attn_decode_fwd(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), workspace.data_ptr(), nbytes, B, Hq, Hkv, Sq, Sk, D,
+                                         int(bool(causal)), float(scale), int(num_splits), _stream_handle(stream))
+    _check(rc, "gqa_attn_decode_fwd")
+    return o, lse

@@ -20,6 +20,8 @@ SIGNATURES = {
     "gqa_attn_trace_arm": (_c_int, []),
     "gqa_attn_trace_collect": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(ctypes.c_double)]),
     "gqa_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_c_float, _vp]),
+    "gqa_attn_decode_workspace_size": (_sz, [_c_int] * 7),
+    "gqa_attn_decode_fwd": (_c_int, [_vp] * 6 + [_sz] + [_c_int] * 7 + [_c_float, _c_int, _vp]),
 }
 
 _lib = None

@@ -227,6 +227,105 @@ int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   return GQA_OK;
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------------------ decode
+
+namespace gqa {
+namespace {
+
+int device_sms() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+    return v;
+  return 148;
+}
+
+// Key chunk per split (a multiple of the 128-key tile) and the number of non-empty splits.
+void decode_split_plan(int B, int Hkv, int Sk, int num_splits, int* splits, int* chunk) {
+  const int tiles = (Sk + kTile - 1) / kTile;
+  int s = num_splits;
+  if (s <= 0) {
+    const int units = B * Hkv;
+    s = (2 * device_sms() + units - 1) / units;  // about two CTAs per SM
+  }
+  if (s > tiles) s = tiles;
+  if (s < 1) s = 1;
+  const int tiles_per = (tiles + s - 1) / s;
+  *chunk = tiles_per * kTile;
+  *splits = (tiles + tiles_per - 1) / tiles_per;
+}
+
+int decode_rows_padded(int R) { return R <= 1 ? 1 : R <= 2 ? 2 : R <= 4 ? 4 : R <= 8 ? 8 : 16; }
+
+int check_decode(int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1 || Sq > Sk || Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return GQA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
+  if ((Hq / Hkv) * Sq > kMaxDecodeRows) return GQA_ERR_UNSUPPORTED;
+  if ((long long)B * Hkv >= 65536 || (long long)B * Hq * Sq >= (1ll << 26)) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+size_t decode_workspace(int B, int Hq, int Hkv, int Sq, int Sk, int D, int num_splits, size_t* ml_off) {
+  int splits = 1, chunk = kTile;
+  decode_split_plan(B, Hkv, Sk, num_splits, &splits, &chunk);
+  const size_t rows = (size_t)B * Hkv * splits * decode_rows_padded((Hq / Hkv) * Sq);
+  *ml_off = align256(rows * D * sizeof(float));
+  return align256(*ml_off + rows * 2 * sizeof(float));
+}
+
+}  // namespace
+}  // namespace gqa
+
+extern "C" {
+
+size_t gqa_attn_decode_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int num_splits) {
+  if (check_decode(B, Hq, Hkv, Sq, Sk, D, 1.0f) != GQA_OK) return 0;
+  size_t ml = 0;
+  return decode_workspace(B, Hq, Hkv, Sq, Sk, D, num_splits, &ml);
+}
+
+int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                        void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                        int causal, float scale, int num_splits, void* stream) {
+  if (!q || !k_cache || !v_cache || !o || !lse || !workspace) return GQA_ERR_INVALID_ARG;
+  int rc = check_decode(B, Hq, Hkv, Sq, Sk, D, scale);
+  if (rc != GQA_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(workspace, 256))
+    return GQA_ERR_INVALID_ARG;
+  size_t ml_off = 0;
+  const size_t need = decode_workspace(B, Hq, Hkv, Sq, Sk, D, num_splits, &ml_off);
+  if (workspace_bytes < need) return GQA_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap mk, mv;
+  cudaError_t e;
+  if ((e = encode_bf16(&mk, k_cache, D, Sk, B * Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mv, v_cache, D, Sk, B * Hkv)) != cudaSuccess) return fail_cuda(e);
+  int* status = nullptr;
+  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  DecodeArgs a;
+  a.map_k = &mk;
+  a.map_v = &mv;
+  a.q = q;
+  a.o = o;
+  a.lse = lse;
+  a.part_acc = static_cast<float*>(workspace);
+  a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ml_off);
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.D = D;
+  a.causal = causal ? 1 : 0;
+  decode_split_plan(B, Hkv, Sk, num_splits, &a.splits, &a.chunk);
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  a.status = status;
+  if ((e = launch_decode(a, static_cast<cudaStream_t>(stream))) != cudaSuccess) return fail_cuda(e);
+  return GQA_OK;
+}
+
 int gqa_attn_get_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);

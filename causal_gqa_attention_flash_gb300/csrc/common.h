@@ -51,6 +51,22 @@ struct BwdArgs {
   int* status;
 };
 
+// Query rows (G heads x Sq new queries) one decode CTA handles for a KV head.
+constexpr int kMaxDecodeRows = 16;
+
+struct DecodeArgs {
+  const CUtensorMap* map_k;  // [B*Hkv, Sk, D] bf16 cache
+  const CUtensorMap* map_v;
+  const void* q;             // bf16 [B, Hq, Sq, D]
+  void* o;                   // bf16 [B, Hq, Sq, D]
+  float* lse;                // f32 [B, Hq, Sq]
+  float* part_acc;           // f32 [B*Hkv, splits, rows, D]
+  float* part_ml;            // f32 [B*Hkv, splits, rows, 2]
+  int B, Hq, Hkv, Sq, Sk, D, causal, splits, chunk;
+  float scale_log2;
+  int* status;
+};
+
 // Workspace sections of the backward (byte offsets, each 256-aligned).
 struct BwdWorkspace {
   size_t dvec_off, lse2_off, dqacc_off, total;
@@ -69,7 +85,15 @@ inline BwdWorkspace bwd_workspace_layout(int B, int Hq, int S, int D) {
 }
 
 // Tracing hooks (api.cu): no-ops unless the calling host thread armed tracing.
-enum KernelKind { kKernelFwd = 0, kKernelBwdPrep = 1, kKernelBwdMain = 2, kKernelBwdConvert = 3, kKernelCount = 4 };
+enum KernelKind {
+  kKernelFwd = 0,
+  kKernelBwdPrep = 1,
+  kKernelBwdMain = 2,
+  kKernelBwdConvert = 3,
+  kKernelDecodeSplit = 4,
+  kKernelDecodeCombine = 5,
+  kKernelCount = 6
+};
 void trace_begin(int kind, cudaStream_t s);
 void trace_end(int kind, cudaStream_t s);
 
@@ -80,5 +104,6 @@ int record_cuda_error(cudaError_t e);
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace gqa

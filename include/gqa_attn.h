@@ -104,6 +104,29 @@ int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int D, int causal, float scale, void* stream);
 
 /*
+ * Decode: attention of Sq new query rows against a key/value cache of Sk >= Sq
+ * rows (KV-cached decoding / prefill over a cache).
+ *   q [B,Hq,Sq,D] (bf16, device): the new queries, query i at absolute
+ *     position Sk - Sq + i; k_cache, v_cache [B,Hkv,Sk,D] (bf16, device);
+ *   o [B,Hq,Sq,D] (bf16, device), lse [B,Hq,Sq] (f32, device) as in gqa_attn_fwd.
+ *   causal: key j visible to query i iff j <= Sk - Sq + i (bottom-right).
+ *   num_splits: number of key chunks processed in parallel (<= 0: chosen
+ *     from the device's SM count); the chunk states are merged with the
+ *     associative (m, l, acc) combine.
+ *   workspace: device memory of gqa_attn_decode_workspace_size() bytes (same
+ *     num_splits), 256-byte aligned, owned by the caller (per-chunk partials).
+ * Supported: D in {64, 128}; (Hq/Hkv) * Sq <= 16 query rows per KV head.
+ * Errors as gqa_attn_fwd; GQA_ERR_UNSUPPORTED for more than 16 rows per KV head.
+ * Passage: RustingBrain docs, "Training infrastructure" (KV-cached decoding);
+ * tang page, "How tang works" section 3 (the combine is associative, so the
+ * key range splits and the parts recombine).
+ */
+size_t gqa_attn_decode_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int num_splits);
+int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                        void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                        int causal, float scale, int num_splits, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device. Returns GQA_OK, GQA_ERR_TIMEOUT if a kernel gave up on a
  * wait since the last call, GQA_ERR_INTERNAL if a kernel's own shared-memory
@@ -142,7 +165,9 @@ int gqa_attn_selftest_wait_timeout(int limit_us, void* stream);
 #define GQA_KERNEL_BWD_PREP 1
 #define GQA_KERNEL_BWD_MAIN 2
 #define GQA_KERNEL_BWD_CONVERT 3
-#define GQA_KERNEL_COUNT 4
+#define GQA_KERNEL_DECODE_SPLIT 4
+#define GQA_KERNEL_DECODE_COMBINE 5
+#define GQA_KERNEL_COUNT 6
 int gqa_attn_trace_arm(void);
 int gqa_attn_trace_collect(int* launches, double* total_ms);
 
