@@ -242,12 +242,26 @@ int device_sms() {
 }
 
 // Key chunk per split (a multiple of the 128-key tile) and the number of non-empty splits.
+// Automatic choice: the split count that minimises (waves of CTAs) x (key tiles per CTA + one
+// tile's worth of per-CTA overhead), one decode CTA per SM, so that the last wave is not mostly
+// empty and CTAs are not too short.
 void decode_split_plan(int B, int Hkv, int Sk, int num_splits, int* splits, int* chunk) {
   const int tiles = (Sk + kTile - 1) / kTile;
   int s = num_splits;
   if (s <= 0) {
-    const int units = B * Hkv;
-    s = (2 * device_sms() + units - 1) / units;  // about two CTAs per SM
+    const long long units = (long long)B * Hkv;
+    const long long sms = device_sms();
+    long long best = -1;
+    s = 1;
+    for (int c = 1; c <= tiles && c <= 256; ++c) {
+      const long long per = (tiles + c - 1) / c;
+      const long long waves = (units * c + sms - 1) / sms;
+      const long long cost = waves * (per + 1) * 64 + c;  // small tie-break toward fewer chunks
+      if (best < 0 || cost < best) {
+        best = cost;
+        s = c;
+      }
+    }
   }
   if (s > tiles) s = tiles;
   if (s < 1) s = 1;

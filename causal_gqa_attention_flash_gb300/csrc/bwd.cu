@@ -134,6 +134,10 @@ struct BwdBars {
   int abort_flag;
 };
 
+static_assert(sizeof(BwdBars<BwdCfg<64>::kStages>) <= 256 && sizeof(BwdBars<BwdCfg<128>::kStages>) <= 256,
+              "backward barriers exceed the 256 bytes reserved for them");
+static_assert(BwdCfg<64>::kSmemBytes <= 232448 && BwdCfg<128>::kSmemBytes <= 232448, "backward smem over the limit");
+
 struct BwdKParams {
   const float* lse2;
   const float* dvec;

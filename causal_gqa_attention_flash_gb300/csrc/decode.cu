@@ -31,15 +31,18 @@ template <int D>
 struct DecCfg {
   static constexpr int kChunks = D / kChunk;
   static constexpr int kTileBytes = kTile * D * 2;   // 128 keys
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kStages = (D == 64) ? 6 : 3;  // ~192 KB of K/V in flight per CTA
   static constexpr int kDC = D / 32;                 // head-dim columns per lane in P.V
   static constexpr int kQOff = 0;                    // f32 [kMaxRows][D], pre-scaled by scale*log2(e)
   static constexpr int kKOff = kMaxDecodeRows * D * 4;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kRedOff = kVOff + kStages * kTileBytes;  // warp states for the final combine
+  // warp states for the final combine, over the K/V ring (every tile has been consumed by then)
+  static constexpr int kRedOff = kKOff;
   static constexpr int kRedBytes = kDecWarps * kMaxDecodeRows * (D + 2) * 4;
-  static constexpr int kBarOff = kRedOff + kRedBytes;
-  static constexpr int kSmemBytes = kBarOff + 128;
+  static_assert(kRedBytes <= 2 * kStages * kTileBytes, "combine buffer must fit in the K/V ring");
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBarBytes = 256;  // DecBars<kStages>, checked below
+  static constexpr int kSmemBytes = kBarOff + kBarBytes;
 };
 
 template <int ST>
@@ -47,6 +50,9 @@ struct DecBars {
   uint64_t k_full[ST], v_full[ST], kv_empty[ST];
   int abort_flag;
 };
+static_assert(sizeof(DecBars<DecCfg<64>::kStages>) <= DecCfg<64>::kBarBytes, "decode barriers exceed their space");
+static_assert(sizeof(DecBars<DecCfg<128>::kStages>) <= DecCfg<128>::kBarBytes, "decode barriers exceed their space");
+static_assert(DecCfg<64>::kSmemBytes <= 232448 && DecCfg<128>::kSmemBytes <= 232448, "decode smem over the limit");
 
 struct DecKParams {
   const uint16_t* q;   // [B, Hq, Sq, D]
@@ -115,6 +121,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
   __syncthreads();
 
+  // this warp's softmax state over its keys (compute warps only)
+  float m[R], l[R], acc[R][C::kDC];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int c = 0; c < C::kDC; ++c) acc[r][c] = 0.f;
+  }
   if (warp == kDecWarps) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -134,14 +149,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ compute warps
-    float m[R], l[R], acc[R][C::kDC];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      m[r] = -INFINITY;
-      l[r] = 0.f;
-#pragma unroll
-      for (int c = 0; c < C::kDC; ++c) acc[r][c] = 0.f;
-    }
     const int kk = warp * 32 + lane;  // this lane's key within a 128-key tile (scores)
     for (int t = 0; t < n_tiles; ++t) {
       const int st = t % ST;
@@ -224,6 +231,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       mbar_arrive_warp(&bars->kv_empty[st]);
     }
+  }
+  // The combine buffer overlays the K/V ring: every warp must be done with its tiles first.
+  __syncthreads();
+  if (warp < kDecWarps) {
     // ---- combine the warps' states (same monoid) and write this chunk's partial
     float* red = reinterpret_cast<float*>(smem + C::kRedOff);  // [warp][R][D + 2]
 #pragma unroll

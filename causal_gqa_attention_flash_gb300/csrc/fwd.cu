@@ -72,6 +72,10 @@ struct FwdBars {
   int abort_flag;
 };
 
+static_assert(sizeof(FwdBars<FwdCfg<64>::kStages>) <= 256 && sizeof(FwdBars<FwdCfg<128>::kStages>) <= 256,
+              "forward barriers exceed the 256 bytes reserved for them");
+static_assert(FwdCfg<64>::kSmemBytes <= 232448 && FwdCfg<128>::kSmemBytes <= 232448, "forward smem over the limit");
+
 struct FwdKParams {
   float* lse;
   int Hq, Hkv, S, causal, n_tiles;
