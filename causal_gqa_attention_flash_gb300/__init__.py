@@ -36,6 +36,7 @@ __all__ = [
     "gqa_attn_trace_collect",
     "gqa_attn_bwd_noalloc",
     "gqa_attn_decode_fwd",
+    "gqa_attn_fwd_cached",
     "gqa_attn_decode_workspace_size",
     "NOALLOC_SCRATCH_BYTES",
     "KERNEL_NAMES",
@@ -220,4 +221,26 @@ def gqa_attn_decode_fwd(q, k_cache, v_cache, causal: bool = True, scale: float |
                                          lse.data_ptr(), workspace.data_ptr(), nbytes, B, Hq, Hkv, Sq, Sk, D,
                                          int(bool(causal)), float(scale), int(num_splits), _stream_handle(stream))
     _check(rc, "gqa_attn_decode_fwd")
+    return o, lse
+
+
+def gqa_attn_fwd_cached(q, k_cache, v_cache, causal: bool = True, scale: float | None = None, o=None, lse=None,
+                        stream=None):
+    """Forward of q [B,Hq,Sq,D] over k/v [B,Hkv,Sk,D] (Sq <= Sk, query r at position Sk - Sq + r),
+    on the tensor cores. Returns (o [B,Hq,Sq,D] bf16, lse [B,Hq,Sq] f32)."""
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D bfloat16 CUDA tensor (BHSD)")
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape != (B, Hkv, Sk, D) or v_cache.shape != k_cache.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k_cache.shape)}, v {tuple(v_cache.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32) if lse is None else lse
+    rc = _lib.load().gqa_attn_fwd_cached(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), float(scale),
+                                         _stream_handle(stream))
+    _check(rc, "gqa_attn_fwd_cached")
     return o, lse

@@ -138,19 +138,20 @@ using namespace gqa;
 
 extern "C" {
 
-int gqa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
-                 int D, int causal, float scale, void* stream) {
+int gqa_attn_fwd_cached(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Sq, int Sk, int D, int causal, float scale, void* stream) {
   if (!q || !k || !v || !o || !lse) return GQA_ERR_INVALID_ARG;
-  int rc = check_common(B, Hq, Hkv, S, D, scale);
+  if (Sq < 1 || Sq > Sk) return GQA_ERR_INVALID_ARG;
+  int rc = check_common(B, Hq, Hkv, Sk, D, scale);
   if (rc != GQA_OK) return rc;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return GQA_ERR_INVALID_ARG;
   CUtensorMap mq, mk, mv, mo;
   cudaError_t e;
-  if ((e = encode_bf16(&mq, q, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
-  if ((e = encode_bf16(&mk, k, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
-  if ((e = encode_bf16(&mv, v, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
-  if ((e = encode_bf16(&mo, o, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mq, q, D, Sq, B * Hq)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mk, k, D, Sk, B * Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mv, v, D, Sk, B * Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mo, o, D, Sq, B * Hq)) != cudaSuccess) return fail_cuda(e);
   int* status = nullptr;
   if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
   FwdArgs a;
@@ -162,13 +163,19 @@ int gqa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
-  a.S = S;
+  a.Sq = Sq;
+  a.Sk = Sk;
   a.D = D;
   a.causal = causal ? 1 : 0;
   a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   a.status = status;
   if ((e = launch_fwd(a, static_cast<cudaStream_t>(stream))) != cudaSuccess) return fail_cuda(e);
   return GQA_OK;
+}
+
+int gqa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
+                 int D, int causal, float scale, void* stream) {
+  return gqa_attn_fwd_cached(q, k, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, stream);
 }
 
 size_t gqa_attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D) {

@@ -18,9 +18,9 @@
 //                 reduce-add of the f32 partial into the accumulator;
 //   bwd_convert   dQ = bf16(scale * accumulator);                     HBM-bound
 //
-// bwd_main warp roles: warp 4 = TMA producer, warp 5 = MMA issuer, warps 0..3
-// = element-wise work, thread r owning TMEM lane r (key row r for S^T, dP^T,
-// dK, dV; query row r for the dQ partial).
+// bwd_main warp roles are listed above the kernel; element-wise thread r of a
+// lane quarter owns TMEM lane r (key row r for S^T, dP^T, dK, dV; query row r
+// for the dQ partial).
 // TMEM columns: [0,128) S^T f32; column half h (query columns [64h, 64h+64))
 // then holds its packed bf16 P^T in [64h, 64h+32) and dS^T in [64h+32, 64h+64),
 // written only by the warpgroup that read those S^T columns; [128,256) dP^T

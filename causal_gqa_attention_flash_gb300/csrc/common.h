@@ -21,12 +21,12 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 struct FwdArgs {
-  const CUtensorMap* map_q;  // [B*Hq, S, D] bf16, box {64, 128, 1}, 128B swizzle
-  const CUtensorMap* map_k;  // [B*Hkv, S, D]
+  const CUtensorMap* map_q;  // [B*Hq, Sq, D] bf16, box {64, 128, 1}, 128B swizzle
+  const CUtensorMap* map_k;  // [B*Hkv, Sk, D]
   const CUtensorMap* map_v;
-  const CUtensorMap* map_o;  // [B*Hq, S, D] bf16 (TMA store of O)
-  float* lse;                // f32 [B, Hq, S]
-  int B, Hq, Hkv, S, D, causal;
+  const CUtensorMap* map_o;  // [B*Hq, Sq, D] bf16 (TMA store of O)
+  float* lse;                // f32 [B, Hq, Sq]
+  int B, Hq, Hkv, Sq, Sk, D, causal;  // Sq <= Sk; query r at absolute position Sk - Sq + r
   float scale_log2;          // scale * log2(e)
   int* status;               // device status word
 };

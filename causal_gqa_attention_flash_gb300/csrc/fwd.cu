@@ -78,7 +78,9 @@ static_assert(FwdCfg<64>::kSmemBytes <= 232448 && FwdCfg<128>::kSmemBytes <= 232
 
 struct FwdKParams {
   float* lse;
-  int Hq, Hkv, S, causal, n_tiles;
+  // Sq query rows against Sk >= Sq keys; query row r sits at absolute position koff + r,
+  // koff = Sk - Sq (0 for self-attention), and (causal) sees keys j <= koff + r.
+  int Hq, Hkv, Sq, Sk, koff, causal, n_ktiles;
   float scale_log2;
   int* status;
 };
@@ -142,10 +144,12 @@ __device__ __forceinline__ float exp_pack_store(const uint32_t (&r)[128], int la
   return sum0 + sum1;
 }
 
-// Number of key tiles query tile qt (first row q0) visits; 0 if the tile lies past S.
-__device__ __forceinline__ int kv_tiles_of(int qt, int S, int causal, int n_tiles) {
-  if (qt * kTile >= S) return 0;
-  return causal ? (qt + 1) : n_tiles;
+// Number of key tiles query tile qt visits; 0 if the tile lies past Sq.
+__device__ __forceinline__ int kv_tiles_of(int qt, const FwdKParams& p) {
+  if (qt * kTile >= p.Sq) return 0;
+  if (!p.causal) return p.n_ktiles;
+  const int last_row = min(p.Sq - 1, qt * kTile + kTile - 1);
+  return (p.koff + last_row) / kTile + 1;
 }
 
 template <int D>
@@ -168,8 +172,8 @@ __global__ void __launch_bounds__(384, 1)
   const int h = bh - b * p.Hq;
   const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int qtA = 2 * pair, qtB = 2 * pair + 1;
-  const int nA = kv_tiles_of(qtA, p.S, p.causal, p.n_tiles);
-  const int nB = kv_tiles_of(qtB, p.S, p.causal, p.n_tiles);
+  const int nA = kv_tiles_of(qtA, p);
+  const int nB = kv_tiles_of(qtB, p);
   const int n_kv = nA > nB ? nA : nB;
   const WaitGuard wg{&bars->abort_flag, p.status, kWaitLimitNs};
 
@@ -352,9 +356,14 @@ __global__ void __launch_bounds__(384, 1)
       for (int q = 0; q < 4; ++q) tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[32 * q]));
 
       const int kv0 = j * kTile;
-      const bool diag = p.causal && (j == qt);
-      const bool tail = !p.causal && (kv0 + kTile > p.S);
-      const int last = diag ? row : (tail ? (p.S - kv0 - 1) : (kTile - 1));  // last visible local key
+      // last visible local key of this row in key tile j: the causal bound koff + q - kv0 and the
+      // end of the keys; tiles where some row sees fewer than 128 keys take the masked path.
+      const int qpos = p.koff + qt * kTile;  // absolute position of the tile's first row
+      const bool diag = p.causal && (qpos < kv0 + kTile - 1);
+      const bool tail = kv0 + kTile > p.Sk;
+      int last = kTile - 1;
+      if (diag) last = min(last, qpos + row - kv0);
+      if (tail) last = min(last, p.Sk - kv0 - 1);
       const bool masked = diag || tail;
       const float mx = masked ? row_max<true>(r, last) : row_max<false>(r, last);
       const float m_tile = mx * c;
@@ -423,7 +432,7 @@ __global__ void __launch_bounds__(384, 1)
         bulk_commit_group();
       }
       const int qrow = qt * kTile + row;
-      if (qrow < p.S) p.lse[(size_t)bh * p.S + qrow] = (m_ref + __log2f(l)) * 0.69314718055994530942f;
+      if (qrow < p.Sq) p.lse[(size_t)bh * p.Sq + qrow] = (m_ref + __log2f(l)) * 0.69314718055994530942f;
       if (row == 0) bulk_wait_group_read<0>();
     }
     tc_fence_before();
@@ -443,9 +452,11 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.lse = a.lse;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
-  p.S = a.S;
+  p.Sq = a.Sq;
+  p.Sk = a.Sk;
+  p.koff = a.Sk - a.Sq;
   p.causal = a.causal;
-  p.n_tiles = ceil_div(a.S, kTile);
+  p.n_ktiles = ceil_div(a.Sk, kTile);
   p.scale_log2 = a.scale_log2;
   p.status = a.status;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -455,7 +466,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   cudaFuncAttributes fa;
   if ((e = cudaFuncGetAttributes(&fa, fwd_kernel<D>)) != cudaSuccess) return e;
   if (fa.numRegs * C::kThreads < 2 * 128 * C::kHighRegs + 128 * C::kLowRegs) return cudaErrorInvalidConfiguration;
-  dim3 grid((unsigned)(a.B * a.Hq), (unsigned)ceil_div(a.S, 2 * kTile));
+  dim3 grid((unsigned)(a.B * a.Hq), (unsigned)ceil_div(a.Sq, 2 * kTile));
   trace_begin(kKernelFwd, stream);
   fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_o, p);
   e = cudaGetLastError();

@@ -75,6 +75,20 @@ int gqa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int D, int causal, float scale, void* stream);
 
 /*
+ * Forward over a key/value cache: Sq <= Sk query rows against Sk keys, query r
+ * at absolute position Sk - Sq + r (causal: sees keys j <= Sk - Sq + r, the
+ * bottom-right alignment; Sq = Sk is gqa_attn_fwd). Prefill of Sq new tokens
+ * over a cache, on the tensor cores (gqa_attn_decode_fwd serves Sq with at
+ * most 16 rows per KV head, split over key chunks).
+ *   q, o [B,Hq,Sq,D], k, v [B,Hkv,Sk,D] (bf16, device), lse [B,Hq,Sq] (f32).
+ * Errors as gqa_attn_fwd; GQA_ERR_INVALID_ARG if Sq < 1 or Sq > Sk.
+ * Passage: RustingBrain docs, "Training infrastructure" (KV-cached decoding);
+ * tang page, "An LLM" (prefill 512).
+ */
+int gqa_attn_fwd_cached(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Sq, int Sk, int D, int causal, float scale, void* stream);
+
+/*
  * Size in bytes of the device workspace gqa_attn_bwd needs (256-byte aligned
  * sections: the per-row D = rowsum(dO * O) and the scaled LSE, f32
  * [B,Hq,ceil(S/128)*128] each, and the f32 dQ accumulator [B,Hq,S,D]).
