@@ -396,6 +396,73 @@ def check_decode(orc):
     assert _relerr(O, ref.numpy()) <= 1e-12, "cached vs torch SDPA"
 
 
+# ---------------------------------------------------------------------------
+# 10. Packed variable-length batches: torch f64 SDPA over the whole pack with an
+#     explicit mask (same sequence, bottom-right causal within it), forward and
+#     autograd backward; reversing the order of the sequences in the pack
+#     reverses the result.
+# ---------------------------------------------------------------------------
+
+def _pack_mask(cq, ck, causal):
+    Tq, Tk = int(cq[-1]), int(ck[-1])
+    mask = torch.zeros(Tq, Tk, dtype=torch.bool)
+    for i in range(len(cq) - 1):
+        nq, nk = int(cq[i + 1] - cq[i]), int(ck[i + 1] - ck[i])
+        r = torch.arange(nq)[:, None]
+        j = torch.arange(nk)[None, :]
+        blk = (j <= (nk - nq) + r) if causal else torch.ones(nq, nk, dtype=torch.bool)
+        mask[cq[i]:cq[i + 1], ck[i]:ck[i + 1]] = blk
+    return mask
+
+
+def _sdpa_pack(q, k, v, cq, ck, causal, scale, G):
+    mask = _pack_mask(cq, ck, causal)
+    return torch.nn.functional.scaled_dot_product_attention(
+        q[None], k.repeat_interleave(G, dim=0)[None], v.repeat_interleave(G, dim=0)[None],
+        attn_mask=mask, scale=scale)[0]
+
+
+def check_varlen(orc):
+    rng = _rng(19)
+    Hq, Hkv, D, scale = 6, 2, 8, 0.45
+    G = Hq // Hkv
+    # forward: separate query and key bounds, an empty sequence, Sq < Sk and Sq = Sk
+    cq = np.array([0, 3, 3, 10, 11])
+    ck = np.array([0, 5, 7, 14, 19])
+    q = rng.standard_normal((Hq, cq[-1], D))
+    k = rng.standard_normal((Hkv, ck[-1], D))
+    v = rng.standard_normal((Hkv, ck[-1], D))
+    for causal in (True, False):
+        O, L = orc.forward_varlen(q, k, v, cq, ck, causal=causal, scale=scale)
+        ref = _sdpa_pack(torch.tensor(q), torch.tensor(k), torch.tensor(v), cq, ck, causal, scale, G)
+        assert _relerr(O, ref.numpy()) <= 1e-12, f"varlen forward vs torch SDPA (causal={causal})"
+        s = scale * np.einsum("htd,hsd->hts", q, np.repeat(k, G, axis=0))
+        s = np.where(_pack_mask(cq, ck, causal).numpy()[None], s, -np.inf)
+        m = s.max(axis=2)
+        assert np.max(np.abs(L - (m + np.log(np.exp(s - m[..., None]).sum(axis=2))))) <= 1e-12, "varlen LSE"
+    # backward, packed self-attention
+    cu = np.array([0, 4, 5, 12, 12, 20])
+    T = int(cu[-1])
+    q = rng.standard_normal((Hq, T, D))
+    k = rng.standard_normal((Hkv, T, D))
+    v = rng.standard_normal((Hkv, T, D))
+    dO = rng.standard_normal((Hq, T, D))
+    for causal in (True, False):
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        out = _sdpa_pack(tq, tk, tv, cu, cu, causal, scale, G)
+        (out * torch.tensor(dO)).sum().backward()
+        dQ, dK, dV = orc.backward_varlen(q, k, v, dO, cu, causal=causal, scale=scale)
+        for name, mine, ref in (("dQ", dQ, tq.grad), ("dK", dK, tk.grad), ("dV", dV, tv.grad)):
+            assert _relerr(mine, ref.numpy()) <= 1e-11, f"varlen {name} vs torch autograd (causal={causal})"
+    # reversing the sequences of the pack reverses the result
+    lens = np.diff(cu)
+    rev_cu = np.concatenate([[0], np.cumsum(lens[::-1])])
+    perm = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in reversed(range(len(lens)))])
+    O1, L1 = orc.forward_varlen(q, k, v, cu, cu, causal=True, scale=scale)
+    O2, L2 = orc.forward_varlen(q[:, perm], k[:, perm], v[:, perm], rev_cu, rev_cu, causal=True, scale=scale)
+    assert np.array_equal(O1[:, perm], O2) and np.array_equal(L1[:, perm], L2), "varlen pack order"
+
+
 ALL_CHECKS = [
     "check_decimal_bruteforce",
     "check_finite_differences",
@@ -406,4 +473,5 @@ ALL_CHECKS = [
     "check_row_variants",
     "check_golden",
     "check_decode",
+    "check_varlen",
 ]

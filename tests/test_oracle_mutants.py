@@ -17,6 +17,7 @@ from oracle import monoid
 
 SRC = (pathlib.Path(oracle.__file__).parent / "attention.py").read_text()
 DECODE_SRC = (pathlib.Path(oracle.__file__).parent / "decode.py").read_text()
+VARLEN_SRC = (pathlib.Path(oracle.__file__).parent / "varlen.py").read_text()
 
 MUTANTS = {
     "gqa_head_mapping_modulo": ("return h // (Hq // Hkv)", "return h % Hkv"),
@@ -42,12 +43,24 @@ DECODE_MUTANTS = {
 }
 
 
+VARLEN_MUTANTS = {
+    "varlen_keys_of_earlier_sequences": ("k[None, :, k0:k1], v[None, :, k0:k1]", "k[None, :, :k1], v[None, :, :k1]"),
+    "varlen_key_bounds_from_queries": ("q0, q1, k0, k1 = cq[i], cq[i + 1], ck[i], ck[i + 1]",
+                                       "q0, q1, k0, k1 = cq[i], cq[i + 1], cq[i], cq[i + 1]"),
+    "varlen_backward_always_causal": ("dO[None, :, s0:s1],\n                              causal=causal",
+                                      "dO[None, :, s0:s1],\n                              causal=True"),
+    "varlen_backward_drops_last_sequence": ("    for i in range(len(cu) - 1):", "    for i in range(len(cu) - 2):"),
+}
+
+
 def _mutant_module(name):
     old, new = MUTANTS[name]
     assert SRC.count(old) >= 1, f"mutation anchor for {name} not found in the oracle source"
     mod = types.ModuleType(f"oracle_mutant_{name}")
     exec(compile(SRC.replace(old, new, 1), f"<mutant {name}>", "exec"), mod.__dict__)
     mod.forward_cached = oracle.forward_cached
+    mod.forward_varlen = oracle.forward_varlen
+    mod.backward_varlen = oracle.backward_varlen
     return mod
 
 
@@ -62,6 +75,24 @@ def _decode_mutant_module(name):
     mod.__dict__.update({k: getattr(oracle, k) for k in ("forward", "backward", "forward_rows",
                                                           "backward_dq_rows", "backward_dkdv_rows")})
     mod.forward_cached = dmod.forward_cached
+    mod.forward_varlen = oracle.forward_varlen
+    mod.backward_varlen = oracle.backward_varlen
+    return mod
+
+
+def _varlen_mutant_module(name):
+    """The real oracle with a mutated copy of the packed variable-length oracle."""
+    old, new = VARLEN_MUTANTS[name]
+    assert VARLEN_SRC.count(old) == 1, f"mutation anchor for {name} not found"
+    src = (VARLEN_SRC.replace(old, new, 1).replace("from .attention import", "from oracle.attention import")
+           .replace("from .decode import", "from oracle.decode import"))
+    vmod = types.ModuleType(f"oracle_varlen_mutant_{name}")
+    exec(compile(src, f"<mutant {name}>", "exec"), vmod.__dict__)
+    mod = types.ModuleType(f"oracle_with_{name}")
+    mod.__dict__.update({k: getattr(oracle, k) for k in ("forward", "backward", "forward_rows", "forward_cached",
+                                                          "backward_dq_rows", "backward_dkdv_rows")})
+    mod.forward_varlen = vmod.forward_varlen
+    mod.backward_varlen = vmod.backward_varlen
     return mod
 
 
@@ -90,3 +121,10 @@ def test_planted_decode_mistake_is_caught(name):
     mod = _decode_mutant_module(name)
     with pytest.raises(AssertionError):
         oc.check_decode(mod)
+
+
+@pytest.mark.parametrize("name", sorted(VARLEN_MUTANTS))
+def test_planted_varlen_mistake_is_caught(name):
+    mod = _varlen_mutant_module(name)
+    with pytest.raises(AssertionError):
+        oc.check_varlen(mod)

@@ -44,6 +44,10 @@ def test_decode_cached_attention():
     oc.check_decode(oracle)
 
 
+def test_varlen_packed_batches():
+    oc.check_varlen(oracle)
+
+
 def test_golden_file():
     oc.check_golden(oracle)
 
