@@ -266,6 +266,52 @@ def prefill_measurement(g, torch, peaks, peak_src, steps=20, warmup=3):
                          "peak_source": f"{peak_src} bf16 dense, burst (kernel timed alone)"}}
 
 
+PACKED = dict(Hq=32, Hkv=8, D=128, n=16, lo=512, hi=3584, seed=8)
+
+
+def packed_measurement(g, torch, peaks, peak_src, steps=20, warmup=3):
+    """Forward of a packed batch of 16 causal sequences of mixed length (uniform on [512, 3584]
+    tokens, laid end to end): FLOPs are 4 D per visible pair of each sequence, against the
+    measured bf16 burst peak."""
+    from gqa_inputs import draw_lengths, make_packed_inputs
+    c = PACKED
+    lens = draw_lengths(c["n"], c["lo"], c["hi"], c["seed"])
+    q, k, v, _, cu, _ = make_packed_inputs(c["Hq"], c["Hkv"], lens, lens, c["D"], c["seed"], with_do=False)
+    q, k, v, cu = q.cuda(), k.cuda(), v.cuda(), cu.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], device="cuda", dtype=torch.float32)
+    flush = torch.empty(256 << 20, device="cuda", dtype=torch.uint8)
+    for _ in range(warmup):
+        g.gqa_attn_fwd_varlen(q, k, v, cu, cu, max(lens), o=o, lse=lse)
+    torch.cuda.synchronize()
+    total = 0.0
+    g.gqa_attn_trace_arm()
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.gqa_attn_fwd_varlen(q, k, v, cu, cu, max(lens), o=o, lse=lse)
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    tr = g.gqa_attn_trace_collect()
+    if g.gqa_attn_get_error() != 0:
+        raise RuntimeError("packed forward failed")
+    ms = total / steps
+    fl = 4.0 * c["D"] * c["Hq"] * sum(n * (n + 1) // 2 for n in lens)
+    n_, t_ = tr["fwd"]
+    kern_ms = t_ / max(n_, 1)
+    achieved = fl / (kern_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"workload": (f"packed: Hq=32 Hkv=8 D=128, {c['n']} causal sequences of {min(lens)}..{max(lens)} tokens "
+                         f"({sum(lens)} in all, lengths uniform on [{c['lo']}, {c['hi']}], seed {c['seed']})"),
+            "value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "us_per_call": ms * 1e3,
+            "l2": "256 MB buffer written between calls",
+            "roofline": {"kernel": "fwd", "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 dense, burst (kernel timed alone)"}}
+
+
 def config_of(w):
     return {"workload": f"{w.name}: causal GQA B={w.B} Hq={w.Hq} Hkv={w.Hkv} S={w.S} D={w.D}",
             "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": True, "scale": w.scale,
@@ -284,7 +330,7 @@ def main():
                     help="B,Hq,Hkv,S,D: override the workload's shape (same seed and value distributions); "
                          "for profiling smaller cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode and prefill-over-cache measurements")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode, prefill-over-cache and packed-batch measurements")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -438,6 +484,7 @@ def main():
     if world == 1 and not args.no_decode:
         line["decode"] = decode_measurement(g, torch, peaks, peak_src)
         line["prefill"] = prefill_measurement(g, torch, peaks, peak_src)
+        line["packed"] = packed_measurement(g, torch, peaks, peak_src)
     if world == 1 and not args.no_cpu_baseline:
         val, desc, cores = cpu_oracle_sample(w)
         line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}

@@ -37,6 +37,7 @@ __all__ = [
     "gqa_attn_bwd_noalloc",
     "gqa_attn_decode_fwd",
     "gqa_attn_fwd_cached",
+    "gqa_attn_fwd_varlen",
     "gqa_attn_decode_workspace_size",
     "NOALLOC_SCRATCH_BYTES",
     "KERNEL_NAMES",
@@ -243,4 +244,44 @@ def gqa_attn_fwd_cached(q, k_cache, v_cache, causal: bool = True, scale: float |
                                          lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), float(scale),
                                          _stream_handle(stream))
     _check(rc, "gqa_attn_fwd_cached")
+    return o, lse
+
+
+def _check_packed(name, t):
+    if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 3-D bfloat16 CUDA tensor ([H, T, D])")
+
+
+def _check_cu(name, cu, device):
+    if not cu.is_cuda or cu.dtype != torch.int32 or cu.dim() != 1 or not cu.is_contiguous() or cu.numel() < 2:
+        raise ValueError(f"{name} must be a contiguous 1-D int32 CUDA tensor of nseq + 1 bounds")
+    if cu.device != device:
+        raise ValueError(f"{name} is on {cu.device}, the tensors on {device}")
+
+
+def gqa_attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool = True,
+                        scale: float | None = None, o=None, lse=None, stream=None):
+    """Forward of a packed batch: q [Hq, Tq, D], k/v [Hkv, Tk, D], sequence i owning query rows
+    cu_seqlens_q[i]:cu_seqlens_q[i+1] and key rows cu_seqlens_k[i]:cu_seqlens_k[i+1] (int32 CUDA
+    tensors). Returns (o [Hq, Tq, D] bf16, lse [Hq, Tq] f32)."""
+    _check_packed("q", q)
+    _check_packed("k", k)
+    _check_packed("v", v)
+    Hq, Tq, D = q.shape
+    Hkv, Tk = k.shape[0], k.shape[1]
+    if k.shape != (Hkv, Tk, D) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    _check_cu("cu_seqlens_q", cu_seqlens_q, q.device)
+    _check_cu("cu_seqlens_k", cu_seqlens_k, q.device)
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel():
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must describe the same number of sequences")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((Hq, Tq), device=q.device, dtype=torch.float32) if lse is None else lse
+    rc = _lib.load().gqa_attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                         cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                                         cu_seqlens_q.numel() - 1, int(max_seqlen_q), Hq, Hkv, Tq, Tk, D,
+                                         int(bool(causal)), float(scale), _stream_handle(stream))
+    _check(rc, "gqa_attn_fwd_varlen")
     return o, lse

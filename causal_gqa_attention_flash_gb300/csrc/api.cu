@@ -160,6 +160,10 @@ int gqa_attn_fwd_cached(const void* q, const void* k, const void* v, void* o, fl
   a.map_v = &mv;
   a.map_o = &mo;
   a.lse = lse;
+  a.o = o;
+  a.cu_q = nullptr;
+  a.cu_k = nullptr;
+  a.max_seqlen_q = 0;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
@@ -176,6 +180,48 @@ int gqa_attn_fwd_cached(const void* q, const void* k, const void* v, void* o, fl
 int gqa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
                  int D, int causal, float scale, void* stream) {
   return gqa_attn_fwd_cached(q, k, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, stream);
+}
+
+int gqa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                        const int* cu_seqlens_k, int nseq, int max_seqlen_q, int Hq, int Hkv, int Tq, int Tk, int D,
+                        int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return GQA_ERR_INVALID_ARG;
+  if (nseq < 1 || Tq < 1 || Tk < 1 || max_seqlen_q < 1 || max_seqlen_q > Tq) return GQA_ERR_INVALID_ARG;
+  int rc = check_common(1, Hq, Hkv, Tq > Tk ? Tq : Tk, D, scale);
+  if (rc != GQA_OK) return rc;
+  if ((long long)nseq * Hq >= (1ll << 31)) return GQA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
+    return GQA_ERR_INVALID_ARG;
+  CUtensorMap mq, mk, mv, mo;
+  cudaError_t e;
+  if ((e = encode_bf16(&mq, q, D, Tq, Hq)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mk, k, D, Tk, Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mv, v, D, Tk, Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mo, o, D, Tq, Hq)) != cudaSuccess) return fail_cuda(e);
+  int* status = nullptr;
+  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  FwdArgs a;
+  a.map_q = &mq;
+  a.map_k = &mk;
+  a.map_v = &mv;
+  a.map_o = &mo;
+  a.lse = lse;
+  a.o = o;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.max_seqlen_q = max_seqlen_q;
+  a.B = nseq;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sq = Tq;
+  a.Sk = Tk;
+  a.D = D;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  a.status = status;
+  if ((e = launch_fwd(a, static_cast<cudaStream_t>(stream))) != cudaSuccess) return fail_cuda(e);
+  return GQA_OK;
 }
 
 size_t gqa_attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D) {
@@ -359,6 +405,7 @@ int gqa_attn_get_error(void* stream) {
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail_cuda(e);
   if (h & STATUS_TIMEOUT) return GQA_ERR_TIMEOUT;
   if (h & STATUS_MISALIGNED_SMEM) return GQA_ERR_INTERNAL;
+  if (h & STATUS_BAD_SEQLENS) return GQA_ERR_INVALID_ARG;
   return GQA_OK;
 }
 

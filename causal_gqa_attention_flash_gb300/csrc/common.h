@@ -26,7 +26,13 @@ struct FwdArgs {
   const CUtensorMap* map_v;
   const CUtensorMap* map_o;  // [B*Hq, Sq, D] bf16 (TMA store of O)
   float* lse;                // f32 [B, Hq, Sq]
-  int B, Hq, Hkv, Sq, Sk, D, causal;  // Sq <= Sk; query r at absolute position Sk - Sq + r
+  void* o;                   // O itself (packed batches store ragged tiles row by row)
+  const int* cu_q;           // packed batch: device int32 [B + 1] query bounds; nullptr = dense
+  const int* cu_k;           // packed batch: key bounds
+  int max_seqlen_q;          // packed batch: bound on every sequence's query count
+  // Dense: Sq <= Sk; query r at absolute position Sk - Sq + r. Packed: B sequences, Sq / Sk the
+  // total query / key rows, maps [Hq, Sq, D] and [Hkv, Sk, D].
+  int B, Hq, Hkv, Sq, Sk, D, causal;
   float scale_log2;          // scale * log2(e)
   int* status;               // device status word
 };

@@ -31,6 +31,10 @@
 // means the previous P V is done, so O can be rescaled right away.
 // Epilogue: O / l in bf16 is written into the tile's (no longer needed) Q
 // buffer in the TMA box layout and stored by TMA; rows past S are clipped.
+// Queries may be fewer than keys (Sq <= Sk, bottom-right causal alignment), and
+// a batch may be packed: sequences of different lengths laid end to end along
+// the row axis, each CTA reading its sequence's bounds, the last ragged query
+// tile of a sequence storing its rows one by one.
 #include "common.h"
 #include "ptx.cuh"
 
@@ -78,12 +82,59 @@ static_assert(FwdCfg<64>::kSmemBytes <= 232448 && FwdCfg<128>::kSmemBytes <= 232
 
 struct FwdKParams {
   float* lse;
-  // Sq query rows against Sk >= Sq keys; query row r sits at absolute position koff + r,
-  // koff = Sk - Sq (0 for self-attention), and (causal) sees keys j <= koff + r.
+  uint16_t* o;         // O itself: packed batches store a sequence's ragged last tile row by row
+  const int* cu_q;     // packed batches: sequence bounds [nseq + 1] (nullptr: dense batch)
+  const int* cu_k;
+  int Tq, Tk;          // packed batches: total query and key rows
+  int max_seqlen_q;    // packed batches: bound on any sequence's query rows
+  // Dense batch: Sq query rows against Sk >= Sq keys; query row r sits at absolute position
+  // koff + r, koff = Sk - Sq (0 for self-attention), and (causal) sees keys j <= koff + r.
   int Hq, Hkv, Sq, Sk, koff, causal, n_ktiles;
   float scale_log2;
   int* status;
 };
+
+// The rows one CTA works on: its sequence's query and key counts and where they start.
+struct FwdGeom {
+  int Sq, Sk, koff, n_ktiles;
+  int q_row0, k_row0;    // first query / key row of the sequence in its tensor map
+  int q_coord, kv_coord; // outermost tensor-map coordinate of the query head and of its KV head
+  size_t lse_base;       // LSE index of the sequence's first query row
+};
+
+// Dense batch: (b, h) = blockIdx.x. Packed batch: sequence blockIdx.x / Hq, head blockIdx.x % Hq,
+// bounds read from cu_q / cu_k and checked; returns false (status bit set) for bounds that are
+// not a valid packing, and the CTA does nothing.
+__device__ __forceinline__ bool fwd_geom(const FwdKParams& p, int bh, FwdGeom& g) {
+  const int b = bh / p.Hq;
+  const int h = bh - b * p.Hq;
+  const int G = p.Hq / p.Hkv;
+  if (p.cu_q == nullptr) {
+    g.Sq = p.Sq;
+    g.Sk = p.Sk;
+    g.q_row0 = 0;
+    g.k_row0 = 0;
+    g.q_coord = bh;
+    g.kv_coord = b * p.Hkv + h / G;
+    g.lse_base = (size_t)bh * p.Sq;
+  } else {
+    const int q0 = __ldg(p.cu_q + b), q1 = __ldg(p.cu_q + b + 1);
+    const int k0 = __ldg(p.cu_k + b), k1 = __ldg(p.cu_k + b + 1);
+    if (q0 < 0 || q1 < q0 || q1 > p.Tq || k0 < 0 || k1 < k0 || k1 > p.Tk || q1 - q0 > k1 - k0 ||
+        q1 - q0 > p.max_seqlen_q)
+      return false;
+    g.Sq = q1 - q0;
+    g.Sk = k1 - k0;
+    g.q_row0 = q0;
+    g.k_row0 = k0;
+    g.q_coord = h;
+    g.kv_coord = h / G;
+    g.lse_base = (size_t)h * p.Tq + q0;
+  }
+  g.koff = g.Sk - g.Sq;
+  g.n_ktiles = (g.Sk + kTile - 1) / kTile;
+  return true;
+}
 
 // Time-bounded wait that ignores the abort flag: used when tearing down after
 // an abort, to let copies and MMAs already in flight land before the CTA exits.
@@ -145,11 +196,11 @@ __device__ __forceinline__ float exp_pack_store(const uint32_t (&r)[128], int la
 }
 
 // Number of key tiles query tile qt visits; 0 if the tile lies past Sq.
-__device__ __forceinline__ int kv_tiles_of(int qt, const FwdKParams& p) {
-  if (qt * kTile >= p.Sq) return 0;
-  if (!p.causal) return p.n_ktiles;
-  const int last_row = min(p.Sq - 1, qt * kTile + kTile - 1);
-  return (p.koff + last_row) / kTile + 1;
+__device__ __forceinline__ int kv_tiles_of(int qt, const FwdGeom& g, int causal) {
+  if (qt * kTile >= g.Sq) return 0;
+  if (!causal) return g.n_ktiles;
+  const int last_row = min(g.Sq - 1, qt * kTile + kTile - 1);
+  return (g.koff + last_row) / kTile + 1;
 }
 
 template <int D>
@@ -168,13 +219,16 @@ __global__ void __launch_bounds__(384, 1)
   const int lane = tid & 31;
   const int bh = blockIdx.x;                                   // b * Hq + h
   const int pair = (int)gridDim.y - 1 - (int)blockIdx.y;       // longest pairs first
-  const int b = bh / p.Hq;
-  const int h = bh - b * p.Hq;
-  const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
+  FwdGeom g;
+  if (!fwd_geom(p, bh, g)) {
+    if (tid == 0) atomicOr(p.status, STATUS_BAD_SEQLENS);
+    return;
+  }
   const int qtA = 2 * pair, qtB = 2 * pair + 1;
-  const int nA = kv_tiles_of(qtA, p);
-  const int nB = kv_tiles_of(qtB, p);
+  const int nA = kv_tiles_of(qtA, g, p.causal);
+  const int nB = kv_tiles_of(qtB, g, p.causal);
   const int n_kv = nA > nB ? nA : nB;
+  if (nA == 0) return;  // a packed batch's short sequence: no query tile of this CTA exists
   const WaitGuard wg{&bars->abort_flag, p.status, kWaitLimitNs};
 
   if (tid == 0) {
@@ -214,7 +268,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int t = 0; t < 2; ++t)
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * kBoxBytes, &map_q, &bars->q_full, c * kChunk,
-                      (qtA + t) * kTile, bh);
+                      g.q_row0 + (qtA + t) * kTile, g.q_coord);
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % ST;
@@ -223,7 +277,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kKOff + st * C::kTileBytes + c * kBoxBytes, &map_k, &bars->k_full[st], c * kChunk,
-                      j * kTile, kvh);
+                      g.k_row0 + j * kTile, g.kv_coord);
         issued = j + 1;
       }
       if (bars->abort_flag) {
@@ -245,7 +299,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kVOff + st * C::kTileBytes + c * kBoxBytes, &map_v, &bars->v_full[st], c * kChunk,
-                      j * kTile, kvh);
+                      g.k_row0 + j * kTile, g.kv_coord);
         issued = j + 1;
       }
       if (bars->abort_flag) {
@@ -358,12 +412,12 @@ __global__ void __launch_bounds__(384, 1)
       const int kv0 = j * kTile;
       // last visible local key of this row in key tile j: the causal bound koff + q - kv0 and the
       // end of the keys; tiles where some row sees fewer than 128 keys take the masked path.
-      const int qpos = p.koff + qt * kTile;  // absolute position of the tile's first row
+      const int qpos = g.koff + qt * kTile;  // absolute position of the tile's first row
       const bool diag = p.causal && (qpos < kv0 + kTile - 1);
-      const bool tail = kv0 + kTile > p.Sk;
+      const bool tail = kv0 + kTile > g.Sk;
       int last = kTile - 1;
       if (diag) last = min(last, qpos + row - kv0);
-      if (tail) last = min(last, p.Sk - kv0 - 1);
+      if (tail) last = min(last, g.Sk - kv0 - 1);
       const bool masked = diag || tail;
       const float mx = masked ? row_max<true>(r, last) : row_max<false>(r, last);
       const float m_tile = mx * c;
@@ -405,7 +459,12 @@ __global__ void __launch_bounds__(384, 1)
     if (ok && n_x > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l;
+      const int qrow = qt * kTile + row;
+      // A packed batch's last, ragged query tile must not write the rows past its sequence (they
+      // belong to the next one): it stores its rows one by one. Every other tile goes through TMA.
+      const bool rowwise = p.cu_q != nullptr && (qt + 1) * kTile > g.Sq;
       uint8_t* stage = smem + C::kQOff + x * C::kTileBytes;  // Q_X is no longer read by any MMA
+      uint16_t* orow = p.o + ((size_t)g.q_coord * p.Tq + g.q_row0 + qrow) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -419,21 +478,26 @@ __global__ void __launch_bounds__(384, 1)
           w.z = pack_bf16(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
           w.w = pack_bf16(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
           const int col = cc * 32 + u * 8;      // first column of the unit
-          const int unit = (col & 63) >> 3;     // unit within the 128-byte row of its box
-          *reinterpret_cast<uint4*>(stage + (col >> 6) * kBoxBytes + row * 128 + ((unit ^ (row & 7)) << 4)) = w;
+          if (rowwise) {
+            if (qrow < g.Sq) *reinterpret_cast<uint4*>(orow + col) = w;
+          } else {
+            const int unit = (col & 63) >> 3;     // unit within the 128-byte row of its box
+            *reinterpret_cast<uint4*>(stage + (col >> 6) * kBoxBytes + row * 128 + ((unit ^ (row & 7)) << 4)) = w;
+          }
         }
       }
-      fence_proxy_async_smem();
-      uint32_t wg_phase = 0;
-      ok = wg_barrier(&bars->wg_bar[x], wg_phase, wg);
-      if (ok && row == 0) {
-        for (int cb = 0; cb < C::kChunks; ++cb)
-          tma_store_3d(&map_o, stage + cb * kBoxBytes, cb * kChunk, qt * kTile, bh);
-        bulk_commit_group();
+      if (!rowwise) {
+        fence_proxy_async_smem();
+        uint32_t wg_phase = 0;
+        ok = wg_barrier(&bars->wg_bar[x], wg_phase, wg);
+        if (ok && row == 0) {
+          for (int cb = 0; cb < C::kChunks; ++cb)
+            tma_store_3d(&map_o, stage + cb * kBoxBytes, cb * kChunk, g.q_row0 + qt * kTile, g.q_coord);
+          bulk_commit_group();
+        }
       }
-      const int qrow = qt * kTile + row;
-      if (qrow < p.Sq) p.lse[(size_t)bh * p.Sq + qrow] = (m_ref + __log2f(l)) * 0.69314718055994530942f;
-      if (row == 0) bulk_wait_group_read<0>();
+      if (qrow < g.Sq) p.lse[g.lse_base + qrow] = (m_ref + __log2f(l)) * 0.69314718055994530942f;
+      if (!rowwise && row == 0) bulk_wait_group_read<0>();
     }
     tc_fence_before();
   }
@@ -450,6 +514,12 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
   FwdKParams p;
   p.lse = a.lse;
+  p.o = static_cast<uint16_t*>(a.o);
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.Tq = a.Sq;
+  p.Tk = a.Sk;
+  p.max_seqlen_q = a.max_seqlen_q;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.Sq = a.Sq;
@@ -466,7 +536,9 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   cudaFuncAttributes fa;
   if ((e = cudaFuncGetAttributes(&fa, fwd_kernel<D>)) != cudaSuccess) return e;
   if (fa.numRegs * C::kThreads < 2 * 128 * C::kHighRegs + 128 * C::kLowRegs) return cudaErrorInvalidConfiguration;
-  dim3 grid((unsigned)(a.B * a.Hq), (unsigned)ceil_div(a.Sq, 2 * kTile));
+  // Packed batch: one row of CTAs per (sequence, head), enough pairs for the longest sequence.
+  const int rows = a.cu_q ? a.max_seqlen_q : a.Sq;
+  dim3 grid((unsigned)(a.B * a.Hq), (unsigned)ceil_div(rows, 2 * kTile));
   trace_begin(kKernelFwd, stream);
   fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_o, p);
   e = cudaGetLastError();

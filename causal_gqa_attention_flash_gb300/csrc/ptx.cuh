@@ -14,6 +14,7 @@ namespace gqa {
 // Device status bits (OR-ed into the library's status word).
 constexpr int STATUS_TIMEOUT = 1;
 constexpr int STATUS_MISALIGNED_SMEM = 2;
+constexpr int STATUS_BAD_SEQLENS = 4;  // a packed batch's sequence bounds are not a valid packing
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -23,6 +23,11 @@ draw Q, K, V, dO in that order as float32 ``randn`` of their full shapes;
 multiply dO by ``do_std`` (0.1, i.e. N(0, 1e-2) read as a variance; 1.0 for
 the tiny case); round each to bfloat16 (round-to-nearest-even). The same
 bfloat16 bits feed the GPU path and the oracle.
+
+Packed batches of variable-length sequences (``make_packed_inputs``) lay the
+sequences end to end along the token axis, one [H, T, D] tensor per operand;
+the lengths are given, or drawn by ``draw_lengths`` (uniform on [lo, hi] with
+its own generator), and the bounds are their running sums starting at 0.
 """
 
 from __future__ import annotations
@@ -80,6 +85,37 @@ def make_inputs(B: int, Hq: int, Hkv: int, S: int, D: int, seed: int,
     if with_do:
         dO = (torch.randn(B, Hq, S, D, generator=g, dtype=torch.float32) * do_std).to(torch.bfloat16)
     return q, k, v, dO
+
+
+def seq_bounds(lengths):
+    """Bounds [0, l0, l0+l1, ...] of sequences laid end to end (int32 CPU tensor)."""
+    out = [0]
+    for n in lengths:
+        out.append(out[-1] + int(n))
+    return torch.tensor(out, dtype=torch.int32)
+
+
+def draw_lengths(n: int, lo: int, hi: int, seed: int):
+    """n sequence lengths, uniform on [lo, hi], from their own seeded generator."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
+
+
+def make_packed_inputs(Hq: int, Hkv: int, lens_q, lens_k, D: int, seed: int,
+                       do_std: float = 0.1, with_do: bool = True):
+    """Packed batch: bf16 CPU tensors q [Hq, Tq, D], k, v [Hkv, Tk, D], dO [Hq, Tq, D] (or None)
+    drawn in that order as the recipe says, plus the int32 bounds cu_q, cu_k."""
+    cu_q = seq_bounds(lens_q)
+    cu_k = seq_bounds(lens_k)
+    Tq, Tk = int(cu_q[-1]), int(cu_k[-1])
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = torch.randn(Hq, Tq, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn(Hkv, Tk, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn(Hkv, Tk, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    dO = None
+    if with_do:
+        dO = (torch.randn(Hq, Tq, D, generator=g, dtype=torch.float32) * do_std).to(torch.bfloat16)
+    return q, k, v, dO, cu_q, cu_k
 
 
 def workload_inputs(name: str, with_do: bool = True):

@@ -89,6 +89,32 @@ int gqa_attn_fwd_cached(const void* q, const void* k, const void* v, void* o, fl
                         int Sq, int Sk, int D, int causal, float scale, void* stream);
 
 /*
+ * Forward over a packed batch of variable-length sequences: the nseq sequences
+ * lie end to end along the row axis, sequence i owning query rows
+ * cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1 and key/value rows cu_seqlens_k[i] ..
+ * cu_seqlens_k[i+1]-1. A query attends only to keys of its own sequence; with
+ * Sq_i queries and Sk_i >= Sq_i keys, query r of the sequence sits at position
+ * Sk_i - Sq_i + r and (causal) sees its keys j <= Sk_i - Sq_i + r (packed
+ * self-attention: cu_seqlens_q = cu_seqlens_k).
+ *   q, o [Hq,Tq,D], k, v [Hkv,Tk,D] (bf16, device), lse [Hq,Tq] (f32);
+ *   cu_seqlens_q, cu_seqlens_k: DEVICE int32 [nseq + 1], nondecreasing, first 0,
+ *   last Tq (resp. Tk); max_seqlen_q >= every Sq_i (sizes the grid).
+ * K/V rows of other sequences never enter a result, but must be finite
+ * (they meet a zero weight in the P V product).
+ * Errors: GQA_ERR_INVALID_ARG on the host for null or misaligned pointers,
+ * nseq, Tq, Tk < 1 or max_seqlen_q outside [1, Tq]; sizes as gqa_attn_fwd.
+ * The bounds themselves live on the device and are checked there: a sequence
+ * whose bounds are out of range, decreasing, have more queries than keys or
+ * more than max_seqlen_q queries is skipped and gqa_attn_get_error() reports
+ * GQA_ERR_INVALID_ARG.
+ * Passage: RustingBrain docs, "Training infrastructure" (batches of token
+ * windows); tang page, "An LLM" (prefill 512).
+ */
+int gqa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                        const int* cu_seqlens_k, int nseq, int max_seqlen_q, int Hq, int Hkv, int Tq, int Tk, int D,
+                        int causal, float scale, void* stream);
+
+/*
  * Size in bytes of the device workspace gqa_attn_bwd needs (256-byte aligned
  * sections: the per-row D = rowsum(dO * O) and the scaled LSE, f32
  * [B,Hq,ceil(S/128)*128] each, and the f32 dQ accumulator [B,Hq,S,D]).
@@ -144,8 +170,9 @@ int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device. Returns GQA_OK, GQA_ERR_TIMEOUT if a kernel gave up on a
  * wait since the last call, GQA_ERR_INTERNAL if a kernel's own shared-memory
- * alignment check failed (it then returned without work), or GQA_ERR_CUDA if
- * the stream reports an error.
+ * alignment check failed (it then returned without work), GQA_ERR_INVALID_ARG
+ * if a packed batch's device-side sequence bounds were invalid (those
+ * sequences were skipped), or GQA_ERR_CUDA if the stream reports an error.
  */
 int gqa_attn_get_error(void* stream);
 

@@ -42,6 +42,24 @@ def test_binding_declares_every_symbol():
     assert sorted(_lib.SIGNATURES) == _declared_functions()
 
 
+def _declared_arities():
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(gqa_attn_[a-z_]+)\s*\(([^)]*)\)\s*;", src):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_arities_match_the_header():
+    """Each ctypes prototype has as many parameters as the C declaration."""
+    from causal_gqa_attention_flash_gb300 import _lib
+    arities = _declared_arities()
+    assert sorted(arities) == _declared_functions()
+    for name, (_, argtypes) in _lib.SIGNATURES.items():
+        assert len(argtypes) == arities[name], f"{name}: binding {len(argtypes)} vs header {arities[name]}"
+
+
 def test_strerror_and_workspace_size(lib):
     for code in (0, -1, -2, -3, -4, -5, -99):
         assert isinstance(lib.gqa_attn_strerror(code), bytes)
