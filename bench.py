@@ -270,19 +270,28 @@ PACKED = dict(Hq=32, Hkv=8, D=128, n=16, lo=512, hi=3584, seed=8)
 
 
 def packed_measurement(g, torch, peaks, peak_src, steps=20, warmup=3):
-    """Forward of a packed batch of 16 causal sequences of mixed length (uniform on [512, 3584]
-    tokens, laid end to end): FLOPs are 4 D per visible pair of each sequence, against the
-    measured bf16 burst peak."""
+    """Forward + backward of a packed batch of 16 causal sequences of mixed length (uniform on
+    [512, 3584] tokens, laid end to end): FLOPs are 4 D (forward) + 10 D (backward) per visible
+    pair of each sequence, against the measured bf16 burst peak (each step timed alone)."""
     from gqa_inputs import draw_lengths, make_packed_inputs
     c = PACKED
     lens = draw_lengths(c["n"], c["lo"], c["hi"], c["seed"])
-    q, k, v, _, cu, _ = make_packed_inputs(c["Hq"], c["Hkv"], lens, lens, c["D"], c["seed"], with_do=False)
-    q, k, v, cu = q.cuda(), k.cuda(), v.cuda(), cu.cuda()
+    q, k, v, dO, cu, _ = make_packed_inputs(c["Hq"], c["Hkv"], lens, lens, c["D"], c["seed"])
+    q, k, v, dO, cu = q.cuda(), k.cuda(), v.cuda(), dO.cuda(), cu.cuda()
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:2], device="cuda", dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(g.gqa_attn_bwd_varlen_workspace_size(c["Hq"], c["Hkv"], q.shape[1], c["D"]),
+                     device="cuda", dtype=torch.uint8)
     flush = torch.empty(256 << 20, device="cuda", dtype=torch.uint8)
+    m = max(lens)
+
+    def step():
+        g.gqa_attn_fwd_varlen(q, k, v, cu, cu, m, o=o, lse=lse)
+        g.gqa_attn_bwd_varlen(q, k, v, o, dO, lse, cu, m, dq=dq, dk=dk, dv=dv, workspace=ws)
+
     for _ in range(warmup):
-        g.gqa_attn_fwd_varlen(q, k, v, cu, cu, max(lens), o=o, lse=lse)
+        step()
     torch.cuda.synchronize()
     total = 0.0
     g.gqa_attn_trace_arm()
@@ -290,26 +299,30 @@ def packed_measurement(g, torch, peaks, peak_src, steps=20, warmup=3):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        g.gqa_attn_fwd_varlen(q, k, v, cu, cu, max(lens), o=o, lse=lse)
+        step()
         e1.record()
         torch.cuda.synchronize()
         total += e0.elapsed_time(e1)
     tr = g.gqa_attn_trace_collect()
     if g.gqa_attn_get_error() != 0:
-        raise RuntimeError("packed forward failed")
+        raise RuntimeError("packed forward/backward failed")
     ms = total / steps
-    fl = 4.0 * c["D"] * c["Hq"] * sum(n * (n + 1) // 2 for n in lens)
-    n_, t_ = tr["fwd"]
-    kern_ms = t_ / max(n_, 1)
-    achieved = fl / (kern_ms * 1e-3) / 1e12
+    pairs = c["Hq"] * sum(n * (n + 1) // 2 for n in lens)
+    fwd_fl, bwd_fl = 4.0 * c["D"] * pairs, 10.0 * c["D"] * pairs
+    avg = {name: (t_ / n_ if n_ else None) for name, (n_, t_) in tr.items()}
+    fwd_tf = fwd_fl / (avg["fwd"] * 1e-3) / 1e12
+    bwd_tf = bwd_fl / (avg["bwd_main"] * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     return {"workload": (f"packed: Hq=32 Hkv=8 D=128, {c['n']} causal sequences of {min(lens)}..{max(lens)} tokens "
-                         f"({sum(lens)} in all, lengths uniform on [{c['lo']}, {c['hi']}], seed {c['seed']})"),
-            "value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "us_per_call": ms * 1e3,
-            "l2": "256 MB buffer written between calls",
-            "roofline": {"kernel": "fwd", "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None,
-                         "peak_source": f"{peak_src} bf16 dense, burst (kernel timed alone)"}}
+                         f"({sum(lens)} in all, lengths uniform on [{c['lo']}, {c['hi']}], seed {c['seed']}), "
+                         "forward + backward"),
+            "value": (fwd_fl + bwd_fl) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "l2": "256 MB buffer written between steps",
+            "kernels": {k_: {"launches": n_, "avg_ms": avg[k_]} for k_, (n_, _) in tr.items() if n_},
+            "roofline": {"kernel": "bwd_main", "bound": "tensor", "achieved": bwd_tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": bwd_tf / peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 dense, burst (each step timed alone)",
+                         "fwd_kernel": {"achieved": fwd_tf, "frac": fwd_tf / peak}}}
 
 
 def config_of(w):

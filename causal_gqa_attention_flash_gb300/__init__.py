@@ -38,6 +38,8 @@ __all__ = [
     "gqa_attn_decode_fwd",
     "gqa_attn_fwd_cached",
     "gqa_attn_fwd_varlen",
+    "gqa_attn_bwd_varlen",
+    "gqa_attn_bwd_varlen_workspace_size",
     "gqa_attn_decode_workspace_size",
     "NOALLOC_SCRATCH_BYTES",
     "KERNEL_NAMES",
@@ -285,3 +287,40 @@ def gqa_attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, 
                                          int(bool(causal)), float(scale), _stream_handle(stream))
     _check(rc, "gqa_attn_fwd_varlen")
     return o, lse
+
+
+def gqa_attn_bwd_varlen_workspace_size(Hq: int, Hkv: int, T: int, D: int) -> int:
+    """Bytes of device workspace gqa_attn_bwd_varlen needs (0 for unsupported sizes)."""
+    return int(_lib.load().gqa_attn_bwd_varlen_workspace_size(Hq, Hkv, T, D))
+
+
+def gqa_attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, max_seqlen: int, causal: bool = True,
+                        scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of packed self-attention (q, o, dO [Hq, T, D], k, v [Hkv, T, D], lse [Hq, T], int32
+    CUDA bounds cu_seqlens): returns (dq, dk, dv), bf16, shaped like q, k, v."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO)):
+        _check_packed(name, t)
+    Hq, T, D = q.shape
+    Hkv = k.shape[0]
+    if k.shape != (Hkv, T, D) or v.shape != k.shape or o.shape != q.shape or dO.shape != q.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}, "
+                         f"o {tuple(o.shape)}, dO {tuple(dO.shape)}")
+    if lse.shape != (Hq, T) or lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [Hq, T]")
+    _check_cu("cu_seqlens", cu_seqlens, q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = gqa_attn_bwd_varlen_workspace_size(Hq, Hkv, T, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = _lib.load().gqa_attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
+                                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                         cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, int(max_seqlen),
+                                         workspace.data_ptr(), nbytes, Hq, Hkv, T, D, int(bool(causal)),
+                                         float(scale), _stream_handle(stream))
+    _check(rc, "gqa_attn_bwd_varlen")
+    return dq, dk, dv

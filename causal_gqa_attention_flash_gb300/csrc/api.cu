@@ -267,10 +267,76 @@ int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   a.dvec = reinterpret_cast<float*>(wsb + ws.dvec_off);
   a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
   a.dq_acc = reinterpret_cast<float*>(wsb + ws.dqacc_off);
+  a.cu = nullptr;
+  a.max_seqlen = 0;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.S = S;
+  a.D = D;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  a.status = status;
+  if ((e = launch_bwd(a, static_cast<cudaStream_t>(stream))) != cudaSuccess) return fail_cuda(e);
+  return GQA_OK;
+}
+
+size_t gqa_attn_bwd_varlen_workspace_size(int Hq, int Hkv, int T, int D) {
+  if (check_common(1, Hq, Hkv, T, D, 1.0f) != GQA_OK) return 0;
+  if ((long long)Hq * T + kRowPad >= (1ll << 31)) return 0;
+  return bwd_workspace_layout_packed(Hq, T, D).total;
+}
+
+int gqa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                        void* dq, void* dk, void* dv, const int* cu_seqlens, int nseq, int max_seqlen, void* workspace,
+                        size_t workspace_bytes, int Hq, int Hkv, int T, int D, int causal, float scale,
+                        void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !cu_seqlens || !workspace)
+    return GQA_ERR_INVALID_ARG;
+  if (nseq < 1 || T < 1 || max_seqlen < 1 || max_seqlen > T) return GQA_ERR_INVALID_ARG;
+  int rc = check_common(1, Hq, Hkv, T, D, scale);
+  if (rc != GQA_OK) return rc;
+  if ((long long)Hq * T + kRowPad >= (1ll << 31) || (long long)nseq * Hkv >= (1ll << 31)) return GQA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(cu_seqlens, 4) ||
+      !aligned(workspace, 256))
+    return GQA_ERR_INVALID_ARG;
+  const BwdWorkspace ws = bwd_workspace_layout_packed(Hq, T, D);
+  if (workspace_bytes < ws.total) return GQA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  CUtensorMap mq, mk, mv, mdo, macc;
+  cudaError_t e;
+  if ((e = encode_bf16(&mq, q, D, T, Hq)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mk, k, D, T, Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mv, v, D, T, Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mdo, dO, D, T, Hq)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_3d(&macc, wsb + ws.dqacc_off, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, T, Hq, 32,
+                     CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return fail_cuda(e);
+  int* status = nullptr;
+  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  BwdArgs a;
+  a.map_q = &mq;
+  a.map_k = &mk;
+  a.map_v = &mv;
+  a.map_do = &mdo;
+  a.map_dqacc = &macc;
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dvec = reinterpret_cast<float*>(wsb + ws.dvec_off);
+  a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
+  a.dq_acc = reinterpret_cast<float*>(wsb + ws.dqacc_off);
+  a.cu = cu_seqlens;
+  a.max_seqlen = max_seqlen;
+  a.B = nseq;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.S = T;
   a.D = D;
   a.causal = causal ? 1 : 0;
   a.scale = scale;

@@ -41,13 +41,14 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 
 // ------------------------------------------------------------------ prep
 
-// One group of D/8 threads per row: each thread reads 8 bf16 of dO and of O.
+// One group of D/8 threads per row: each thread reads 8 bf16 of dO and of O. Rows of the padded
+// arrays past rows_valid, or with s >= S, are padding (D = 0, LSE2 = +inf).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dO,
                                                        const float* __restrict__ lse, float* __restrict__ dvec,
                                                        float* __restrict__ lse2, float* __restrict__ dq_acc,
-                                                       int rows_total, int S, int S_pad, float log2e,
-                                                       long long acc_vec4) {
+                                                       int rows_total, int rows_valid, int S, int S_pad,
+                                                       float log2e, long long acc_vec4) {
   constexpr int TPR = D / 8;            // threads per row
   constexpr int RPW = 32 / TPR;          // rows per warp and iteration
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
@@ -61,8 +62,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
     const int bh = r / S_pad;
     const int s = r - bh * S_pad;
     const bool live = r < rows_total;
+    const bool real = r < rows_valid && s < S;  // a row of O / dO (not padding)
     float acc = 0.f;
-    if (live && s < S) {
+    if (live && real) {
       const size_t base = ((size_t)bh * S + s) * D + sub * 8;
       const uint4 a = *reinterpret_cast<const uint4*>(o + base);
       const uint4 b = *reinterpret_cast<const uint4*>(dO + base);
@@ -78,7 +80,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
     if (live && sub == 0) {
       dvec[r] = acc;
-      lse2[r] = (s < S) ? lse[(size_t)bh * S + s] * log2e : INFINITY;
+      lse2[r] = real ? lse[(size_t)bh * S + s] * log2e : INFINITY;
     }
   }
   float4* acc4 = reinterpret_cast<float4*>(dq_acc);
@@ -115,8 +117,9 @@ struct BwdCfg {
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;
   static constexpr int kDSOff = kDOOff + kStages * kTileBytes;         // dS bf16 [128 kv][128 q], MN-major
   static constexpr int kDSBytes = kTile * kTile * 2;
-  static constexpr int kRowOff = kDSOff + kDSBytes;                    // per stage: lse2[128], dvec[128]
-  static constexpr int kBarOff = kRowOff + kStages * 2 * kTile * 4;
+  static constexpr int kRowOff = kDSOff + kDSBytes;                    // per stage: lse2, dvec rows
+  static constexpr int kRowFl = 136;                                   // floats per row buffer (>= 4 + 128)
+  static constexpr int kBarOff = kRowOff + kStages * 2 * kRowFl * 4;
   static constexpr int kSmemBytes = kBarOff + 256;                     // the base is checked to be 1024-aligned
   static constexpr int kThreads = 352;
   static constexpr int kRounds = D / 64;                               // 32-column dQ slices per warpgroup
@@ -143,7 +146,10 @@ struct BwdKParams {
   const float* dvec;
   uint16_t* dk;
   uint16_t* dv;
-  int Hq, Hkv, S, S_pad, causal, n_tiles;
+  const int* cu;  // packed batch: sequence bounds (nullptr: dense batch)
+  // Dense: S rows per (b, head), D / LSE2 rows padded to S_pad per head. Packed: S = total rows
+  // T, row stride of D / LSE2 = T (S_pad = T), sequences of at most max_seqlen rows.
+  int Hq, Hkv, S, S_pad, causal, max_seqlen;
   float scale, scale_log2;
   int* status;
 };
@@ -182,15 +188,38 @@ __global__ void __launch_bounds__(352, 1)
     if (tid == 0) atomicOr(p.status, STATUS_MISALIGNED_SMEM);
     return;
   }
-  const int kvh = blockIdx.x;  // b * Hkv + hkv
   const int jt = blockIdx.y;   // key tile; tile 0 sees the most query tiles when causal
   const int G = p.Hq / p.Hkv;
-  const int b = kvh / p.Hkv;
-  const int hkv = kvh - b * p.Hkv;
-  const int bhq0 = b * p.Hq + hkv * G;  // first query head of the group
+  const int b = (int)blockIdx.x / p.Hkv;  // batch entry (dense) or sequence (packed)
+  const int hkv = (int)blockIdx.x - b * p.Hkv;
+  // L rows in this CTA's sequence, starting at row0 of the tensor maps; the KV head's map
+  // coordinate, the first query head's, and the row stride of the D / LSE2 arrays.
+  int L, row0, kv_coord, bhq0;
+  if (p.cu == nullptr) {
+    L = p.S;
+    row0 = 0;
+    kv_coord = (int)blockIdx.x;
+    bhq0 = b * p.Hq + hkv * G;
+  } else {
+    const int s0 = __ldg(p.cu + b), s1 = __ldg(p.cu + b + 1);
+    if (s0 < 0 || s1 < s0 || s1 > p.S || s1 - s0 > p.max_seqlen) {
+      if (tid == 0) atomicOr(p.status, STATUS_BAD_SEQLENS);
+      return;
+    }
+    L = s1 - s0;
+    row0 = s0;
+    kv_coord = hkv;
+    bhq0 = hkv * G;
+  }
+  if (jt * kTile >= L) return;  // a packed batch's short sequence: this key tile does not exist
+  const int n_tiles = (L + kTile - 1) / kTile;
   const int i_start = p.causal ? jt : 0;
-  const int n_i = p.n_tiles - i_start;
+  const int n_i = n_tiles - i_start;
   const int n_steps = G * n_i;
+  // D / LSE2 rows of query tile i of query head bhq0 + hl: copied from the 16-byte aligned row
+  // below (the copy is 4 rows wider when a packed sequence starts off a multiple of 4 rows).
+  const int n_rowfl = p.cu ? kTile + 4 : kTile;
+  auto rows_at = [&](int hl, int i) { return (size_t)(bhq0 + hl) * p.S_pad + (size_t)row0 + (size_t)i * kTile; };
   const WaitGuard wg{&bars->abort_flag, p.status, kWaitLimitNs};
 
   if (tid == 0) {
@@ -228,8 +257,8 @@ __global__ void __launch_bounds__(352, 1)
       tma_prefetch_desc(&map_do);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(smem + C::kKOff + c * kBoxBytes, &map_k, &bars->kv_full, c * kChunk, jt * kTile, kvh);
-        tma_load_3d(smem + C::kVOff + c * kBoxBytes, &map_v, &bars->kv_full, c * kChunk, jt * kTile, kvh);
+        tma_load_3d(smem + C::kKOff + c * kBoxBytes, &map_k, &bars->kv_full, c * kChunk, row0 + jt * kTile, kv_coord);
+        tma_load_3d(smem + C::kVOff + c * kBoxBytes, &map_v, &bars->kv_full, c * kChunk, row0 + jt * kTile, kv_coord);
       }
       int issued = 0;
       for (int t = 0; t < n_steps; ++t) {
@@ -240,16 +269,17 @@ __global__ void __launch_bounds__(352, 1)
         const int i = i_start + (t - hl * n_i);
         const int bhq = bhq0 + hl;
         uint64_t* bar = &bars->qdo_full[st];
-        mbar_arrive_expect_tx(bar, 2 * C::kTileBytes + 2 * kTile * 4);
+        mbar_arrive_expect_tx(bar, 2 * C::kTileBytes + 2 * n_rowfl * 4);
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(smem + C::kQOff + st * C::kTileBytes + c * kBoxBytes, &map_q, bar, c * kChunk, i * kTile, bhq);
-          tma_load_3d(smem + C::kDOOff + st * C::kTileBytes + c * kBoxBytes, &map_do, bar, c * kChunk, i * kTile,
-                      bhq);
+          tma_load_3d(smem + C::kQOff + st * C::kTileBytes + c * kBoxBytes, &map_q, bar, c * kChunk,
+                      row0 + i * kTile, bhq);
+          tma_load_3d(smem + C::kDOOff + st * C::kTileBytes + c * kBoxBytes, &map_do, bar, c * kChunk,
+                      row0 + i * kTile, bhq);
         }
-        float* srow = reinterpret_cast<float*>(smem + C::kRowOff) + st * 2 * kTile;
-        const size_t roff = (size_t)bhq * p.S_pad + (size_t)i * kTile;
-        bulk_load(srow, p.lse2 + roff, kTile * 4, bar);
-        bulk_load(srow + kTile, p.dvec + roff, kTile * 4, bar);
+        float* srow = reinterpret_cast<float*>(smem + C::kRowOff) + st * 2 * C::kRowFl;
+        const size_t roff = rows_at(hl, i) & ~size_t(3);
+        bulk_load(srow, p.lse2 + roff, n_rowfl * 4, bar);
+        bulk_load(srow + C::kRowFl, p.dvec + roff, n_rowfl * 4, bar);
         issued = t + 1;
       }
       if (bars->abort_flag) {
@@ -345,7 +375,7 @@ __global__ void __launch_bounds__(352, 1)
         for (int s2 = 0; s2 < D / 32; ++s2) {
           const uint8_t* stage = s2 < C::kChunks ? smem + C::kQOff + st * C::kTileBytes + s2 * kBoxBytes
                                                  : smem + C::kDOOff + st * C::kTileBytes + (s2 - C::kChunks) * kBoxBytes;
-          tma_reduce_add_3d(&map_acc, stage, s2 * 32, i * kTile, bhq);
+          tma_reduce_add_3d(&map_acc, stage, s2 * 32, row0 + i * kTile, bhq);
         }
         bulk_commit_group();
         bulk_wait_group_read<0>();
@@ -363,16 +393,19 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t dp_tmem = tbase + lane_off + C::kDPCol;
     const float c = p.scale_log2;
     const int kv_row = jt * kTile + row;
-    const bool kv_valid = kv_row < p.S;
+    const bool kv_valid = kv_row < L;
     uint8_t* sds_half = smem + C::kDSOff + hf * kBoxBytes;  // dS columns [64hf, 64hf+64)
     bool ok = true;
     for (int t = 0; t < n_steps; ++t) {
       const int st = t % ST;
-      const int i = i_start + (t % n_i);
-      const float* slse = reinterpret_cast<const float*>(smem + C::kRowOff) + st * 2 * kTile + hf * 64;
-      const float* sdv = slse + kTile;
+      const int hl = t / n_i;
+      const int i = i_start + (t - hl * n_i);
+      const int roff = (int)(rows_at(hl, i) & 3);  // the rows' offset within their widened copy
+      const float* slse = reinterpret_cast<const float*>(smem + C::kRowOff) + st * 2 * C::kRowFl + roff + hf * 64;
+      const float* sdv = slse + C::kRowFl;
       // visible iff key (jt*128 + row) <= query (i*128 + col): on the diagonal tile, col >= row
       const int first_visible = (p.causal && i == jt) ? row : 0;
+      const int q_limit = L - i * kTile;  // query columns at or past it lie beyond the sequence
 
       // ---- P^T = exp2(S^T c - LSE2) for the 64 query columns of this half
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, t & 1, wg));
@@ -386,15 +419,17 @@ __global__ void __launch_bounds__(352, 1)
         tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
         tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         uint32_t pk[32];
-        const bool masked = first_visible > hf * 64 || !kv_valid;  // causal diagonal or keys past S
+        // causal diagonal, keys past the sequence, or queries past it
+        const bool masked = first_visible > hf * 64 || !kv_valid || q_limit < hf * 64 + 64;
         if (masked) {
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
             const int c0 = 2 * x;
+            const int col = hf * 64 + c0;
             const float e0 = ex2_approx(fmaf(__uint_as_float(r[c0]), c, -slse[c0]));
             const float e1 = ex2_approx(fmaf(__uint_as_float(r[c0 + 1]), c, -slse[c0 + 1]));
-            P[c0] = (kv_valid && hf * 64 + c0 >= first_visible) ? e0 : 0.f;
-            P[c0 + 1] = (kv_valid && hf * 64 + c0 + 1 >= first_visible) ? e1 : 0.f;
+            P[c0] = (kv_valid && col >= first_visible && col < q_limit) ? e0 : 0.f;
+            P[c0 + 1] = (kv_valid && col + 1 >= first_visible && col + 1 < q_limit) ? e1 : 0.f;
             pk[x] = pack_bf16(P[c0], P[c0 + 1]);
           }
         } else {
@@ -476,7 +511,7 @@ __global__ void __launch_bounds__(352, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->dkv_done, 0, wg));
     if (ok) {
       tc_fence_after();
-      const size_t orow = ((size_t)kvh * p.S + kv_row) * D;
+      const size_t orow = ((size_t)kv_coord * p.S + row0 + kv_row) * D;
 #pragma unroll
       for (int q = 0; q < D / 64; ++q) {
         const int col = hf * (D / 2) + q * 32;
@@ -529,10 +564,12 @@ int num_sms() {
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  const int n_tiles = ceil_div(a.S, kTile);
-  const int S_pad = n_tiles * kTile;
-  const int rows_total = a.B * a.Hq * S_pad;
-  const long long acc_elems = (long long)a.B * a.Hq * a.S * D;
+  const bool packed = a.cu != nullptr;
+  const int n_tiles = ceil_div(packed ? a.max_seqlen : a.S, kTile);  // key tiles of the longest sequence
+  const int S_pad = packed ? a.S : ceil_div(a.S, kTile) * kTile;     // row stride of D / LSE2
+  const int rows_valid = packed ? a.Hq * a.S : a.B * a.Hq * S_pad;
+  const int rows_total = packed ? rows_valid + kRowPad : rows_valid;
+  const long long acc_elems = (long long)(packed ? 1 : a.B) * a.Hq * a.S * D;
   const int sms = num_sms();
   {
     const int threads = 256;
@@ -541,7 +578,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     trace_begin(kKernelBwdPrep, stream);
     bwd_prep_kernel<D><<<blocks, threads, 0, stream>>>(
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse, a.dvec, a.lse2, a.dq_acc,
-        rows_total, a.S, S_pad, 1.4426950408889634f, acc_elems / 4);
+        rows_total, rows_valid, a.S, S_pad, 1.4426950408889634f, acc_elems / 4);
     cudaError_t e = cudaGetLastError();
     trace_end(kKernelBwdPrep, stream);
     if (e != cudaSuccess) return e;
@@ -552,12 +589,13 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     p.dvec = a.dvec;
     p.dk = static_cast<uint16_t*>(a.dk);
     p.dv = static_cast<uint16_t*>(a.dv);
+    p.cu = a.cu;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.S = a.S;
     p.S_pad = S_pad;
     p.causal = a.causal;
-    p.n_tiles = n_tiles;
+    p.max_seqlen = a.max_seqlen;
     p.scale = a.scale;
     p.scale_log2 = a.scale_log2;
     p.status = a.status;

@@ -52,6 +52,10 @@ struct BwdArgs {
   float* dvec;                 // f32 [B*Hq, S_pad]: D_i = rowsum(dO * O)
   float* lse2;                 // f32 [B*Hq, S_pad]: LSE * log2(e), +inf past S
   float* dq_acc;               // f32 [B*Hq, S, D]
+  const int* cu;               // packed batch: device int32 [B + 1] sequence bounds; nullptr = dense
+  int max_seqlen;              // packed batch: bound on every sequence's length
+  // Packed batch: B sequences, S = total rows, tensors [H, S, D], dvec / lse2 [Hq*S + kRowPad]
+  // with no per-head padding.
   int B, Hq, Hkv, S, D, causal;
   float scale, scale_log2;
   int* status;
@@ -87,6 +91,20 @@ inline BwdWorkspace bwd_workspace_layout(int B, int Hq, int S, int D) {
   w.lse2_off = align256(w.dvec_off + rows_pad * sizeof(float));
   w.dqacc_off = align256(w.lse2_off + rows_pad * sizeof(float));
   w.total = align256(w.dqacc_off + (size_t)B * Hq * S * D * sizeof(float));
+  return w;
+}
+
+// Packed batches: the D and LSE2 rows are [Hq * T] plus kRowPad rows of padding, enough for the
+// widened (16-byte aligned) 132-row copies of the last query tile.
+constexpr int kRowPad = 256;
+
+inline BwdWorkspace bwd_workspace_layout_packed(int Hq, int T, int D) {
+  BwdWorkspace w;
+  const size_t rows = (size_t)Hq * T + kRowPad;
+  w.dvec_off = 0;
+  w.lse2_off = align256(w.dvec_off + rows * sizeof(float));
+  w.dqacc_off = align256(w.lse2_off + rows * sizeof(float));
+  w.total = align256(w.dqacc_off + (size_t)Hq * T * D * sizeof(float));
   return w;
 }
 

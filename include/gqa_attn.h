@@ -167,6 +167,37 @@ int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
                         int causal, float scale, int num_splits, void* stream);
 
 /*
+ * Size in bytes of the device workspace gqa_attn_bwd_varlen needs for Hq query
+ * heads over T packed rows (256-byte aligned sections: D and LSE*log2(e) rows,
+ * f32 [Hq*T + 256] each, then the f32 dQ accumulator [Hq, T, D]).
+ * Returns 0 for unsupported sizes.
+ */
+size_t gqa_attn_bwd_varlen_workspace_size(int Hq, int Hkv, int T, int D);
+
+/*
+ * Backward of packed self-attention over variable-length sequences: the
+ * gradients of L = sum(O * dO) for the forward of gqa_attn_fwd_varlen with
+ * cu_seqlens_q = cu_seqlens_k = cu_seqlens (each sequence attends only to
+ * itself; causal: query r of a sequence sees its keys j <= r).
+ *   q, o, dO, dq [Hq,T,D], k, v, dk, dv [Hkv,T,D] (bf16, device), lse [Hq,T]
+ *   (f32, as the forward wrote it); cu_seqlens: DEVICE int32 [nseq + 1],
+ *   nondecreasing, first 0, last T; max_seqlen >= every sequence's length.
+ * dK, dV are summed over each KV head's query heads inside one CTA (bitwise
+ * deterministic); dQ accumulates in f32 in the workspace (caller-owned,
+ * 256-byte aligned, >= gqa_attn_bwd_varlen_workspace_size bytes).
+ * Errors: as gqa_attn_bwd on the host (plus nseq, T < 1, max_seqlen outside
+ * [1, T]); device-side bounds are checked as in gqa_attn_fwd_varlen (invalid
+ * sequences skipped, GQA_ERR_INVALID_ARG from gqa_attn_get_error()).
+ * Passage: aiinsiders.net, "A compiler that derives GPU kernels matches
+ * hand-tuned code" (the backward as a comprehension, f32 accumulation);
+ * RustingBrain docs, "Training infrastructure" (batches of token windows).
+ */
+int gqa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                        void* dq, void* dk, void* dv, const int* cu_seqlens, int nseq, int max_seqlen, void* workspace,
+                        size_t workspace_bytes, int Hq, int Hkv, int T, int D, int causal, float scale,
+                        void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device. Returns GQA_OK, GQA_ERR_TIMEOUT if a kernel gave up on a
  * wait since the last call, GQA_ERR_INTERNAL if a kernel's own shared-memory

@@ -1,12 +1,12 @@
 """GPU parity of packed variable-length batches (sequences laid end to end along the token axis)
-with the f64 oracle's ``forward_varlen``."""
+with the f64 oracle's ``forward_varlen`` and ``backward_varlen``."""
 
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_helpers import assert_fwd_close, gqa
+from gpu_helpers import assert_fwd_close, assert_grad_close, gqa
 from gqa_inputs import draw_lengths, make_inputs, make_packed_inputs, to_f64
 
 pytestmark = pytest.mark.gpu
@@ -117,3 +117,78 @@ def test_host_rejects_bad_arguments():
         g.gqa_attn_fwd_varlen(q, k, k, cu, cu, 0)
     with pytest.raises(ValueError):
         g.gqa_attn_fwd_varlen(q, k, k, cu.long(), cu, 64)
+
+
+def _fwd_bwd_case(g, Hq, Hkv, lens, D, seed, causal=True):
+    """Packed self-attention: forward, then backward from the forward's O and LSE."""
+    q, k, v, dO, cu, _ = make_packed_inputs(Hq, Hkv, lens, lens, D, seed)
+    scale = 1.0 / np.sqrt(D)
+    qd, kd, vd, dOd, cud = q.cuda(), k.cuda(), v.cuda(), dO.cuda(), cu.cuda()
+    o, lse = g.gqa_attn_fwd_varlen(qd, kd, vd, cud, cud, max(lens), causal=causal, scale=scale)
+    dq, dk, dv = g.gqa_attn_bwd_varlen(qd, kd, vd, o, dOd, lse, cud, max(lens), causal=causal, scale=scale)
+    assert g.gqa_attn_get_error() == 0
+    qf, kf, vf, dOf = (to_f64(t) for t in (q, k, v, dO))
+    where = f"varlen bwd Hq={Hq} Hkv={Hkv} lens={lens} D={D} causal={causal}"
+    O_ref, L_ref = oracle.forward_varlen(qf, kf, vf, cu.numpy(), cu.numpy(), causal=causal, scale=scale)
+    assert_fwd_close(o.float().cpu().numpy()[None], lse.cpu().numpy()[None], O_ref[None], L_ref[None], where)
+    dQ, dK, dV = oracle.backward_varlen(qf, kf, vf, dOf, cu.numpy(), causal=causal, scale=scale)
+    for name, got, ref in (("dQ", dq, dQ), ("dK", dk, dK), ("dV", dv, dV)):
+        assert_grad_close(name, got.float().cpu().numpy(), ref, where)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("lens", PACKS)
+def test_packed_backward(lens, D):
+    g = gqa()
+    _fwd_bwd_case(g, 4, 2, lens, D, seed=sum(lens) * 3 + D)
+
+
+@pytest.mark.parametrize("lens", [[130, 5, 400], [1, 1, 1]])
+def test_packed_backward_non_causal(lens):
+    g = gqa()
+    _fwd_bwd_case(g, 6, 3, lens, 64, seed=11 + len(lens), causal=False)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (12, 4), (16, 1)])
+def test_packed_backward_head_groupings(Hq, Hkv):
+    g = gqa()
+    _fwd_bwd_case(g, Hq, Hkv, [1, 200, 383, 4, 129], 128, seed=Hq + Hkv)
+
+
+def test_packed_backward_many_random_lengths():
+    g = gqa()
+    lens = draw_lengths(20, 1, 600, seed=13)
+    _fwd_bwd_case(g, 8, 2, lens, 128, seed=13)
+
+
+def test_packed_backward_equals_dense_batch():
+    """At equal lengths the packed backward matches the dense one: dK, dV bitwise (both reduce
+    over the group in a fixed order in one CTA), dQ within f32 reduction-order noise."""
+    g = gqa()
+    B, Hq, Hkv, S, D = 3, 8, 2, 333, 128
+    q, k, v, dO = (t.cuda() for t in make_inputs(B, Hq, Hkv, S, D, 19))
+    o, lse = g.gqa_attn_fwd(q, k, v)
+    dq_d, dk_d, dv_d = g.gqa_attn_bwd(q, k, v, o, dO, lse)
+
+    def pack(x):  # [B, H, S, D] -> [H, B*S, D]
+        return x.permute(1, 0, 2, 3).reshape(x.shape[1], B * S, x.shape[3]).contiguous()
+
+    cu = torch.arange(0, (B + 1) * S, S, dtype=torch.int32, device="cuda")
+    lse_p = lse.permute(1, 0, 2).reshape(Hq, B * S).contiguous()
+    dq_p, dk_p, dv_p = g.gqa_attn_bwd_varlen(pack(q), pack(k), pack(v), pack(o), pack(dO), lse_p, cu, S)
+    assert g.gqa_attn_get_error() == 0
+    assert torch.equal(dk_p, pack(dk_d)) and torch.equal(dv_p, pack(dv_d))
+    assert (dq_p.float() - pack(dq_d).float()).abs().max().item() <= 1e-2 * pack(dq_d).float().abs().max().item()
+
+
+def test_packed_backward_invalid_bounds_reported():
+    g = gqa()
+    Hq, Hkv, D, T = 4, 2, 64, 300
+    q, k, v, dO, _, _ = make_packed_inputs(Hq, Hkv, [T], [T], D, seed=6)
+    q, k, v, dO = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+    o = torch.zeros_like(q)
+    lse = torch.zeros(Hq, T, device="cuda")
+    for cu, max_len in (([0, 100, 50, 300], 300), ([0, 100, 400, 300], 300), ([0, 299, 300, 300], 200)):
+        cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+        g.gqa_attn_bwd_varlen(q, k, v, o, dO, lse, cu_d, max_len)
+        assert g.gqa_attn_get_error() == g.GQA_ERR_INVALID_ARG, cu
