@@ -325,6 +325,47 @@ def packed_measurement(g, torch, peaks, peak_src, steps=20, warmup=3):
                          "fwd_kernel": {"achieved": fwd_tf, "frac": fwd_tf / peak}}}
 
 
+def deterministic_measurement(g, torch, w, peaks, peak_src, steps, warmup, bufs):
+    """The same fwd+bwd step with the deterministic backward (query-major dQ kernel, KV-major dK/dV
+    kernel), timed back to back like the main line. `value` counts the same algorithmic flops as
+    the main line (4 D + 10 D per visible pair), so the two compare by time; the kernels' rooflines
+    count the work they execute (dK/dV kernel 8 D per pair, dQ kernel 6 D per pair)."""
+    q, k, v, dO, o, lse, dq, dk, dv, ws = bufs
+
+    def step():
+        g.gqa_attn_fwd(q, k, v, causal=True, scale=w.scale, o=o, lse=lse)
+        g.gqa_attn_bwd(q, k, v, o, dO, lse, causal=True, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                       deterministic=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    g.gqa_attn_trace_arm()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    tr = g.gqa_attn_trace_collect()
+    if g.gqa_attn_get_error() != 0:
+        raise RuntimeError("deterministic backward failed")
+    ms = e0.elapsed_time(e1) / steps
+    fwd_fl, bwd_fl = flops(w.B, w.Hq, w.S, w.D)
+    pairs_fl = bwd_fl / 10.0  # D flops per visible pair, all heads
+    avg = {name: (t_ / n_ if n_ else None) for name, (n_, t_) in tr.items()}
+    peak = peaks["bf16_tflops_sustained"]
+    dq_tf = 6.0 * pairs_fl / (avg["bwd_dq"] * 1e-3) / 1e12
+    dkdv_tf = 8.0 * pairs_fl / (avg["bwd_dkdv"] * 1e-3) / 1e12
+    return {"workload": config_of(w)["workload"] + ", deterministic backward",
+            "value": (fwd_fl + bwd_fl) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "kernels": {k_: {"launches": n_, "avg_ms": avg[k_]} for k_, (n_, _) in tr.items() if n_},
+            "roofline": {"kernel": "bwd_dq", "bound": "tensor", "achieved": dq_tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": dq_tf / peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 dense, sustained (kernel timed inside back-to-back steps)",
+                         "bwd_dkdv_kernel": {"achieved": dkdv_tf, "frac": dkdv_tf / peak}}}
+
+
 def config_of(w):
     return {"workload": f"{w.name}: causal GQA B={w.B} Hq={w.Hq} Hkv={w.Hkv} S={w.S} D={w.D}",
             "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": True, "scale": w.scale,
@@ -343,7 +384,7 @@ def main():
                     help="B,Hq,Hkv,S,D: override the workload's shape (same seed and value distributions); "
                          "for profiling smaller cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode, prefill-over-cache and packed-batch measurements")
+    ap.add_argument("--no-decode", action="store_true", help="skip the deterministic-backward, decode, prefill-over-cache and packed-batch measurements")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -495,6 +536,8 @@ def main():
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_decode:
+        line["deterministic"] = deterministic_measurement(g, torch, w, peaks, peak_src, args.steps, args.warmup,
+                                                          (q, k, v, dO, o, lse, dq, dk, dv, ws))
         line["decode"] = decode_measurement(g, torch, peaks, peak_src)
         line["prefill"] = prefill_measurement(g, torch, peaks, peak_src)
         line["packed"] = packed_measurement(g, torch, peaks, peak_src)

@@ -46,7 +46,7 @@ __all__ = [
     "lib_path",
 ]
 
-KERNEL_NAMES = ("fwd", "bwd_prep", "bwd_main", "bwd_convert", "decode_split", "decode_combine")
+KERNEL_NAMES = ("fwd", "bwd_prep", "bwd_main", "bwd_convert", "decode_split", "decode_combine", "bwd_dkdv", "bwd_dq")
 
 GQA_OK = 0
 GQA_ERR_INVALID_ARG = -1
@@ -123,11 +123,12 @@ def gqa_attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, S: int, D: int) -> in
 
 
 def gqa_attn_bwd(q, k, v, o, dO, lse, causal: bool = True, scale: float | None = None,
-                 dq=None, dk=None, dv=None, workspace=None, stream=None):
+                 dq=None, dk=None, dv=None, workspace=None, stream=None, deterministic: bool = False):
     """Backward of sum(o * dO): returns (dq, dk, dv), bf16, shaped like q, k, v.
 
     ``workspace`` (optional) is a uint8 CUDA tensor of at least
     ``gqa_attn_bwd_workspace_size(...)`` bytes; one is allocated if omitted.
+    ``deterministic`` selects gqa_attn_bwd_deterministic (bitwise reproducible dQ).
     """
     B, Hq, Hkv, S, D = _dims(q, k, v)
     for name, t in (("o", o), ("dO", dO)):
@@ -144,11 +145,12 @@ def gqa_attn_bwd(q, k, v, o, dO, lse, causal: bool = True, scale: float | None =
     if workspace is None:
         workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
     nbytes = workspace.numel() * workspace.element_size()
-    rc = _lib.load().gqa_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
-                                  lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                                  workspace.data_ptr(), nbytes, B, Hq, Hkv, S, D, int(bool(causal)),
-                                  float(scale), _stream_handle(stream))
-    _check(rc, "gqa_attn_bwd")
+    name = "gqa_attn_bwd_deterministic" if deterministic else "gqa_attn_bwd"
+    rc = getattr(_lib.load(), name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
+                                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                    workspace.data_ptr(), nbytes, B, Hq, Hkv, S, D, int(bool(causal)),
+                                    float(scale), _stream_handle(stream))
+    _check(rc, name)
     return dq, dk, dv
 
 

@@ -63,14 +63,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [nheads, S, D] tensor (D innermost) as a 3-D tiled map with box {inner, 128, 1}.
+// [nheads, S, D] tensor (D innermost) as a 3-D tiled map with box {inner, box_rows, 1}.
 cudaError_t encode_3d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, int elem_bytes, int D, int S,
-                      int nheads, int box_inner, CUtensorMapSwizzle swz) {
+                      int nheads, int box_inner, CUtensorMapSwizzle swz, int box_rows = kTile) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)nheads};
   cuuint64_t strides[2] = {(cuuint64_t)D * elem_bytes, (cuuint64_t)S * D * elem_bytes};
-  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)kTile, 1};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -229,9 +229,13 @@ size_t gqa_attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D) {
   return bwd_workspace_layout(B, Hq, S, D).total;
 }
 
-int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S,
-                 int D, int causal, float scale, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int bwd_dense(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
+              void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S, int D,
+              int causal, float scale, int deterministic, void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace) return GQA_ERR_INVALID_ARG;
   int rc = check_common(B, Hq, Hkv, S, D, scale);
   if (rc != GQA_OK) return rc;
@@ -241,9 +245,18 @@ int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   const BwdWorkspace ws = bwd_workspace_layout(B, Hq, S, D);
   if (workspace_bytes < ws.total) return GQA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  CUtensorMap mq, mk, mv, mdo, macc;
+  CUtensorMap mq, mk, mv, mdo, macc, mdq;
   cudaError_t e;
   if ((e = encode_bf16(&mq, q, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_bf16(&mdq, dq, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
+  // 64-row K / V boxes: the query-major dQ kernel streams keys in 64-row units.
+  CUtensorMap mk64, mv64;
+  if ((e = encode_3d(&mk64, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, S, B * Hkv, kChunk, CU_TENSOR_MAP_SWIZZLE_128B,
+                     64)) != cudaSuccess)
+    return fail_cuda(e);
+  if ((e = encode_3d(&mv64, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, S, B * Hkv, kChunk, CU_TENSOR_MAP_SWIZZLE_128B,
+                     64)) != cudaSuccess)
+    return fail_cuda(e);
   if ((e = encode_bf16(&mk, k, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
   if ((e = encode_bf16(&mv, v, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
   if ((e = encode_bf16(&mdo, dO, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
@@ -258,6 +271,10 @@ int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   a.map_v = &mv;
   a.map_do = &mdo;
   a.map_dqacc = &macc;
+  a.map_dq = &mdq;
+  a.map_k64 = &mk64;
+  a.map_v64 = &mv64;
+  a.deterministic = deterministic;
   a.o = o;
   a.dO = dO;
   a.lse = lse;
@@ -280,6 +297,25 @@ int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   a.status = status;
   if ((e = launch_bwd(a, static_cast<cudaStream_t>(stream))) != cudaSuccess) return fail_cuda(e);
   return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S,
+                 int D, int causal, float scale, void* stream) {
+  return bwd_dense(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, S, D, causal, scale, 0,
+                   stream);
+}
+
+int gqa_attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                               const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                               size_t workspace_bytes, int B, int Hq, int Hkv, int S, int D, int causal, float scale,
+                               void* stream) {
+  return bwd_dense(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, S, D, causal, scale, 1,
+                   stream);
 }
 
 size_t gqa_attn_bwd_varlen_workspace_size(int Hq, int Hkv, int T, int D) {
@@ -322,6 +358,10 @@ int gqa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void*
   a.map_v = &mv;
   a.map_do = &mdo;
   a.map_dqacc = &macc;
+  a.map_dq = nullptr;
+  a.map_k64 = nullptr;
+  a.map_v64 = nullptr;
+  a.deterministic = 0;
   a.o = o;
   a.dO = dO;
   a.lse = lse;

@@ -170,7 +170,9 @@ struct BwdKParams {
 //   step's Q and dO tiles (free once dQ(t) has completed). Warp 10 issues the TMA
 //   reduce-adds, waits until they have read the staging and hands the Q/dO stage
 //   back to the producer; the reduce streams out while the next step runs.
-template <int D>
+// kDq = false: the deterministic backward's dK/dV kernel. It skips the dQ partial (a
+// query-major kernel computes dQ); the Q/dO stage is released once dK and dV have read it.
+template <int D, bool kDq>
 __global__ void __launch_bounds__(352, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
@@ -338,19 +340,25 @@ __global__ void __launch_bounds__(352, 1)
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_ts(tbase + C::kDKCol, tbase + C::kSPCol + p_col(kk) + 32u,
                   stage_desc(dq_mn0, t) + (uint64_t)((kk * 2048) >> 4), idesc_tb, (t > 0 || kk > 0) ? 1u : 0u);
+        if (kDq) {
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ss(tbase + C::kDPCol, dds_mn + (uint64_t)((kk * 2048) >> 4), dk_mn + (uint64_t)((kk * 2048) >> 4),
-                  idesc_mm, kk > 0 ? 1u : 0u);
-        umma_commit(&bars->dq_full);
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ss(tbase + C::kDPCol, dds_mn + (uint64_t)((kk * 2048) >> 4), dk_mn + (uint64_t)((kk * 2048) >> 4),
+                    idesc_mm, kk > 0 ? 1u : 0u);
+          umma_commit(&bars->dq_full);
+        } else {
+          umma_commit(&bars->qdo_empty[t % ST]);  // dK(t) and dV(t) were the last readers of Q(t), dO(t)
+        }
         if (t + 1 < n_steps) {
           const int t1 = t + 1;
           if (!(ok = mbar_wait(&bars->qdo_full[t1 % ST], (t1 / ST) & 1, wg))) break;
           tc_fence_after();
           issue_kmajor(C::kSPCol, dk_k, stage_desc(dq_k0, t1));  // P^T(t), dS^T(t) were consumed by dV(t), dK(t)
           umma_commit(&bars->s_full);
-          if (!(ok = mbar_wait(&bars->dq_free, t & 1, wg))) break;
-          tc_fence_after();
+          if (kDq) {  // dP(t+1) overwrites the dQ(t) partial: wait until it has been read out
+            if (!(ok = mbar_wait(&bars->dq_free, t & 1, wg))) break;
+            tc_fence_after();
+          }
           issue_kmajor(C::kDPCol, dv_k, stage_desc(ddo_k0, t1));
           umma_commit(&bars->dp_full);
         }
@@ -363,7 +371,7 @@ __global__ void __launch_bounds__(352, 1)
     // ------------------------------------------------------------ dQ reduce warp
     // Issues the TMA reduce-adds of each step's staged dQ partial, waits until they have read
     // the staging (the step's Q and dO tiles), and hands the stage back to the producer.
-    if (lane == 0) {
+    if (kDq && lane == 0) {
       tma_prefetch_desc(&map_acc);
       for (int t = 0; t < n_steps; ++t) {
         if (!mbar_wait(&bars->stage_full, t & 1, wg)) break;
@@ -466,17 +474,20 @@ __global__ void __launch_bounds__(352, 1)
         }
         tmem_st_32x32b_x16(sp_tmem + hf * 64 + 32 + q * 16, pk);
         // dS[row = key][col = query] into the MN-major (query-contiguous) 128B-swizzled tile.
+        if (kDq) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int unit = q * 4 + u;  // 16-byte unit within this half's 128-byte row
-          *reinterpret_cast<uint4*>(sds_half + (row >> 3) * 1024 + (row & 7) * 128 + ((unit ^ (row & 7)) << 4)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          for (int u = 0; u < 4; ++u) {
+            const int unit = q * 4 + u;  // 16-byte unit within this half's 128-byte row
+            *reinterpret_cast<uint4*>(sds_half + (row >> 3) * 1024 + (row & 7) * 128 + ((unit ^ (row & 7)) << 4)) =
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
         }
       }
-      fence_proxy_async_smem();
+      if (kDq) fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(&bars->ds_full);
+      if (!kDq) continue;
 
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, t & 1, wg));
       if (!ok) break;
@@ -564,12 +575,13 @@ int num_sms() {
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
+  const bool det = a.deterministic != 0;  // dQ by the query-major kernel, no f32 accumulator
   const bool packed = a.cu != nullptr;
   const int n_tiles = ceil_div(packed ? a.max_seqlen : a.S, kTile);  // key tiles of the longest sequence
   const int S_pad = packed ? a.S : ceil_div(a.S, kTile) * kTile;     // row stride of D / LSE2
   const int rows_valid = packed ? a.Hq * a.S : a.B * a.Hq * S_pad;
   const int rows_total = packed ? rows_valid + kRowPad : rows_valid;
-  const long long acc_elems = (long long)(packed ? 1 : a.B) * a.Hq * a.S * D;
+  const long long acc_elems = det ? 0 : (long long)(packed ? 1 : a.B) * a.Hq * a.S * D;
   const int sms = num_sms();
   {
     const int threads = 256;
@@ -599,17 +611,18 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     p.scale = a.scale;
     p.scale_log2 = a.scale_log2;
     p.status = a.status;
-    cudaError_t e =
-        cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    auto kern = det ? bwd_main_kernel<D, false> : bwd_main_kernel<D, true>;
+    const KernelKind kind = det ? kKernelBwdDkdv : kKernelBwdMain;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(a.B * a.Hkv), (unsigned)n_tiles);
-    trace_begin(kKernelBwdMain, stream);
-    bwd_main_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_do,
-                                                                     *a.map_dqacc, p);
+    trace_begin(kind, stream);
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_do, *a.map_dqacc, p);
     e = cudaGetLastError();
-    trace_end(kKernelBwdMain, stream);
+    trace_end(kind, stream);
     if (e != cudaSuccess) return e;
   }
+  if (det) return launch_bwd_dq(a, stream);
   {
     const long long n8 = acc_elems / 8;
     const int threads = 256;

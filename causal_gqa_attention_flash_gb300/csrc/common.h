@@ -43,6 +43,9 @@ struct BwdArgs {
   const CUtensorMap* map_v;
   const CUtensorMap* map_do;   // [B*Hq, S, D] bf16
   const CUtensorMap* map_dqacc;// [B*Hq, S, D] f32, box {32, 128, 1}, 128B swizzle
+  const CUtensorMap* map_dq;   // [B*Hq, S, D] bf16 (deterministic path: dQ stored by TMA)
+  const CUtensorMap* map_k64;  // [B*Hkv, S, D] bf16, box {64, 64, 1} (deterministic path)
+  const CUtensorMap* map_v64;
   const void* o;               // bf16 [B, Hq, S, D]
   const void* dO;              // bf16 [B, Hq, S, D]
   const float* lse;            // f32 [B, Hq, S]
@@ -54,6 +57,7 @@ struct BwdArgs {
   float* dq_acc;               // f32 [B*Hq, S, D]
   const int* cu;               // packed batch: device int32 [B + 1] sequence bounds; nullptr = dense
   int max_seqlen;              // packed batch: bound on every sequence's length
+  int deterministic;           // 1: dQ by the query-major kernel (dense batches only)
   // Packed batch: B sequences, S = total rows, tensors [H, S, D], dvec / lse2 [Hq*S + kRowPad]
   // with no per-head padding.
   int B, Hq, Hkv, S, D, causal;
@@ -116,7 +120,9 @@ enum KernelKind {
   kKernelBwdConvert = 3,
   kKernelDecodeSplit = 4,
   kKernelDecodeCombine = 5,
-  kKernelCount = 6
+  kKernelBwdDkdv = 6,
+  kKernelBwdDq = 7,
+  kKernelCount = 8
 };
 void trace_begin(int kind, cudaStream_t s);
 void trace_end(int kind, cudaStream_t s);
@@ -127,6 +133,7 @@ int record_cuda_error(cudaError_t e);
 // Host launchers (fwd.cu, bwd.cu). Return a cudaError_t.
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

@@ -167,6 +167,22 @@ int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
                         int causal, float scale, int num_splits, void* stream);
 
 /*
+ * Deterministic backward: the same arguments, workspace and results as
+ * gqa_attn_bwd, but dQ is bitwise reproducible. A query-major kernel computes
+ * each 128-row dQ tile in one CTA, in a fixed key order (recomputing S and dP
+ * per (query, key) pair: 14 D flops per pair for the whole backward instead of
+ * 10 D), and the KV-major kernel computes only dK and dV. No f32 dQ
+ * accumulator is used (the workspace's dQ section is left untouched).
+ * Passage: aiinsiders.net, "A compiler that derives GPU kernels matches
+ * hand-tuned code" (the backward as a comprehension); the atomic-free dQ split
+ * is the alternative to the f32 reduce-add named with the fused backward.
+ */
+int gqa_attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                               const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                               size_t workspace_bytes, int B, int Hq, int Hkv, int S, int D, int causal, float scale,
+                               void* stream);
+
+/*
  * Size in bytes of the device workspace gqa_attn_bwd_varlen needs for Hq query
  * heads over T packed rows (256-byte aligned sections: D and LSE*log2(e) rows,
  * f32 [Hq*T + 256] each, then the f32 dQ accumulator [Hq, T, D]).
@@ -239,7 +255,9 @@ int gqa_attn_selftest_wait_timeout(int limit_us, void* stream);
 #define GQA_KERNEL_BWD_CONVERT 3
 #define GQA_KERNEL_DECODE_SPLIT 4
 #define GQA_KERNEL_DECODE_COMBINE 5
-#define GQA_KERNEL_COUNT 6
+#define GQA_KERNEL_BWD_DKDV 6 /* the deterministic backward's dK/dV kernel */
+#define GQA_KERNEL_BWD_DQ 7   /* the deterministic backward's query-major dQ kernel */
+#define GQA_KERNEL_COUNT 8
 int gqa_attn_trace_arm(void);
 int gqa_attn_trace_collect(int* launches, double* total_ms);
 
