@@ -24,6 +24,9 @@ multiply dO by ``do_std`` (0.1, i.e. N(0, 1e-2) read as a variance; 1.0 for
 the tiny case); round each to bfloat16 (round-to-nearest-even). The same
 bfloat16 bits feed the GPU path and the oracle.
 
+Rotary-position tables (``rope_tables``) are inputs too: cos and sin of
+position times base^(-2i/D), the table a caller hands to the RoPE entry points.
+
 Packed batches of variable-length sequences (``make_packed_inputs``) lay the
 sequences end to end along the token axis, one [H, T, D] tensor per operand;
 the lengths are given, or drawn by ``draw_lengths`` (uniform on [lo, hi] with
@@ -116,6 +119,16 @@ def make_packed_inputs(Hq: int, Hkv: int, lens_q, lens_k, D: int, seed: int,
     if with_do:
         dO = (torch.randn(Hq, Tq, D, generator=g, dtype=torch.float32) * do_std).to(torch.bfloat16)
     return q, k, v, dO, cu_q, cu_k
+
+
+def rope_tables(S: int, D: int, base: float = 10000.0, offset: int = 0):
+    """Rotary-position tables, the input a caller of the RoPE entry points supplies: f32 CPU
+    tensors cos, sin of shape [S, D/2] with entry [p, i] = cos / sin((offset + p) * base**(-2i/D)),
+    evaluated in float64 and rounded to float32."""
+    i = torch.arange(D // 2, dtype=torch.float64)
+    p = torch.arange(offset, offset + S, dtype=torch.float64)
+    ang = p[:, None] * torch.pow(torch.tensor(float(base), dtype=torch.float64), -2.0 * i / D)[None, :]
+    return torch.cos(ang).to(torch.float32), torch.sin(ang).to(torch.float32)
 
 
 def workload_inputs(name: str, with_do: bool = True):

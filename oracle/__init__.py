@@ -14,13 +14,15 @@ anything here, and nothing here imports the product.
   (Sq <= Sk, bottom-right causal alignment).
 * ``oracle.varlen``    -- variable-length sequences packed along the token
   axis (each sequence attends only to itself).
+* ``oracle.rope``      -- rotary position embedding of Q and K before the
+  attention (rotate-half pairing, caller-supplied cos/sin tables).
 
 Pins (in ``tests/``): decimal brute force, central finite differences,
 closed forms, invariants, torch f64 SDPA, monoid regrouping and a stored
 golden file. Every function here is pinned; none is "parity unpinned".
 """
 
-from . import attention, decode, monoid, varlen  # noqa: F401
+from . import attention, decode, monoid, rope, varlen  # noqa: F401
 from .attention import (  # noqa: F401
     backward,
     backward_dkdv_rows,
@@ -30,4 +32,5 @@ from .attention import (  # noqa: F401
     kv_head_of,
 )
 from .decode import forward_cached  # noqa: F401
+from .rope import backward_rope, forward_rope  # noqa: F401
 from .varlen import backward_varlen, forward_varlen  # noqa: F401

@@ -463,6 +463,80 @@ def check_varlen(orc):
     assert np.array_equal(O1[:, perm], O2) and np.array_equal(L1[:, perm], L2), "varlen pack order"
 
 
+# ---------------------------------------------------------------------------
+# 11. Rotary position embedding: the rotation against complex multiplication,
+#     norms kept, scores that depend only on the distance between positions,
+#     central finite differences of L = sum(O * dO) through the rotation, and
+#     torch f64 autograd of an explicit rotation followed by SDPA.
+# ---------------------------------------------------------------------------
+
+def _tables64(S, D, base=10000.0, offset=0):
+    i = np.arange(D // 2)
+    ang = (offset + np.arange(S))[:, None] * base ** (-2.0 * i / D)[None, :]
+    return np.cos(ang), np.sin(ang)
+
+
+def check_rope(orc):
+    rng = _rng(20)
+    S, D = 9, 8
+    cos, sin = _tables64(S, D)
+    x = rng.standard_normal((2, 3, S, D))
+    xr = orc.rope.rotate(x, cos, sin)
+    z = (x[..., : D // 2] + 1j * x[..., D // 2:]) * np.exp(1j * np.arctan2(sin, cos))
+    assert _relerr(xr, np.concatenate([z.real, z.imag], axis=-1)) <= 1e-14, "rotation vs complex product"
+    assert np.max(np.abs(np.linalg.norm(xr, axis=-1) - np.linalg.norm(x, axis=-1))) <= 1e-13, "norm kept"
+    assert _relerr(orc.rope.unrotate(xr, cos, sin), x) <= 1e-14, "unrotate inverts rotate"
+    # scores depend on positions only through their difference
+    q = rng.standard_normal((S, D))
+    k = rng.standard_normal((S, D))
+    c2, s2 = _tables64(S, D, offset=37)
+    s_a = orc.rope.rotate(q, cos, sin) @ orc.rope.rotate(k, cos, sin).T
+    s_b = orc.rope.rotate(q, c2, s2) @ orc.rope.rotate(k, c2, s2).T
+    assert np.max(np.abs(s_a - s_b)) <= 1e-12, "relative-position property"
+    # gradients through the rotation: central finite differences
+    B, Hq, Hkv, S, D = 1, 4, 2, 6, 4
+    cos, sin = _tables64(S, D, base=3.0)
+    q = rng.standard_normal((B, Hq, S, D))
+    k = rng.standard_normal((B, Hkv, S, D))
+    v = rng.standard_normal((B, Hkv, S, D))
+    dO = rng.standard_normal((B, Hq, S, D))
+    dQ, dK, dV = orc.backward_rope(q, k, v, dO, cos, sin, causal=True, scale=0.7)
+
+    def loss(qq, kk, vv):
+        return float(np.sum(orc.forward_rope(qq, kk, vv, cos, sin, causal=True, scale=0.7)[0] * dO))
+
+    h = 1e-5
+    for name, X, G in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        num = np.zeros_like(X)
+        it = np.nditer(X, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            Xp = X.copy()
+            Xm = X.copy()
+            Xp[idx] += h
+            Xm[idx] -= h
+            args_p = {"q": (Xp, k, v), "k": (q, Xp, v), "v": (q, k, Xp)}[name]
+            args_m = {"q": (Xm, k, v), "k": (q, Xm, v), "v": (q, k, Xm)}[name]
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert _relerr(G, num) <= 1e-6, f"rope d{name} vs finite differences"
+    # torch f64: explicit rotation, SDPA, autograd
+    G_ = Hq // Hkv
+    tq, tk, tv = (torch.tensor(t, requires_grad=True) for t in (q, k, v))
+    tc, ts = torch.tensor(cos), torch.tensor(sin)
+
+    def trot(t):
+        lo, hi = t[..., : D // 2], t[..., D // 2:]
+        return torch.cat([lo * tc - hi * ts, hi * tc + lo * ts], dim=-1)
+
+    out = torch.nn.functional.scaled_dot_product_attention(
+        trot(tq), trot(tk).repeat_interleave(G_, dim=1), tv.repeat_interleave(G_, dim=1), is_causal=True, scale=0.7)
+    (out * torch.tensor(dO)).sum().backward()
+    O, _ = orc.forward_rope(q, k, v, cos, sin, causal=True, scale=0.7)
+    assert _relerr(O, out.detach().numpy()) <= 1e-12, "rope forward vs torch"
+    for name, mine, ref in (("dQ", dQ, tq.grad), ("dK", dK, tk.grad), ("dV", dV, tv.grad)):
+        assert _relerr(mine, ref.numpy()) <= 1e-11, f"rope {name} vs torch autograd"
+
+
 ALL_CHECKS = [
     "check_decimal_bruteforce",
     "check_finite_differences",
@@ -474,4 +548,5 @@ ALL_CHECKS = [
     "check_golden",
     "check_decode",
     "check_varlen",
+    "check_rope",
 ]

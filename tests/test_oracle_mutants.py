@@ -18,6 +18,7 @@ from oracle import monoid
 SRC = (pathlib.Path(oracle.__file__).parent / "attention.py").read_text()
 DECODE_SRC = (pathlib.Path(oracle.__file__).parent / "decode.py").read_text()
 VARLEN_SRC = (pathlib.Path(oracle.__file__).parent / "varlen.py").read_text()
+ROPE_SRC = (pathlib.Path(oracle.__file__).parent / "rope.py").read_text()
 
 MUTANTS = {
     "gqa_head_mapping_modulo": ("return h // (Hq // Hkv)", "return h % Hkv"),
@@ -53,6 +54,18 @@ VARLEN_MUTANTS = {
 }
 
 
+ROPE_MUTANTS = {
+    "rope_interleaved_pairs": ("lo, hi = x[..., :h], x[..., h:]", "lo, hi = x[..., 0::2], x[..., 1::2]"),
+    "rope_sin_sign": ("lo * c - hi * s, hi * c + lo * s", "lo * c + hi * s, hi * c - lo * s"),
+    "rope_gradient_not_turned_back": ("return unrotate(gq, cos, sin), unrotate(gk, cos, sin), gv",
+                                      "return gq, gk, gv"),
+    "rope_turned_back_the_wrong_way": ("return rotate(g, cos, -np.asarray(sin, dtype=np.float64))",
+                                       "return rotate(g, cos, np.asarray(sin, dtype=np.float64))"),
+    "rope_values_rotated": ("return forward(rotate(q, cos, sin), rotate(k, cos, sin), v,",
+                            "return forward(rotate(q, cos, sin), rotate(k, cos, sin), rotate(v, cos, sin),"),
+}
+
+
 def _mutant_module(name):
     old, new = MUTANTS[name]
     assert SRC.count(old) >= 1, f"mutation anchor for {name} not found in the oracle source"
@@ -61,6 +74,7 @@ def _mutant_module(name):
     mod.forward_cached = oracle.forward_cached
     mod.forward_varlen = oracle.forward_varlen
     mod.backward_varlen = oracle.backward_varlen
+    mod.rope, mod.forward_rope, mod.backward_rope = oracle.rope, oracle.forward_rope, oracle.backward_rope
     return mod
 
 
@@ -77,6 +91,7 @@ def _decode_mutant_module(name):
     mod.forward_cached = dmod.forward_cached
     mod.forward_varlen = oracle.forward_varlen
     mod.backward_varlen = oracle.backward_varlen
+    mod.rope, mod.forward_rope, mod.backward_rope = oracle.rope, oracle.forward_rope, oracle.backward_rope
     return mod
 
 
@@ -128,3 +143,24 @@ def test_planted_varlen_mistake_is_caught(name):
     mod = _varlen_mutant_module(name)
     with pytest.raises(AssertionError):
         oc.check_varlen(mod)
+
+
+def _rope_mutant_module(name):
+    """The real oracle with a mutated copy of the rotary-embedding oracle."""
+    old, new = ROPE_MUTANTS[name]
+    assert ROPE_SRC.count(old) == 1, f"mutation anchor for {name} not found"
+    src = ROPE_SRC.replace(old, new, 1).replace("from .attention import", "from oracle.attention import")
+    rmod = types.ModuleType(f"oracle_rope_mutant_{name}")
+    exec(compile(src, f"<mutant {name}>", "exec"), rmod.__dict__)
+    mod = types.ModuleType(f"oracle_with_{name}")
+    mod.rope = rmod
+    mod.forward_rope = rmod.forward_rope
+    mod.backward_rope = rmod.backward_rope
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(ROPE_MUTANTS))
+def test_planted_rope_mistake_is_caught(name):
+    mod = _rope_mutant_module(name)
+    with pytest.raises(AssertionError):
+        oc.check_rope(mod)

@@ -48,6 +48,10 @@ def test_varlen_packed_batches():
     oc.check_varlen(oracle)
 
 
+def test_rope():
+    oc.check_rope(oracle)
+
+
 def test_golden_file():
     oc.check_golden(oracle)
 
