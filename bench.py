@@ -366,6 +366,49 @@ def deterministic_measurement(g, torch, w, peaks, peak_src, steps, warmup, bufs)
                          "bwd_dkdv_kernel": {"achieved": dkdv_tf, "frac": dkdv_tf / peak}}}
 
 
+def rope_measurement(g, torch, w, peaks, peak_src, steps, warmup, bufs):
+    """The same fwd+bwd step with the rotary embedding fused in (tables for base 10000): `value`
+    counts the same algorithmic attention flops as the main line, so the two compare by time; the
+    rotation passes (keys once in the forward, queries once in the backward) are listed."""
+    from gqa_inputs import rope_tables
+    q, k, v, dO, o, lse, dq, dk, dv, _ = bufs
+    cos, sin = (t.cuda() for t in rope_tables(w.S, w.D))
+    ws_f = torch.empty(g.gqa_attn_fwd_rope_workspace_size(w.B, w.Hkv, w.S, w.D), device="cuda", dtype=torch.uint8)
+    ws_b = torch.empty(g.gqa_attn_bwd_rope_workspace_size(w.B, w.Hq, w.Hkv, w.S, w.D), device="cuda",
+                       dtype=torch.uint8)
+
+    def step():
+        g.gqa_attn_fwd_rope(q, k, v, cos, sin, scale=w.scale, o=o, lse=lse, workspace=ws_f)
+        g.gqa_attn_bwd_rope(q, k, v, o, dO, lse, cos, sin, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws_b)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    g.gqa_attn_trace_arm()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    tr = g.gqa_attn_trace_collect()
+    if g.gqa_attn_get_error() != 0:
+        raise RuntimeError("rotary-embedding step failed")
+    ms = e0.elapsed_time(e1) / steps
+    fwd_fl, bwd_fl = flops(w.B, w.Hq, w.S, w.D)
+    avg = {name: (t_ / n_ if n_ else None) for name, (n_, t_) in tr.items()}
+    peak = peaks["bf16_tflops_sustained"]
+    main_tf = bwd_fl / (avg["bwd_main"] * 1e-3) / 1e12
+    fwd_tf = fwd_fl / (avg["fwd"] * 1e-3) / 1e12
+    return {"workload": config_of(w)["workload"] + ", rotary embedding (rotate-half, base 10000)",
+            "value": (fwd_fl + bwd_fl) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "kernels": {k_: {"launches": n_, "avg_ms": avg[k_]} for k_, (n_, _) in tr.items() if n_},
+            "roofline": {"kernel": "bwd_main", "bound": "tensor", "achieved": main_tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": main_tf / peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 dense, sustained (kernel timed inside back-to-back steps)",
+                         "fwd_kernel": {"achieved": fwd_tf, "frac": fwd_tf / peak}}}
+
+
 def config_of(w):
     return {"workload": f"{w.name}: causal GQA B={w.B} Hq={w.Hq} Hkv={w.Hkv} S={w.S} D={w.D}",
             "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": True, "scale": w.scale,
@@ -384,7 +427,7 @@ def main():
                     help="B,Hq,Hkv,S,D: override the workload's shape (same seed and value distributions); "
                          "for profiling smaller cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true", help="skip the deterministic-backward, decode, prefill-over-cache and packed-batch measurements")
+    ap.add_argument("--no-decode", action="store_true", help="skip the deterministic-backward, rotary-embedding, decode, prefill-over-cache and packed-batch measurements")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -538,6 +581,8 @@ def main():
     if world == 1 and not args.no_decode:
         line["deterministic"] = deterministic_measurement(g, torch, w, peaks, peak_src, args.steps, args.warmup,
                                                           (q, k, v, dO, o, lse, dq, dk, dv, ws))
+        line["rope"] = rope_measurement(g, torch, w, peaks, peak_src, args.steps, args.warmup,
+                                        (q, k, v, dO, o, lse, dq, dk, dv, ws))
         line["decode"] = decode_measurement(g, torch, peaks, peak_src)
         line["prefill"] = prefill_measurement(g, torch, peaks, peak_src)
         line["packed"] = packed_measurement(g, torch, peaks, peak_src)

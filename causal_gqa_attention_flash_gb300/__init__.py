@@ -40,13 +40,17 @@ __all__ = [
     "gqa_attn_fwd_varlen",
     "gqa_attn_bwd_varlen",
     "gqa_attn_bwd_varlen_workspace_size",
+    "gqa_attn_fwd_rope",
+    "gqa_attn_bwd_rope",
+    "gqa_attn_fwd_rope_workspace_size",
+    "gqa_attn_bwd_rope_workspace_size",
     "gqa_attn_decode_workspace_size",
     "NOALLOC_SCRATCH_BYTES",
     "KERNEL_NAMES",
     "lib_path",
 ]
 
-KERNEL_NAMES = ("fwd", "bwd_prep", "bwd_main", "bwd_convert", "decode_split", "decode_combine", "bwd_dkdv", "bwd_dq")
+KERNEL_NAMES = ("fwd", "bwd_prep", "bwd_main", "bwd_convert", "decode_split", "decode_combine", "bwd_dkdv", "bwd_dq", "rope")
 
 GQA_OK = 0
 GQA_ERR_INVALID_ARG = -1
@@ -325,4 +329,69 @@ def gqa_attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, max_seqlen: int, causal
                                          workspace.data_ptr(), nbytes, Hq, Hkv, T, D, int(bool(causal)),
                                          float(scale), _stream_handle(stream))
     _check(rc, "gqa_attn_bwd_varlen")
+    return dq, dk, dv
+
+
+def _check_tables(cos, sin, S, D, device):
+    for name, t in (("rope_cos", cos), ("rope_sin", sin)):
+        if (not t.is_cuda or t.dtype != torch.float32 or tuple(t.shape) != (S, D // 2) or not t.is_contiguous()
+                or t.device != device):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor [S, D/2] = [{S}, {D // 2}]")
+
+
+def gqa_attn_fwd_rope_workspace_size(B: int, Hkv: int, S: int, D: int) -> int:
+    """Bytes of device workspace gqa_attn_fwd_rope needs (the rotated keys; 0 for unsupported sizes)."""
+    return int(_lib.load().gqa_attn_fwd_rope_workspace_size(B, Hkv, S, D))
+
+
+def gqa_attn_bwd_rope_workspace_size(B: int, Hq: int, Hkv: int, S: int, D: int) -> int:
+    """Bytes of device workspace gqa_attn_bwd_rope needs (0 for unsupported sizes)."""
+    return int(_lib.load().gqa_attn_bwd_rope_workspace_size(B, Hq, Hkv, S, D))
+
+
+def gqa_attn_fwd_rope(q, k, v, rope_cos, rope_sin, causal: bool = True, scale: float | None = None, o=None,
+                      lse=None, workspace=None, stream=None):
+    """Forward over rotary-embedded q and k (rotate-half pairing, f32 tables [S, D/2]):
+    returns (o, lse) like gqa_attn_fwd."""
+    B, Hq, Hkv, S, D = _dims(q, k, v)
+    _check_tables(rope_cos, rope_sin, S, D, q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, S), device=q.device, dtype=torch.float32) if lse is None else lse
+    need = gqa_attn_fwd_rope_workspace_size(B, Hkv, S, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = _lib.load().gqa_attn_fwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), rope_cos.data_ptr(),
+                                       rope_sin.data_ptr(), o.data_ptr(), lse.data_ptr(), workspace.data_ptr(), nbytes,
+                                       B, Hq, Hkv, S, D, int(bool(causal)), float(scale), _stream_handle(stream))
+    _check(rc, "gqa_attn_fwd_rope")
+    return o, lse
+
+
+def gqa_attn_bwd_rope(q, k, v, o, dO, lse, rope_cos, rope_sin, causal: bool = True, scale: float | None = None,
+                      dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of the rotary-embedded forward: (dq, dk, dv) with respect to the unrotated q, k."""
+    B, Hq, Hkv, S, D = _dims(q, k, v)
+    _check_tables(rope_cos, rope_sin, S, D, q.device)
+    for name, t in (("o", o), ("dO", dO)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor shaped like q")
+    if lse.shape != (B, Hq, S) or lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, Hq, S]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = gqa_attn_bwd_rope_workspace_size(B, Hq, Hkv, S, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = _lib.load().gqa_attn_bwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
+                                       lse.data_ptr(), rope_cos.data_ptr(), rope_sin.data_ptr(), dq.data_ptr(),
+                                       dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), nbytes, B, Hq, Hkv, S, D,
+                                       int(bool(causal)), float(scale), _stream_handle(stream))
+    _check(rc, "gqa_attn_bwd_rope")
     return dq, dk, dv

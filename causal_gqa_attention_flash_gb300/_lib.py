@@ -16,6 +16,10 @@ SIGNATURES = {
     "gqa_attn_bwd_workspace_size": (_sz, [_c_int] * 5),
     "gqa_attn_bwd_varlen_workspace_size": (_sz, [_c_int] * 4),
     "gqa_attn_bwd_deterministic": (_c_int, [_vp] * 10 + [_sz] + [_c_int] * 6 + [_c_float, _vp]),
+    "gqa_attn_fwd_rope_workspace_size": (_sz, [_c_int] * 4),
+    "gqa_attn_fwd_rope": (_c_int, [_vp] * 8 + [_sz] + [_c_int] * 6 + [_c_float, _vp]),
+    "gqa_attn_bwd_rope_workspace_size": (_sz, [_c_int] * 5),
+    "gqa_attn_bwd_rope": (_c_int, [_vp] * 12 + [_sz] + [_c_int] * 6 + [_c_float, _vp]),
     "gqa_attn_bwd_varlen": (_c_int, [_vp] * 10 + [_c_int] * 2 + [_vp, _sz] + [_c_int] * 5 + [_c_float, _vp]),
     "gqa_attn_bwd": (_c_int, [_vp] * 10 + [_sz] + [_c_int] * 6 + [_c_float, _vp]),
     "gqa_attn_get_error": (_c_int, [_vp]),

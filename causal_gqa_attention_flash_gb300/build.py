@@ -19,7 +19,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgqa_attn.so")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_dq.cu", "decode.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_dq.cu", "decode.cu", "noalloc.cu", "rope.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
           "-Xptxas", "-warn-spills", "-I", os.path.join(os.path.dirname(HERE), "include")]

@@ -138,8 +138,14 @@ using namespace gqa;
 
 extern "C" {
 
-int gqa_attn_fwd_cached(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                        int Sq, int Sk, int D, int causal, float scale, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Dense forward, Sq <= Sk; with rotary tables (Sq = Sk) Q is rotated on load and k must
+// already hold the rotated keys.
+int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk,
+              int D, int causal, float scale, const float* rope_cos, const float* rope_sin, void* stream) {
   if (!q || !k || !v || !o || !lse) return GQA_ERR_INVALID_ARG;
   if (Sq < 1 || Sq > Sk) return GQA_ERR_INVALID_ARG;
   int rc = check_common(B, Hq, Hkv, Sk, D, scale);
@@ -164,6 +170,8 @@ int gqa_attn_fwd_cached(const void* q, const void* k, const void* v, void* o, fl
   a.cu_q = nullptr;
   a.cu_k = nullptr;
   a.max_seqlen_q = 0;
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
@@ -177,9 +185,39 @@ int gqa_attn_fwd_cached(const void* q, const void* k, const void* v, void* o, fl
   return GQA_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int gqa_attn_fwd_cached(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Sq, int Sk, int D, int causal, float scale, void* stream) {
+  return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, nullptr, nullptr, stream);
+}
+
 int gqa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
                  int D, int causal, float scale, void* stream) {
-  return gqa_attn_fwd_cached(q, k, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, stream);
+  return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, nullptr, nullptr, stream);
+}
+
+size_t gqa_attn_fwd_rope_workspace_size(int B, int Hkv, int S, int D) {
+  if (check_common(B, Hkv, Hkv, S, D, 1.0f) != GQA_OK) return 0;
+  return align256((size_t)B * Hkv * S * D * 2);
+}
+
+int gqa_attn_fwd_rope(const void* q, const void* k, const void* v, const float* rope_cos, const float* rope_sin,
+                      void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S,
+                      int D, int causal, float scale, void* stream) {
+  if (!k || !rope_cos || !rope_sin || !workspace) return GQA_ERR_INVALID_ARG;
+  int rc = check_common(B, Hq, Hkv, S, D, scale);
+  if (rc != GQA_OK) return rc;
+  if (!aligned(k, 16) || !aligned(rope_cos, 16) || !aligned(rope_sin, 16) || !aligned(workspace, 256))
+    return GQA_ERR_INVALID_ARG;
+  if (workspace_bytes < gqa_attn_fwd_rope_workspace_size(B, Hkv, S, D)) return GQA_ERR_WORKSPACE_TOO_SMALL;
+  // The keys are re-read by every query tile of their group: rotate them once, here.
+  cudaError_t e = launch_rope_rotate(k, workspace, rope_cos, rope_sin, (long long)B * Hkv * S, S, D,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return fwd_dense(q, workspace, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, rope_cos, rope_sin, stream);
 }
 
 int gqa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
@@ -211,6 +249,8 @@ int gqa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
   a.cu_q = cu_seqlens_q;
   a.cu_k = cu_seqlens_k;
   a.max_seqlen_q = max_seqlen_q;
+  a.rope_cos = nullptr;
+  a.rope_sin = nullptr;
   a.B = nseq;
   a.Hq = Hq;
   a.Hkv = Hkv;
@@ -235,7 +275,8 @@ namespace {
 
 int bwd_dense(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
               void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S, int D,
-              int causal, float scale, int deterministic, void* stream) {
+              int causal, float scale, int deterministic, const float* rope_cos, const float* rope_sin,
+              void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace) return GQA_ERR_INVALID_ARG;
   int rc = check_common(B, Hq, Hkv, S, D, scale);
   if (rc != GQA_OK) return rc;
@@ -275,6 +316,8 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
   a.map_k64 = &mk64;
   a.map_v64 = &mv64;
   a.deterministic = deterministic;
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
   a.o = o;
   a.dO = dO;
   a.lse = lse;
@@ -307,7 +350,7 @@ int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S,
                  int D, int causal, float scale, void* stream) {
   return bwd_dense(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, S, D, causal, scale, 0,
-                   stream);
+                   nullptr, nullptr, stream);
 }
 
 int gqa_attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
@@ -315,7 +358,33 @@ int gqa_attn_bwd_deterministic(const void* q, const void* k, const void* v, cons
                                size_t workspace_bytes, int B, int Hq, int Hkv, int S, int D, int causal, float scale,
                                void* stream) {
   return bwd_dense(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, S, D, causal, scale, 1,
-                   stream);
+                   nullptr, nullptr, stream);
+}
+
+size_t gqa_attn_bwd_rope_workspace_size(int B, int Hq, int Hkv, int S, int D) {
+  if (check_common(B, Hq, Hkv, S, D, 1.0f) != GQA_OK) return 0;
+  return bwd_workspace_layout(B, Hq, S, D).total + align256((size_t)B * Hq * S * D * 2);
+}
+
+int gqa_attn_bwd_rope(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      const float* rope_cos, const float* rope_sin, void* dq, void* dk, void* dv, void* workspace,
+                      size_t workspace_bytes, int B, int Hq, int Hkv, int S, int D, int causal, float scale,
+                      void* stream) {
+  if (!q || !rope_cos || !rope_sin || !workspace) return GQA_ERR_INVALID_ARG;
+  int rc = check_common(B, Hq, Hkv, S, D, scale);
+  if (rc != GQA_OK) return rc;
+  if (!aligned(q, 16) || !aligned(rope_cos, 16) || !aligned(rope_sin, 16) || !aligned(workspace, 256))
+    return GQA_ERR_INVALID_ARG;
+  if (workspace_bytes < gqa_attn_bwd_rope_workspace_size(B, Hq, Hkv, S, D)) return GQA_ERR_WORKSPACE_TOO_SMALL;
+  // The queries are re-read by every key tile that sees them: rotate them once, after the
+  // backward's own workspace sections.
+  const size_t bwd_bytes = bwd_workspace_layout(B, Hq, S, D).total;
+  void* q_rot = static_cast<uint8_t*>(workspace) + bwd_bytes;
+  cudaError_t e = launch_rope_rotate(q, q_rot, rope_cos, rope_sin, (long long)B * Hq * S, S, D,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return bwd_dense(q_rot, k, v, o, dO, lse, dq, dk, dv, workspace, bwd_bytes, B, Hq, Hkv, S, D, causal, scale, 0,
+                   rope_cos, rope_sin, stream);
 }
 
 size_t gqa_attn_bwd_varlen_workspace_size(int Hq, int Hkv, int T, int D) {
@@ -362,6 +431,8 @@ int gqa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void*
   a.map_k64 = nullptr;
   a.map_v64 = nullptr;
   a.deterministic = 0;
+  a.rope_cos = nullptr;
+  a.rope_sin = nullptr;
   a.o = o;
   a.dO = dO;
   a.lse = lse;

@@ -27,6 +27,7 @@
 // f32, then the dQ partial f32 [128, 128+D); [256,256+D) dV; [256+D,256+2D) dK.
 #include "common.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace gqa {
 namespace {
@@ -133,6 +134,7 @@ struct BwdBars {
   uint64_t qdo_full[ST];
   uint64_t qdo_empty[ST];
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free, stage_full, dkv_done, drain;
+  uint64_t k_ready;  // rotary embedding: the key tile rotated in shared memory
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -152,6 +154,8 @@ struct BwdKParams {
   int Hq, Hkv, S, S_pad, causal, max_seqlen;
   float scale, scale_log2;
   int* status;
+  const float* rope_cos;  // rotary tables [S, D/2] (nullptr: none): K is rotated in shared memory,
+  const float* rope_sin;  // the queries arrive rotated, dK is turned back in the epilogue
 };
 
 // One CTA per (batch, KV head, 128-key tile jt), 352 threads:
@@ -172,7 +176,11 @@ struct BwdKParams {
 //   back to the producer; the reduce streams out while the next step runs.
 // kDq = false: the deterministic backward's dK/dV kernel. It skips the dQ partial (a
 // query-major kernel computes dQ); the Q/dO stage is released once dK and dV have read it.
-template <int D, bool kDq>
+// kRope: the key tile is turned by the rotary embedding in shared memory (the queries arrive
+// rotated) and dK is turned back in the epilogue. kPacked: a packed batch of variable-length
+// sequences (bounds read per CTA, query columns past the sequence masked explicitly, D / LSE2
+// rows copied from an aligned start).
+template <int D, bool kDq, bool kRope, bool kPacked>
 __global__ void __launch_bounds__(352, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
@@ -197,7 +205,7 @@ __global__ void __launch_bounds__(352, 1)
   // L rows in this CTA's sequence, starting at row0 of the tensor maps; the KV head's map
   // coordinate, the first query head's, and the row stride of the D / LSE2 arrays.
   int L, row0, kv_coord, bhq0;
-  if (p.cu == nullptr) {
+  if (!kPacked) {
     L = p.S;
     row0 = 0;
     kv_coord = (int)blockIdx.x;
@@ -220,7 +228,7 @@ __global__ void __launch_bounds__(352, 1)
   const int n_steps = G * n_i;
   // D / LSE2 rows of query tile i of query head bhq0 + hl: copied from the 16-byte aligned row
   // below (the copy is 4 rows wider when a packed sequence starts off a multiple of 4 rows).
-  const int n_rowfl = p.cu ? kTile + 4 : kTile;
+  constexpr int n_rowfl = kPacked ? kTile + 4 : kTile;
   auto rows_at = [&](int hl, int i) { return (size_t)(bhq0 + hl) * p.S_pad + (size_t)row0 + (size_t)i * kTile; };
   const WaitGuard wg{&bars->abort_flag, p.status, kWaitLimitNs};
 
@@ -239,6 +247,7 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(&bars->stage_full, 8);
     mbar_init(&bars->dkv_done, 1);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->k_ready, 8);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -320,6 +329,7 @@ __global__ void __launch_bounds__(352, 1)
       // column half h = kk / 4 keeps its packed P^T in [64h, 64h+32) and dS^T in [64h+32, 64h+64).
       auto p_col = [](int kk) { return (uint32_t)(kk >> 2) * 64u + (uint32_t)(kk & 3) * 8u; };
       bool ok = mbar_wait(&bars->kv_full, 0, wg) && mbar_wait(&bars->qdo_full[0], 0, wg);
+      if (kRope && ok) ok = mbar_wait(&bars->k_ready, 0, wg);  // keys rotated by the element-wise warps
       if (ok) {
         tc_fence_after();
         issue_kmajor(C::kSPCol, dk_k, stage_desc(dq_k0, 0));
@@ -404,16 +414,28 @@ __global__ void __launch_bounds__(352, 1)
     const bool kv_valid = kv_row < L;
     uint8_t* sds_half = smem + C::kDSOff + hf * kBoxBytes;  // dS columns [64hf, 64hf+64)
     bool ok = true;
+    if (kRope) {
+      // Rotary embedding: thread (row, hf) turns half of its key row's pairs in shared memory.
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_full, 0, wg));
+      if (ok && kv_valid) {
+        const int pos = row0 + kv_row;  // position within the (dense) sequence
+        rope_rotate_row_smem<D>(smem + C::kKOff, row, p.rope_cos + (size_t)pos * (D / 2),
+                                p.rope_sin + (size_t)pos * (D / 2), 1.f, hf * (D / 32), (hf + 1) * (D / 32));
+      }
+      fence_proxy_async_smem();
+      mbar_arrive_warp(&bars->k_ready);
+    }
     for (int t = 0; t < n_steps; ++t) {
       const int st = t % ST;
       const int hl = t / n_i;
       const int i = i_start + (t - hl * n_i);
-      const int roff = (int)(rows_at(hl, i) & 3);  // the rows' offset within their widened copy
+      const int roff = kPacked ? (int)(rows_at(hl, i) & 3) : 0;  // the rows' offset within their widened copy
       const float* slse = reinterpret_cast<const float*>(smem + C::kRowOff) + st * 2 * C::kRowFl + roff + hf * 64;
       const float* sdv = slse + C::kRowFl;
       // visible iff key (jt*128 + row) <= query (i*128 + col): on the diagonal tile, col >= row
       const int first_visible = (p.causal && i == jt) ? row : 0;
-      const int q_limit = L - i * kTile;  // query columns at or past it lie beyond the sequence
+      // Packed: query columns at or past q_limit lie beyond the sequence (dense: LSE2 = +inf there).
+      const int q_limit = kPacked ? L - i * kTile : kTile;
 
       // ---- P^T = exp2(S^T c - LSE2) for the 64 query columns of this half
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, t & 1, wg));
@@ -428,7 +450,7 @@ __global__ void __launch_bounds__(352, 1)
         tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         uint32_t pk[32];
         // causal diagonal, keys past the sequence, or queries past it
-        const bool masked = first_visible > hf * 64 || !kv_valid || q_limit < hf * 64 + 64;
+        const bool masked = first_visible > hf * 64 || !kv_valid || (kPacked && q_limit < hf * 64 + 64);
         if (masked) {
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
@@ -520,6 +542,47 @@ __global__ void __launch_bounds__(352, 1)
       if (!ok) break;
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->dkv_done, 0, wg));
+    if (kRope && ok) {
+      // dK of the unrotated keys: thread (row, hf) takes pairs [hf D/4, hf D/4 + D/4), i.e. its
+      // columns c and c + D/2, and turns them back by the transposed rotation.
+      tc_fence_after();
+      constexpr int kQ = D / 4;
+      const int i0 = hf * kQ;
+      uint32_t lo[kQ], hi[kQ];
+      if constexpr (D == 128) {
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kDKCol + i0, lo);
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kDKCol + D / 2 + i0, hi);
+        tmem_wait_ld_x32(lo);
+        tmem_wait_ld_x32(hi);
+      } else {
+        tmem_ld_32x32b_x16(tbase + lane_off + C::kDKCol + i0, lo);
+        tmem_ld_32x32b_x16(tbase + lane_off + C::kDKCol + D / 2 + i0, hi);
+        tmem_wait_ld_x16(lo);
+        tmem_wait_ld_x16(hi);
+      }
+      if (kv_valid) {
+        const int pos = row0 + kv_row;
+        const float* cs = p.rope_cos + (size_t)pos * (D / 2) + i0;
+        const float* sn = p.rope_sin + (size_t)pos * (D / 2) + i0;
+        uint16_t* dst = p.dk + ((size_t)kv_coord * p.S + row0 + kv_row) * D;
+        const float sc = p.scale;
+#pragma unroll
+        for (int x = 0; x < kQ / 8; ++x) {
+          uint32_t wl[4], wh[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int i = 8 * x + 2 * w;
+            const float a0 = __uint_as_float(lo[i]) * sc, a1 = __uint_as_float(lo[i + 1]) * sc;
+            const float b0 = __uint_as_float(hi[i]) * sc, b1 = __uint_as_float(hi[i + 1]) * sc;
+            const float c0 = __ldg(cs + i), c1 = __ldg(cs + i + 1), s0 = __ldg(sn + i), s1 = __ldg(sn + i + 1);
+            wl[w] = pack_bf16(a0 * c0 + b0 * s0, a1 * c1 + b1 * s1);
+            wh[w] = pack_bf16(b0 * c0 - a0 * s0, b1 * c1 - a1 * s1);
+          }
+          *reinterpret_cast<uint4*>(dst + i0 + 8 * x) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+          *reinterpret_cast<uint4*>(dst + D / 2 + i0 + 8 * x) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        }
+      }
+    }
     if (ok) {
       tc_fence_after();
       const size_t orow = ((size_t)kv_coord * p.S + row0 + kv_row) * D;
@@ -541,10 +604,12 @@ __global__ void __launch_bounds__(352, 1)
                                  pack_bf16(__uint_as_float(dv[8 * x + 4]), __uint_as_float(dv[8 * x + 5])),
                                  pack_bf16(__uint_as_float(dv[8 * x + 6]), __uint_as_float(dv[8 * x + 7])));
             const float s = p.scale;
-            dstk[x] = make_uint4(pack_bf16(__uint_as_float(dk[8 * x + 0]) * s, __uint_as_float(dk[8 * x + 1]) * s),
-                                 pack_bf16(__uint_as_float(dk[8 * x + 2]) * s, __uint_as_float(dk[8 * x + 3]) * s),
-                                 pack_bf16(__uint_as_float(dk[8 * x + 4]) * s, __uint_as_float(dk[8 * x + 5]) * s),
-                                 pack_bf16(__uint_as_float(dk[8 * x + 6]) * s, __uint_as_float(dk[8 * x + 7]) * s));
+            if (!kRope) {  // with the rotary embedding dK was stored, turned back, above
+              dstk[x] = make_uint4(pack_bf16(__uint_as_float(dk[8 * x + 0]) * s, __uint_as_float(dk[8 * x + 1]) * s),
+                                   pack_bf16(__uint_as_float(dk[8 * x + 2]) * s, __uint_as_float(dk[8 * x + 3]) * s),
+                                   pack_bf16(__uint_as_float(dk[8 * x + 4]) * s, __uint_as_float(dk[8 * x + 5]) * s),
+                                   pack_bf16(__uint_as_float(dk[8 * x + 6]) * s, __uint_as_float(dk[8 * x + 7]) * s));
+            }
           }
         }
       }
@@ -608,10 +673,14 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     p.S_pad = S_pad;
     p.causal = a.causal;
     p.max_seqlen = a.max_seqlen;
+    p.rope_cos = a.rope_cos;
+    p.rope_sin = a.rope_sin;
     p.scale = a.scale;
     p.scale_log2 = a.scale_log2;
     p.status = a.status;
-    auto kern = det ? bwd_main_kernel<D, false> : bwd_main_kernel<D, true>;
+    auto kern = packed ? bwd_main_kernel<D, true, false, true>
+                : det ? bwd_main_kernel<D, false, false, false>
+                      : (a.rope_cos ? bwd_main_kernel<D, true, true, false> : bwd_main_kernel<D, true, false, false>);
     const KernelKind kind = det ? kKernelBwdDkdv : kKernelBwdMain;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -623,6 +692,9 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   if (det) return launch_bwd_dq(a, stream);
+  if (a.rope_cos)  // dQ of the unrotated queries
+    return launch_rope_convert(a.dq_acc, a.dq, a.rope_cos, a.rope_sin, (long long)a.B * a.Hq * a.S, a.S, D, a.scale,
+                               stream);
   {
     const long long n8 = acc_elems / 8;
     const int threads = 256;

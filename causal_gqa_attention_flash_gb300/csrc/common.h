@@ -30,6 +30,8 @@ struct FwdArgs {
   const int* cu_q;           // packed batch: device int32 [B + 1] query bounds; nullptr = dense
   const int* cu_k;           // packed batch: key bounds
   int max_seqlen_q;          // packed batch: bound on every sequence's query count
+  const float* rope_cos;     // rotary tables f32 [S, D/2] (nullptr: no rotation); Q is rotated
+  const float* rope_sin;     // in shared memory, map_k must already hold rotated keys
   // Dense: Sq <= Sk; query r at absolute position Sk - Sq + r. Packed: B sequences, Sq / Sk the
   // total query / key rows, maps [Hq, Sq, D] and [Hkv, Sk, D].
   int B, Hq, Hkv, Sq, Sk, D, causal;
@@ -58,6 +60,8 @@ struct BwdArgs {
   const int* cu;               // packed batch: device int32 [B + 1] sequence bounds; nullptr = dense
   int max_seqlen;              // packed batch: bound on every sequence's length
   int deterministic;           // 1: dQ by the query-major kernel (dense batches only)
+  const float* rope_cos;       // rotary tables f32 [S, D/2] (nullptr: none): map_q holds rotated
+  const float* rope_sin;       // queries, K is rotated in shared memory, dK and dQ are turned back
   // Packed batch: B sequences, S = total rows, tensors [H, S, D], dvec / lse2 [Hq*S + kRowPad]
   // with no per-head padding.
   int B, Hq, Hkv, S, D, causal;
@@ -122,7 +126,8 @@ enum KernelKind {
   kKernelDecodeCombine = 5,
   kKernelBwdDkdv = 6,
   kKernelBwdDq = 7,
-  kKernelCount = 8
+  kKernelRope = 8,
+  kKernelCount = 9
 };
 void trace_begin(int kind, cudaStream_t s);
 void trace_end(int kind, cudaStream_t s);
@@ -134,6 +139,10 @@ int record_cuda_error(cudaError_t e);
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_rope_rotate(const void* x, void* y, const float* cs, const float* sn, long long rows, int S, int D,
+                               cudaStream_t stream);
+cudaError_t launch_rope_convert(const float* acc, void* dq, const float* cs, const float* sn, long long rows, int S,
+                                int D, float scale, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

@@ -37,6 +37,7 @@
 // tile of a sequence storing its rows one by one.
 #include "common.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace gqa {
 namespace {
@@ -72,6 +73,7 @@ struct FwdBars {
   uint64_t o_done[2];
   uint64_t drain;
   uint64_t wg_bar[2];  // one per softmax warpgroup
+  uint64_t q_ready[2]; // rotary embedding: tile X's queries rotated in shared memory
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -87,6 +89,8 @@ struct FwdKParams {
   const int* cu_k;
   int Tq, Tk;          // packed batches: total query and key rows
   int max_seqlen_q;    // packed batches: bound on any sequence's query rows
+  const float* rope_cos;  // rotary tables [S, D/2] (nullptr: none); dense batches only
+  const float* rope_sin;
   // Dense batch: Sq query rows against Sk >= Sq keys; query row r sits at absolute position
   // koff + r, koff = Sk - Sq (0 for self-attention), and (causal) sees keys j <= koff + r.
   int Hq, Hkv, Sq, Sk, koff, causal, n_ktiles;
@@ -203,7 +207,8 @@ __device__ __forceinline__ int kv_tiles_of(int qt, const FwdGeom& g, int causal)
   return (g.koff + last_row) / kTile + 1;
 }
 
-template <int D>
+// kRope: queries are turned by the rotary embedding as they land in shared memory.
+template <int D, bool kRope>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -247,6 +252,8 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->wg_bar[0], 4);
     mbar_init(&bars->wg_bar[1], 4);
+    mbar_init(&bars->q_ready[0], 4);
+    mbar_init(&bars->q_ready[1], 4);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -346,6 +353,9 @@ __global__ void __launch_bounds__(384, 1)
       // K_j is released once the last S MMA reading it completes, V_j once both P V MMAs do:
       // the K ring refills a full key tile earlier than a shared K/V stage would.
       bool ok = mbar_wait(&bars->q_full, 0, wg) && mbar_wait(&bars->k_full[0], 0, wg);
+      if (kRope && ok) {  // the softmax warps rotate their tile's queries first
+        ok = (nA == 0 || mbar_wait(&bars->q_ready[0], 0, wg)) && (nB == 0 || mbar_wait(&bars->q_ready[1], 0, wg));
+      }
       if (ok) {
         tc_fence_after();
         if (nA > 0) issue_s(0, 0);
@@ -398,6 +408,17 @@ __global__ void __launch_bounds__(384, 1)
     const float c = p.scale_log2;
     float m_ref = 0.f, l = 0.f;
     bool ok = true;
+    if (kRope && n_x > 0) {
+      // Rotary embedding: each thread turns its own query row of tile X in shared memory
+      // (rows past S hold zeros and have no table row).
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, wg));
+      const int qpos = qt * kTile + row;
+      if (ok && qpos < g.Sq)
+        rope_rotate_row_smem<D>(smem + C::kQOff + x * C::kTileBytes, row, p.rope_cos + (size_t)qpos * (D / 2),
+                                p.rope_sin + (size_t)qpos * (D / 2), 1.f);
+      fence_proxy_async_smem();
+      mbar_arrive_warp(&bars->q_ready[x]);
+    }
     for (int j = 0; j < n_x; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[x], j & 1, wg));
       if (!ok) break;
@@ -520,6 +541,8 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.Tq = a.Sq;
   p.Tk = a.Sk;
   p.max_seqlen_q = a.max_seqlen_q;
+  p.rope_cos = a.rope_cos;
+  p.rope_sin = a.rope_sin;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.Sq = a.Sq;
@@ -529,18 +552,19 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.n_ktiles = ceil_div(a.Sk, kTile);
   p.scale_log2 = a.scale_log2;
   p.status = a.status;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  auto kern = a.rope_cos ? fwd_kernel<D, true> : fwd_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The setmaxnreg split must fit the registers the block is launched with, or the
   // increase would wait forever: refuse to launch otherwise.
   cudaFuncAttributes fa;
-  if ((e = cudaFuncGetAttributes(&fa, fwd_kernel<D>)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
   if (fa.numRegs * C::kThreads < 2 * 128 * C::kHighRegs + 128 * C::kLowRegs) return cudaErrorInvalidConfiguration;
   // Packed batch: one row of CTAs per (sequence, head), enough pairs for the longest sequence.
   const int rows = a.cu_q ? a.max_seqlen_q : a.Sq;
   dim3 grid((unsigned)(a.B * a.Hq), (unsigned)ceil_div(rows, 2 * kTile));
   trace_begin(kKernelFwd, stream);
-  fwd_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_o, p);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_o, p);
   e = cudaGetLastError();
   trace_end(kKernelFwd, stream);
   return e;

@@ -183,6 +183,38 @@ int gqa_attn_bwd_deterministic(const void* q, const void* k, const void* v, cons
                                void* stream);
 
 /*
+ * Rotary position embedding fused with the attention (rotate-half pairing):
+ * for position p and 0 <= i < D/2 the plane (x[i], x[i + D/2]) of every query
+ * and key row turns by the angle with cosine rope_cos[p, i] and sine
+ * rope_sin[p, i]; V is not rotated. The tables are f32 [S, D/2], device,
+ * 16-byte aligned, owned by the caller (any base, scaling or offset).
+ * gqa_attn_fwd_rope: O, LSE of attention over the rotated q and k (q, k, v, o,
+ *   lse as gqa_attn_fwd). Queries are rotated as they land in shared memory;
+ *   keys, which every query tile of their group re-reads, are rotated once
+ *   into the workspace (>= gqa_attn_fwd_rope_workspace_size bytes, 256-byte
+ *   aligned, caller-owned).
+ * gqa_attn_bwd_rope: dq, dk (with respect to the UNROTATED q, k) and dv for the
+ *   O, LSE of gqa_attn_fwd_rope. Queries are rotated once into the workspace
+ *   (>= gqa_attn_bwd_rope_workspace_size bytes), keys as they land in shared
+ *   memory; dK is turned back by the transposed rotation in the main kernel's
+ *   epilogue and dQ in its f32-to-bf16 conversion.
+ * Errors as gqa_attn_fwd / gqa_attn_bwd; GQA_ERR_INVALID_ARG for null or
+ * misaligned tables; GQA_ERR_WORKSPACE_TOO_SMALL. Dense self-attention only.
+ * Passage: tang page, "A transformer" (RMSNorm, RoPE, GQA attention, SwiGLU,
+ * forward and backward); RustingBrain docs, "What is in the box" (rotary
+ * positions).
+ */
+size_t gqa_attn_fwd_rope_workspace_size(int B, int Hkv, int S, int D);
+int gqa_attn_fwd_rope(const void* q, const void* k, const void* v, const float* rope_cos, const float* rope_sin,
+                      void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S,
+                      int D, int causal, float scale, void* stream);
+size_t gqa_attn_bwd_rope_workspace_size(int B, int Hq, int Hkv, int S, int D);
+int gqa_attn_bwd_rope(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      const float* rope_cos, const float* rope_sin, void* dq, void* dk, void* dv, void* workspace,
+                      size_t workspace_bytes, int B, int Hq, int Hkv, int S, int D, int causal, float scale,
+                      void* stream);
+
+/*
  * Size in bytes of the device workspace gqa_attn_bwd_varlen needs for Hq query
  * heads over T packed rows (256-byte aligned sections: D and LSE*log2(e) rows,
  * f32 [Hq*T + 256] each, then the f32 dQ accumulator [Hq, T, D]).
@@ -257,7 +289,8 @@ int gqa_attn_selftest_wait_timeout(int limit_us, void* stream);
 #define GQA_KERNEL_DECODE_COMBINE 5
 #define GQA_KERNEL_BWD_DKDV 6 /* the deterministic backward's dK/dV kernel */
 #define GQA_KERNEL_BWD_DQ 7   /* the deterministic backward's query-major dQ kernel */
-#define GQA_KERNEL_COUNT 8
+#define GQA_KERNEL_ROPE 8     /* the rotary embedding's rotation pass */
+#define GQA_KERNEL_COUNT 9
 int gqa_attn_trace_arm(void);
 int gqa_attn_trace_collect(int* launches, double* total_ms);
 
