@@ -24,7 +24,8 @@
 namespace gqa {
 namespace {
 
-constexpr int kDecWarps = 4;              // compute warps; warp 4 is the TMA producer
+constexpr int kDecWarps = 8;              // compute warps (two groups of 4); warp 8 is the TMA producer
+constexpr int kDecGroupWarps = 4;         // warps of a group: one 128-key tile, one key per lane
 constexpr int kDecThreads = 32 * (kDecWarps + 1);
 
 template <int D>
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int s = 0; s < ST; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], kDecWarps);
+      mbar_init(&bars->kv_empty[s], kDecGroupWarps);  // the group that consumed the tile
     }
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -149,8 +150,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ compute warps
-    const int kk = warp * 32 + lane;  // this lane's key within a 128-key tile (scores)
-    for (int t = 0; t < n_tiles; ++t) {
+    // Two groups of 4 warps take alternate tiles (two tiles in flight); each warp keeps its own
+    // state, and all are merged below.
+    const int grp = warp / kDecGroupWarps;
+    const int wq = warp - grp * kDecGroupWarps;
+    const int kk = wq * 32 + lane;  // this lane's key within a 128-key tile (scores)
+    for (int t = grp; t < n_tiles; t += kDecWarps / kDecGroupWarps) {
       const int st = t % ST;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_full[st], (t / ST) & 1, wg))) break;
       const uint8_t* sK = smem + C::kKOff + st * C::kTileBytes;
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const int col0 = lane * C::kDC;
 #pragma unroll 4
       for (int j = 0; j < 32; ++j) {
-        const int vk = warp * 32 + j;
+        const int vk = wq * 32 + j;
         const uint8_t* vrow = sV + (col0 >> 6) * kBoxBytes + vk * 128;
         const int unit = (col0 & 63) >> 3;
         const uint8_t* vp = vrow + ((unit ^ (vk & 7)) << 4) + (col0 & 7) * 2;
