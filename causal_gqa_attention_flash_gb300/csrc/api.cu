@@ -476,14 +476,14 @@ int device_sms() {
 // tile's worth of per-CTA overhead), one decode CTA per SM, so that the last wave is not mostly
 // empty and CTAs are not too short.
 void decode_split_plan(int B, int Hkv, int Sk, int num_splits, int* splits, int* chunk) {
-  const int tiles = (Sk + kTile - 1) / kTile;
+  const int tiles = (Sk + kDecodeKeys - 1) / kDecodeKeys;
   int s = num_splits;
   if (s <= 0) {
     const long long units = (long long)B * Hkv;
-    const long long sms = device_sms();
+    const long long sms = (long long)device_sms() * kDecodeCtasPerSm;  // CTAs resident at once
     long long best = -1;
     s = 1;
-    for (int c = 1; c <= tiles && c <= 256; ++c) {
+    for (int c = 1; c <= tiles && c <= 512; ++c) {
       const long long per = (tiles + c - 1) / c;
       const long long waves = (units * c + sms - 1) / sms;
       const long long cost = waves * (per + 1) * 64 + c;  // small tie-break toward fewer chunks
@@ -496,7 +496,7 @@ void decode_split_plan(int B, int Hkv, int Sk, int num_splits, int* splits, int*
   if (s > tiles) s = tiles;
   if (s < 1) s = 1;
   const int tiles_per = (tiles + s - 1) / s;
-  *chunk = tiles_per * kTile;
+  *chunk = tiles_per * kDecodeKeys;
   *splits = (tiles + tiles_per - 1) / tiles_per;
 }
 
@@ -512,7 +512,7 @@ int check_decode(int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale) {
 }
 
 size_t decode_workspace(int B, int Hq, int Hkv, int Sq, int Sk, int D, int num_splits, size_t* ml_off) {
-  int splits = 1, chunk = kTile;
+  int splits = 1, chunk = kDecodeKeys;
   decode_split_plan(B, Hkv, Sk, num_splits, &splits, &chunk);
   const size_t rows = (size_t)B * Hkv * splits * decode_rows_padded((Hq / Hkv) * Sq);
   *ml_off = align256(rows * D * sizeof(float));
@@ -544,8 +544,12 @@ int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
   if (workspace_bytes < need) return GQA_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap mk, mv;
   cudaError_t e;
-  if ((e = encode_bf16(&mk, k_cache, D, Sk, B * Hkv)) != cudaSuccess) return fail_cuda(e);
-  if ((e = encode_bf16(&mv, v_cache, D, Sk, B * Hkv)) != cudaSuccess) return fail_cuda(e);
+  if ((e = encode_3d(&mk, k_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Sk, B * Hkv, kChunk,
+                     CU_TENSOR_MAP_SWIZZLE_128B, kDecodeKeys)) != cudaSuccess)
+    return fail_cuda(e);
+  if ((e = encode_3d(&mv, v_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Sk, B * Hkv, kChunk,
+                     CU_TENSOR_MAP_SWIZZLE_128B, kDecodeKeys)) != cudaSuccess)
+    return fail_cuda(e);
   int* status = nullptr;
   if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
   DecodeArgs a;

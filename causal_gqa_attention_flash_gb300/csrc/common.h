@@ -71,6 +71,9 @@ struct BwdArgs {
 
 // Query rows (G heads x Sq new queries) one decode CTA handles for a KV head.
 constexpr int kMaxDecodeRows = 16;
+// Decode streams the cache in tiles of 64 keys (64-row TMA boxes), two CTAs per SM.
+constexpr int kDecodeKeys = 64;
+constexpr int kDecodeCtasPerSm = 2;
 
 struct DecodeArgs {
   const CUtensorMap* map_k;  // [B*Hkv, Sk, D] bf16 cache

@@ -15,27 +15,29 @@
 //   decode_combine  one warp per query row: merges the partials of all chunks,
 //                   writes O (bf16) and LSE (f32).
 //
-// The work is bound by HBM (each cached key and value is read once), so the
-// arithmetic runs on the CUDA cores; the key/value tiles are staged by TMA in
-// the same 128B-swizzled 128-row boxes as the training kernels.
+// The work is bound by HBM (each cached key and value is read once). The key /
+// value tiles are staged by TMA in the same 128B-swizzled 128-row boxes as the
+// training kernels; the G Sq <= 16 query rows of a KV head are the M = 16 rows
+// of mma.sync m16n8k16 bf16 products (S = Q K^T, O += P V) with operands read
+// by ldmatrix: a 128-row tcgen05 tile would be at least 4x padding here, and
+// the tensor work is a small fraction of the time the cache takes to stream.
 #include "common.h"
 #include "ptx.cuh"
 
 namespace gqa {
 namespace {
 
-constexpr int kDecWarps = 8;              // compute warps (two groups of 4); warp 8 is the TMA producer
-constexpr int kDecGroupWarps = 4;         // warps of a group: one 128-key tile, one key per lane
+constexpr int kDecWarps = 4;                        // compute warps; warp 4 is the TMA producer
+constexpr int kDecWarpKeys = kDecodeKeys / kDecWarps;  // keys of a tile per compute warp (16)
 constexpr int kDecThreads = 32 * (kDecWarps + 1);
+constexpr int kDecBox = kDecodeKeys * 128;             // one 64-row box of 64 bf16 columns
 
 template <int D>
 struct DecCfg {
   static constexpr int kChunks = D / kChunk;
-  static constexpr int kTileBytes = kTile * D * 2;   // 128 keys
-  static constexpr int kStages = (D == 64) ? 6 : 3;  // ~192 KB of K/V in flight per CTA
-  static constexpr int kDC = D / 32;                 // head-dim columns per lane in P.V
-  static constexpr int kQOff = 0;                    // f32 [kMaxRows][D], pre-scaled by scale*log2(e)
-  static constexpr int kKOff = kMaxDecodeRows * D * 4;
+  static constexpr int kTileBytes = kDecodeKeys * D * 2;  // 64 keys
+  static constexpr int kStages = (D == 64) ? 6 : 3;  // ~96 KB of K/V per CTA, two CTAs per SM
+  static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   // warp states for the final combine, over the K/V ring (every tile has been consumed by then)
   static constexpr int kRedOff = kKOff;
@@ -76,11 +78,34 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// Four 8x8 b16 matrices from shared memory; lane l gives the row address of matrix l / 8.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// The same, each matrix transposed.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// d (m16n8, f32) += a (m16k16, bf16, row) * b (k16n8, bf16, col).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 template <int D, int R>
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                         const DecKParams p) {
   using C = DecCfg<D>;
@@ -99,157 +124,184 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int g = kvh - b * p.Hkv;
   const int key0 = split * p.chunk;
   const int key1 = min(p.Sk, key0 + p.chunk);
-  const int n_tiles = key1 > key0 ? (key1 - key0 + kTile - 1) / kTile : 0;
+  const int n_tiles = key1 > key0 ? (key1 - key0 + kDecodeKeys - 1) / kDecodeKeys : 0;
   const WaitGuard wg{&bars->abort_flag, p.status, kWaitLimitNs};
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], kDecGroupWarps);  // the group that consumed the tile
+      mbar_init(&bars->kv_empty[s], kDecWarps);  // every compute warp, once done with the tile
     }
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  // Query rows r = hl * Sq + i (hl: head within the group) as f32, pre-scaled by scale*log2(e).
-  float* sq = reinterpret_cast<float*>(smem + C::kQOff);
-  for (int e = tid; e < R * D; e += kDecThreads) {
-    const int r = e / D, d = e - r * D;
-    const int hl = r / p.Sq, i = r - hl * p.Sq;
-    float x = 0.f;  // rows padded past G * Sq stay zero (their partials are never read)
-    if (hl < G) x = __uint_as_float((uint32_t)p.q[(((size_t)b * p.Hq + g * G + hl) * p.Sq + i) * D + d] << 16);
-    sq[e] = x * p.scale_log2;
-  }
   __syncthreads();
 
-  // this warp's softmax state over its keys (compute warps only)
-  float m[R], l[R], acc[R][C::kDC];
+  // This warp's softmax state over its keys, in the m16n8 accumulator layout of mma.sync:
+  // thread (lane) holds query rows r0 = lane / 4 and r0 + 8 (of the 16 rows, padding past R),
+  // and, of every 8-column block, columns 2 (lane % 4) and 2 (lane % 4) + 1.
+  constexpr int kNB = D / 8;  // 8-column blocks of O
+  const int r0 = lane >> 2;
+  const int cq = (lane & 3) * 2;
+  float m[2] = {-INFINITY, -INFINITY};  // running max (log2 units) of rows r0, r0 + 8
+  float l[2] = {0.f, 0.f};              // this thread's share of the row sums
+  float acc[kNB][4];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    m[r] = -INFINITY;
-    l[r] = 0.f;
-#pragma unroll
-    for (int c = 0; c < C::kDC; ++c) acc[r][c] = 0.f;
-  }
+  for (int nb = 0; nb < kNB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
   if (warp == kDecWarps) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       for (int t = 0; t < n_tiles; ++t) {
         const int st = t % ST, use = t / ST;
         if (use > 0 && !mbar_wait(&bars->kv_empty[st], (use - 1) & 1, wg)) break;
-        const int y = key0 + t * kTile;
+        const int y = key0 + t * kDecodeKeys;
         mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kKOff + st * C::kTileBytes + c * kBoxBytes, &map_k, &bars->k_full[st], c * kChunk,
+          tma_load_3d(smem + C::kKOff + st * C::kTileBytes + c * kDecBox, &map_k, &bars->k_full[st], c * kChunk,
                       y, kvh);
         mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kVOff + st * C::kTileBytes + c * kBoxBytes, &map_v, &bars->v_full[st], c * kChunk,
+          tma_load_3d(smem + C::kVOff + st * C::kTileBytes + c * kDecBox, &map_v, &bars->v_full[st], c * kChunk,
                       y, kvh);
       }
     }
   } else {
     // ------------------------------------------------------------ compute warps
-    // Two groups of 4 warps take alternate tiles (two tiles in flight); each warp keeps its own
-    // state, and all are merged below.
-    const int grp = warp / kDecGroupWarps;
-    const int wq = warp - grp * kDecGroupWarps;
-    const int kk = wq * 32 + lane;  // this lane's key within a 128-key tile (scores)
-    for (int t = grp; t < n_tiles; t += kDecWarps / kDecGroupWarps) {
+    // Warp w takes keys [16 w, 16 w + 16) of every 64-key tile (two CTAs per SM keep the
+    // cache streaming while either starts or ends). S = Q K^T and O += P V run as m16n8k16 bf16
+    // MMAs (the G Sq <= 16 query rows of the KV head are the M = 16 rows), operands read from
+    // the 128B-swizzled tiles with ldmatrix.
+    constexpr int kWNB = kDecWarpKeys / 8;   // 8-key blocks of S per warp
+    constexpr int kWKS = kDecWarpKeys / 16;  // 16-key steps of P V per warp
+    const int wq = warp;
+    // Q as A fragments, one per 16 columns of D (unscaled bf16; the scores are scaled in f32).
+    uint32_t qa[D / 16][4];
+    {
+      auto qword = [&](int r, int col) -> uint32_t {  // bf16 pair (col, col + 1) of query row r
+        const int hl = r / p.Sq, i = r - hl * p.Sq;
+        if (r >= R || hl >= G) return 0u;  // padding rows: zero queries, partials never read
+        return *reinterpret_cast<const uint32_t*>(p.q + (((size_t)b * p.Hq + g * G + hl) * p.Sq + i) * D + col);
+      };
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        qa[ks][0] = qword(r0, 16 * ks + cq);
+        qa[ks][1] = qword(r0 + 8, 16 * ks + cq);
+        qa[ks][2] = qword(r0, 16 * ks + 8 + cq);
+        qa[ks][3] = qword(r0 + 8, 16 * ks + 8 + cq);
+      }
+    }
+    const float c = p.scale_log2;
+    const int causal_base = p.Sk - p.Sq;  // row r sees keys <= causal_base + r % Sq
+    const int vis0 = causal_base + (r0 % p.Sq), vis1 = causal_base + ((r0 + 8) % p.Sq);
+    for (int t = 0; t < n_tiles; ++t) {
       const int st = t % ST;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_full[st], (t / ST) & 1, wg))) break;
-      const uint8_t* sK = smem + C::kKOff + st * C::kTileBytes;
-      // ---- scores of key kk against every row
-      float s[R];
+      const uint32_t sK = smem_addr(smem + C::kKOff + st * C::kTileBytes);
+      const int kb = wq * kDecWarpKeys;  // this warp's first key in the tile
+      // ---- S (16 rows x 16 keys), blocks of 8 keys
+      float sc[kWNB][4];
 #pragma unroll
-      for (int r = 0; r < R; ++r) s[r] = 0.f;
-#pragma unroll 4
-      for (int c = 0; c < D / 8; ++c) {  // 16-byte units of the key row (8 bf16)
-        const uint4 w = *reinterpret_cast<const uint4*>(sK + (c >> 3) * kBoxBytes + kk * 128 +
-                                                         (((c & 7) ^ (kk & 7)) << 4));
-        const float kv8[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                              bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+      for (int nb = 0; nb < kWNB; ++nb) {
+        sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+        const int key = kb + 8 * nb + (lane & 7);  // this lane's row address for ldmatrix
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float4 qa = *reinterpret_cast<const float4*>(sq + r * D + c * 8);
-          const float4 qb = *reinterpret_cast<const float4*>(sq + r * D + c * 8 + 4);
-          s[r] = fmaf(qa.x, kv8[0], s[r]);
-          s[r] = fmaf(qa.y, kv8[1], s[r]);
-          s[r] = fmaf(qa.z, kv8[2], s[r]);
-          s[r] = fmaf(qa.w, kv8[3], s[r]);
-          s[r] = fmaf(qb.x, kv8[4], s[r]);
-          s[r] = fmaf(qb.y, kv8[5], s[r]);
-          s[r] = fmaf(qb.z, kv8[6], s[r]);
-          s[r] = fmaf(qb.w, kv8[7], s[r]);
+        for (int ks = 0; ks < D / 16; ks += 2) {
+          // four 8x8 matrices: d [16ks, +8), [16ks+8, +8), [16ks+16, +8), [16ks+24, +8) of 8 keys
+          const int d0 = 16 * ks + 8 * (lane >> 3);
+          const uint32_t addr = sK + (d0 >> 6) * kDecBox + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+          uint32_t kf[4];
+          ldmatrix_x4(addr, kf);
+          mma_bf16_16816(sc[nb], qa[ks], kf[0], kf[1]);
+          mma_bf16_16816(sc[nb], qa[ks + 1], kf[2], kf[3]);
         }
       }
-      // ---- mask: keys past the chunk / the cache, and (causal) past each row's position
-      const int key = key0 + t * kTile + kk;
+      // ---- mask (keys past the chunk / the cache; causal per row) and online softmax
+      const int tkey = key0 + t * kDecodeKeys + kb;
+      float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int i = r % p.Sq;
-        const bool vis = key < key1 && (!p.causal || key <= p.Sk - p.Sq + i);
-        if (!vis) s[r] = -INFINITY;
+      for (int nb = 0; nb < kWNB; ++nb) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = tkey + 8 * nb + cq + (e & 1);
+          const bool vis = key < key1 && (!p.causal || key <= ((e & 2) ? vis1 : vis0));
+          sc[nb][e] = vis ? sc[nb][e] * c : -INFINITY;
+          mt[e >> 1] = fmaxf(mt[e >> 1], sc[nb][e]);
+        }
       }
-      // ---- online-softmax update of this warp's state (log2 units)
-      float pr[R];
+      float alpha[2], ref[2];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float mt = warp_max(s[r]);
-        const float mn = fmaxf(m[r], mt);
-        const float ref = (mn == -INFINITY) ? 0.f : mn;  // no visible key yet: keep the state empty
-        const float alpha = ex2_approx(m[r] - ref);       // 0 when m was -inf
-        pr[r] = ex2_approx(s[r] - ref);
-        l[r] = l[r] * alpha + warp_sum(pr[r]);
-        m[r] = mn;
+      for (int h = 0; h < 2; ++h) {
+        mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], 1));
+        mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], 2));
+        const float mn = fmaxf(m[h], mt[h]);
+        ref[h] = (mn == -INFINITY) ? 0.f : mn;  // no visible key yet: keep the state empty
+        alpha[h] = ex2_approx(m[h] - ref[h]);   // 0 when m was -inf
+        m[h] = mn;
+        l[h] *= alpha[h];
+      }
 #pragma unroll
-        for (int c = 0; c < C::kDC; ++c) acc[r][c] *= alpha;
+      for (int nb = 0; nb < kNB; ++nb) {
+        acc[nb][0] *= alpha[0];
+        acc[nb][1] *= alpha[0];
+        acc[nb][2] *= alpha[1];
+        acc[nb][3] *= alpha[1];
+      }
+      // P (bf16) as the A fragments of the 16-key steps
+      uint32_t pa[kWKS][4];
+#pragma unroll
+      for (int nb = 0; nb < kWNB; ++nb) {
+        const float p0 = ex2_approx(sc[nb][0] - ref[0]), p1 = ex2_approx(sc[nb][1] - ref[0]);
+        const float p2 = ex2_approx(sc[nb][2] - ref[1]), p3 = ex2_approx(sc[nb][3] - ref[1]);
+        l[0] += p0 + p1;
+        l[1] += p2 + p3;
+        pa[nb >> 1][(nb & 1) * 2] = pack_bf16(p0, p1);
+        pa[nb >> 1][(nb & 1) * 2 + 1] = pack_bf16(p2, p3);
       }
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (t / ST) & 1, wg))) break;
-      const uint8_t* sV = smem + C::kVOff + st * C::kTileBytes;
-      // ---- acc += P V over this warp's 32 keys; lane owns columns [lane*kDC, lane*kDC + kDC)
-      const int col0 = lane * C::kDC;
-#pragma unroll 4
-      for (int j = 0; j < 32; ++j) {
-        const int vk = wq * 32 + j;
-        const uint8_t* vrow = sV + (col0 >> 6) * kBoxBytes + vk * 128;
-        const int unit = (col0 & 63) >> 3;
-        const uint8_t* vp = vrow + ((unit ^ (vk & 7)) << 4) + (col0 & 7) * 2;
-        float vv[C::kDC];
-        if constexpr (C::kDC == 4) {
-          const uint2 w = *reinterpret_cast<const uint2*>(vp);
-          vv[0] = bf16_lo(w.x);
-          vv[1] = bf16_hi(w.x);
-          vv[2] = bf16_lo(w.y);
-          vv[3] = bf16_hi(w.y);
-        } else {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
-          vv[0] = bf16_lo(w);
-          vv[1] = bf16_hi(w);
-        }
+      const uint32_t sV = smem_addr(smem + C::kVOff + st * C::kTileBytes);
+      // ---- O += P V: per 16 keys and pair of 8-column blocks, four transposed 8x8 matrices
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float pj = __shfl_sync(0xffffffffu, pr[r], j);
+      for (int kp = 0; kp < kWKS; ++kp) {
+        const int key = kb + 16 * kp + 8 * ((lane >> 3) & 1) + (lane & 7);
 #pragma unroll
-          for (int c = 0; c < C::kDC; ++c) acc[r][c] = fmaf(pj, vv[c], acc[r][c]);
+        for (int nb = 0; nb < kNB; nb += 2) {
+          const int d0 = 8 * (nb + (lane >> 4));
+          const uint32_t addr = sV + (d0 >> 6) * kDecBox + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+          uint32_t vf[4];
+          ldmatrix_x4_trans(addr, vf);
+          mma_bf16_16816(acc[nb], pa[kp], vf[0], vf[1]);
+          mma_bf16_16816(acc[nb + 1], pa[kp], vf[2], vf[3]);
         }
       }
       mbar_arrive_warp(&bars->kv_empty[st]);
+    }
+    // row sums: this thread's share over its columns, then over the 4 threads of the row
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
     }
   }
   // The combine buffer overlays the K/V ring: every warp must be done with its tiles first.
   __syncthreads();
   if (warp < kDecWarps) {
-    // ---- combine the warps' states (same monoid) and write this chunk's partial
+    // ---- this warp's state of each real row (r < R) into the combine buffer
     float* red = reinterpret_cast<float*>(smem + C::kRedOff);  // [warp][R][D + 2]
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      float* dst = red + (warp * R + r) * (D + 2);
+    for (int h = 0; h < 2; ++h) {
+      const int r = r0 + 8 * h;
+      if (r < R) {
+        float* dst = red + (warp * R + r) * (D + 2);
 #pragma unroll
-      for (int c = 0; c < C::kDC; ++c) dst[lane * C::kDC + c] = acc[r][c];
-      if (lane == 0) {
-        dst[D] = m[r];
-        dst[D + 1] = l[r];
+        for (int nb = 0; nb < kNB; ++nb) {
+          dst[8 * nb + cq] = acc[nb][2 * h];
+          dst[8 * nb + cq + 1] = acc[nb][2 * h + 1];
+        }
+        if ((lane & 3) == 0) {
+          dst[D] = m[h];
+          dst[D + 1] = l[h];
+        }
       }
     }
   }
