@@ -46,6 +46,29 @@ def flops(B, Hq, S, D):
     return fwd, 2.5 * fwd
 
 
+# ---- replicas over ranks (the path does not shard: every rank solves its own seeded problem)
+
+def replica_seed(seed, rank):
+    """Seed of rank `rank`'s replica of a workload: distinct inputs per rank, rank 0 = the workload's."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks_of(x, world, device):
+    """The largest of every rank's x (the job's step time is its slowest rank's)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(step_flops_per_rank, world, ms_per_step):
+    """Whole-job throughput: every rank's work over the slowest rank's step time."""
+    return world * step_flops_per_rank / (ms_per_step / 1e3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -459,14 +482,10 @@ def main():
             dist.barrier()
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks_of(x, world, "cuda")
 
     # Each rank: its own seeded replica of the workload (independent problems).
-    q_h, k_h, v_h, dO_h = make_inputs(w.B, w.Hq, w.Hkv, w.S, w.D, w.seed + 1000 * rank, do_std=w.do_std)
+    q_h, k_h, v_h, dO_h = make_inputs(w.B, w.Hq, w.Hkv, w.S, w.D, replica_seed(w.seed, rank), do_std=w.do_std)
     q_h, k_h, v_h, dO_h = (t.pin_memory() for t in (q_h, k_h, v_h, dO_h))
     q, k, v, dO = (t.cuda() for t in (q_h, k_h, v_h, dO_h))
     o = torch.empty_like(q)
@@ -588,7 +607,7 @@ def main():
 
     line = {
         "metric": METRIC,
-        "value": world * step_fl / (ms / 1e3) / 1e12,
+        "value": job_tflops(step_fl, world, ms),
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -602,7 +621,7 @@ def main():
         "config": config_of(w),
         "fwd_tflops": fwd_fl / (fwd_avg / 1e3) / 1e12,
         "bwd_tflops": bwd_fl / ((ms - fwd_avg) / 1e3) / 1e12,
-        "frac_of_peak": world * step_fl / (ms / 1e3) / 1e12 / (world * peak_tf),
+        "frac_of_peak": job_tflops(step_fl, world, ms) / (world * peak_tf),
         "kernels": kernels,
         "roofline": {"kernel": "bwd_main", "bound": "tensor", "achieved": achieved, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
@@ -610,7 +629,7 @@ def main():
                      "fwd_kernel": {"achieved": fwd_fl / (fwd_avg / 1e3) / 1e12,
                                     "frac": fwd_fl / (fwd_avg / 1e3) / 1e12 / peak_tf,
                                     "traffic": profiled_traffic("fwd", w.name)}},
-        "e2e": {"value": world * step_fl / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_tflops(step_fl, world, ms_e2e), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                 "copies": "every step: Q, K, V, dO up from pinned host memory, O, LSE, dQ, dK, dV back; "
                           "double-buffered on two copy streams, overlapping the neighbouring steps' compute"},
