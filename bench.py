@@ -77,7 +77,8 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = {"bwd_main": ("bwd.cu", "ptx.cuh", "common.h"), "fwd": ("fwd.cu", "ptx.cuh", "common.h")}
+KERNEL_SOURCES = {"bwd_main": ("bwd.cu", "ptx.cuh", "common.h"), "fwd": ("fwd.cu", "ptx.cuh", "common.h"),
+                  "decode_split": ("decode.cu", "ptx.cuh", "common.h")}
 
 
 def kernel_source_hash(kernel_name):
@@ -240,7 +241,8 @@ def decode_measurement(g, torch, peaks, peak_src, steps=20, warmup=3):
             "value": gbs, "unit": "GB/s", "us_per_call": ms * 1e3, "l2": "256 MB buffer written between calls",
             "kernels": {k_: {"launches": n_, "avg_ms": (t_ / n_ if n_ else None)} for k_, (n_, t_) in tr.items() if n_},
             "roofline": {"kernel": "decode_split", "bound": "hbm", "achieved": split_gbs, "peak": peak, "unit": "GB/s",
-                         "frac": split_gbs / peak, "traffic": None, "peak_source": f"{peak_src} HBM copy"}}
+                         "frac": split_gbs / peak, "traffic": profiled_traffic("decode_split", "decode16k"),
+                         "peak_source": f"{peak_src} HBM copy"}}
 
 
 PREFILL = dict(B=2, Hq=32, Hkv=8, Sq=512, Sk=16384, D=128, seed=6)
