@@ -15,18 +15,26 @@
 // KV-major kernel's dQ (S and dP are recomputed here; that kernel then skips
 // its dQ), 14 D flops per pair for the whole backward instead of 10 D.
 //
-// One CTA = one (batch, query head, 128-row query tile). Keys stream in 64-row
-// units u (keys 64u .. 64u+63), which alternate between two element-wise
-// warpgroups: while warpgroup u % 2 works on unit u, the tensor core runs
-// dQ(u-1) and S, dP of unit u+1. The K/V ring holds units, so a unit's copy is
-// issued two units before its first MMA.
+// One CTA = one (batch, query head, 128-row query tile). Keys stream in
+// 128-row units u (keys 128u .. 128u+127), so that every contraction is a
+// full-rate 128 x N x 16 MMA. Unit u is worked on by element-wise warpgroup
+// u % 2 in TMEM region u % 3 (128 columns): S(u) lands there; the warpgroup
+// turns it into P (bf16, kept in registers) and releases the region; dP(u)
+// is written over it; the warpgroup forms dS = P (dP - D), packs it to bf16
+// over the region's first 64 columns; dQ(u) reads it from there. A third
+// region lets S(u+2) be computed while unit u is still in flight.
+// The MMA thread does not follow a fixed order: it polls which of dP, dQ and S
+// of the oldest pending units is ready and issues the first that is (dP before
+// dQ before S), so that no warpgroup's wait is queued behind an MMA that could
+// not start.
 // Warp roles (320 threads):
 //   warps 0..3  element-wise, even units: thread r owns query row r (TMEM lane r);
 //   warps 4..7  element-wise, odd units;
-//   warp 8      TMA producer: Q and dO once, then K and V units into a ring of stages;
+//   warp 8      TMA producer: Q and dO once, then K and V units into two rings;
 //   warp 9      MMA issuer (one thread) and TMEM owner.
-// TMEM columns: warpgroup h: S [128h, 128h+64) (then dS, packed bf16, in its
-// first 32 columns), dP [128h+64, 128h+128); dQ [256, 256+D).
+// TMEM columns: regions [0,128), [128,256), [256,384); dQ [384, 384+D).
+// A unit's K stays resident from S(u) to dQ(u), its V from dP(u) only: the K
+// ring has more stages than the V ring.
 // Epilogue: dQ * scale in bf16 into the (no longer read) Q buffer in the TMA box
 // layout, stored by TMA; rows past S are clipped.
 #include "common.h"
@@ -35,35 +43,38 @@
 namespace gqa {
 namespace {
 
-constexpr int kUnit = 64;                       // keys per unit
-constexpr int kUnitBox = kUnit * 128;           // one 64-row box of 64 bf16 columns (8 KB)
+constexpr int kUnit = kTile;  // keys per unit (128)
+constexpr int kRegions = 3;
 
 template <int D>
 struct DqCfg {
   static constexpr int kChunks = D / kChunk;
-  static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kUnitBytes = kUnit * D * 2;  // one unit of K (or V)
-  static constexpr int kStages = (D == 64) ? 6 : 4;
+  static constexpr int kTileBytes = kTile * D * 2;  // a Q or dO tile, a K or V unit
+  static constexpr int kKStages = (D == 64) ? 6 : 3;
+  static constexpr int kVStages = (D == 64) ? 4 : 2;
   static constexpr int kQOff = 0;  // Q, then the dQ staging
   static constexpr int kDOOff = kQOff + kTileBytes;
   static constexpr int kKOff = kDOOff + kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kUnitBytes;
-  static constexpr int kBarOff = kVOff + kStages * kUnitBytes;
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // barriers + alignment slack
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kDQCol = 256;
+  static constexpr uint32_t kDQCol = kRegions * 128;
 };
 
-template <int ST>
+template <int KS, int VS>
 struct DqBars {
   uint64_t qdo_full;
-  uint64_t k_full[ST];
-  uint64_t v_full[ST];
-  uint64_t kv_empty[ST];
-  uint64_t s_full[2];
-  uint64_t dp_full[2];
-  uint64_t ds_full[2];
+  uint64_t k_full[KS];
+  uint64_t k_empty[KS];
+  uint64_t v_full[VS];
+  uint64_t v_empty[VS];
+  uint64_t s_full[kRegions];   // S(u) in region u % 3 (MMA commit)
+  uint64_t s_free[kRegions];   // S(u) read into registers (4 warp arrivals)
+  uint64_t dp_full[kRegions];  // dP(u) over it (MMA commit)
+  uint64_t ds_full[kRegions];  // dS(u) packed over it (4 warp arrivals)
   uint64_t dq_done;
   uint64_t drain;
   uint64_t epi_bar;
@@ -71,9 +82,13 @@ struct DqBars {
   int abort_flag;
 };
 
-static_assert(sizeof(DqBars<DqCfg<64>::kStages>) <= 256 && sizeof(DqBars<DqCfg<128>::kStages>) <= 256,
-              "dQ kernel barriers exceed the 256 bytes reserved for them");
+template <int D>
+using DqBarsOf = DqBars<DqCfg<D>::kKStages, DqCfg<D>::kVStages>;
+
+static_assert(sizeof(DqBarsOf<64>) <= DqCfg<64>::kBarBytes && sizeof(DqBarsOf<128>) <= DqCfg<128>::kBarBytes,
+              "dQ kernel barriers exceed the bytes reserved for them");
 static_assert(DqCfg<64>::kSmemBytes <= 232448 && DqCfg<128>::kSmemBytes <= 232448, "dQ kernel smem over the limit");
+static_assert(DqCfg<128>::kDQCol + 128 <= DqCfg<128>::kTmemCols, "dQ kernel TMEM columns");
 
 struct DqKParams {
   const float* lse2;  // f32 [B*Hq, S_pad]: LSE * log2(e), +inf past S
@@ -91,16 +106,33 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return true;
 }
 
+// Non-blocking test of a phase (try_wait may suspend the thread for a while first).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const __grid_constant__ CUtensorMap map_dq, const DqKParams p) {
   using C = DqCfg<D>;
-  constexpr int ST = C::kStages;
+  constexpr int KS = C::kKStages;
+  constexpr int VS = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  auto* bars = reinterpret_cast<DqBars<ST>*>(smem + C::kBarOff);
+  auto* bars = reinterpret_cast<DqBarsOf<D>*>(smem + C::kBarOff);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -111,20 +143,24 @@ __global__ void __launch_bounds__(320, 1)
   const int h = bh - b * p.Hq;
   const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
   // key units this query tile visits: causal, keys up to the tile's last row; else all S keys
-  const int n_units = p.causal ? 2 * (qt + 1) : (p.S + kUnit - 1) / kUnit;
+  const int n_units = p.causal ? qt + 1 : (p.S + kUnit - 1) / kUnit;
   const WaitGuard wg{&bars->abort_flag, p.status, kWaitLimitNs};
 
   if (tid == 0) {
     mbar_init(&bars->qdo_full, 1);
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int i = 0; i < kRegions; ++i) {
       mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], 4);  // one arrival per warp of the unit's warpgroup
       mbar_init(&bars->dp_full[i], 1);
-      mbar_init(&bars->ds_full[i], 4);  // one arrival per warp of the half's warpgroup
+      mbar_init(&bars->ds_full[i], 4);
     }
     mbar_init(&bars->dq_done, 1);
     mbar_init(&bars->drain, 1);
@@ -152,91 +188,115 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(smem + C::kQOff + c * kBoxBytes, &map_q, &bars->qdo_full, c * kChunk, qt * kTile, bh);
         tma_load_3d(smem + C::kDOOff + c * kBoxBytes, &map_do, &bars->qdo_full, c * kChunk, qt * kTile, bh);
       }
-      int issued = 0;
+      // K(u) may reuse its stage once dQ(u - KS) has run, V(u) once dP(u - VS) has.
+      int k_issued = 0, v_issued = 0;
       for (int u = 0; u < n_units; ++u) {
-        const int st = u % ST;
-        const int use = u / ST;
-        if (use > 0 && !mbar_wait(&bars->kv_empty[st], (use - 1) & 1, wg)) break;
-        mbar_arrive_expect_tx(&bars->k_full[st], C::kUnitBytes);
+        const int ks = u % KS;
+        if (u >= KS && !mbar_wait(&bars->k_empty[ks], ((u / KS) - 1) & 1, wg)) break;
+        mbar_arrive_expect_tx(&bars->k_full[ks], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kKOff + st * C::kUnitBytes + c * kUnitBox, &map_k, &bars->k_full[st], c * kChunk,
+          tma_load_3d(smem + C::kKOff + ks * C::kTileBytes + c * kBoxBytes, &map_k, &bars->k_full[ks], c * kChunk,
                       u * kUnit, kvh);
-        mbar_arrive_expect_tx(&bars->v_full[st], C::kUnitBytes);
+        k_issued = u + 1;
+        const int vs = u % VS;
+        if (u >= VS && !mbar_wait(&bars->v_empty[vs], ((u / VS) - 1) & 1, wg)) break;
+        mbar_arrive_expect_tx(&bars->v_full[vs], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kVOff + st * C::kUnitBytes + c * kUnitBox, &map_v, &bars->v_full[st], c * kChunk,
+          tma_load_3d(smem + C::kVOff + vs * C::kTileBytes + c * kBoxBytes, &map_v, &bars->v_full[vs], c * kChunk,
                       u * kUnit, kvh);
-        issued = u + 1;
+        v_issued = u + 1;
       }
       if (bars->abort_flag) {
         // Let every copy already issued land before the CTA's shared memory goes away.
         mbar_wait_drain(&bars->qdo_full, 0, kWaitLimitNs);
-        for (int u = (issued > ST ? issued - ST : 0); u < issued; ++u) {
-          mbar_wait_drain(&bars->k_full[u % ST], (u / ST) & 1, kWaitLimitNs);
-          mbar_wait_drain(&bars->v_full[u % ST], (u / ST) & 1, kWaitLimitNs);
-        }
+        for (int u = (k_issued > KS ? k_issued - KS : 0); u < k_issued; ++u)
+          mbar_wait_drain(&bars->k_full[u % KS], (u / KS) & 1, kWaitLimitNs);
+        for (int u = (v_issued > VS ? v_issued - VS : 0); u < v_issued; ++u)
+          mbar_wait_drain(&bars->v_full[u % VS], (u / VS) & 1, kWaitLimitNs);
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, kUnit, false, false);  // S, dP: 64 keys, both K-major
+      constexpr uint32_t idesc_s = idesc_bf16(128, kUnit, false, false);  // S, dP: 128 keys, both K-major
       constexpr uint32_t idesc_q = idesc_bf16(128, D, false, true);        // dQ: A = dS in TMEM, B = K MN-major
-      constexpr uint64_t kUnitDesc = (uint64_t)(C::kUnitBytes >> 4);
+      constexpr uint64_t kStageDesc = (uint64_t)(C::kTileBytes >> 4);
       const uint64_t dq0 = sdesc_sw128(smem_addr(smem + C::kQOff), 16, 1024);
       const uint64_t ddo0 = sdesc_sw128(smem_addr(smem + C::kDOOff), 16, 1024);
       const uint64_t dk0 = sdesc_sw128(smem_addr(smem + C::kKOff), 16, 1024);
       const uint64_t dv0 = sdesc_sw128(smem_addr(smem + C::kVOff), 16, 1024);
-      const uint64_t dkmn0 = sdesc_sw128(smem_addr(smem + C::kKOff), kUnitBox, 1024);
-      // S(u) = Q K_u^T into warpgroup u % 2's S columns; dP(u) = dO V_u^T into its dP columns.
-      // A operand (Q / dO): 128-row boxes, 16 KB apart; B operand (K / V unit): 64-row boxes, 8 KB apart.
+      const uint64_t dkmn0 = sdesc_sw128(smem_addr(smem + C::kKOff), kBoxBytes, 1024);
+      // S(u) = Q K_u^T and dP(u) = dO V_u^T into region u % 3. Both operands are 128-row
+      // boxes of 64 columns, 16 KB apart; 16 columns per MMA.
       auto issue_s = [=](int u) {
-        const uint64_t bk = dk0 + (uint64_t)(u % ST) * kUnitDesc;
+        const uint32_t dst = tbase + 128u * (uint32_t)(u % kRegions);
+        const uint64_t bk = dk0 + (uint64_t)(u % KS) * kStageDesc;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t offa = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
-          const uint64_t offb = (uint64_t)(((kk >> 2) * kUnitBox + (kk & 3) * 32) >> 4);
-          umma_ss(tbase + 128u * (u & 1), dq0 + offa, bk + offb, idesc_s, kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+          umma_ss(dst, dq0 + off, bk + off, idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->s_full[u & 1]);
+        umma_commit(&bars->s_full[u % kRegions]);
       };
       auto issue_dp = [=](int u) {
-        const uint64_t bv = dv0 + (uint64_t)(u % ST) * kUnitDesc;
+        const uint32_t dst = tbase + 128u * (uint32_t)(u % kRegions);
+        const uint64_t bv = dv0 + (uint64_t)(u % VS) * kStageDesc;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t offa = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
-          const uint64_t offb = (uint64_t)(((kk >> 2) * kUnitBox + (kk & 3) * 32) >> 4);
-          umma_ss(tbase + 128u * (u & 1) + 64u, ddo0 + offa, bv + offb, idesc_s, kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+          umma_ss(dst, ddo0 + off, bv + off, idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->dp_full[u & 1]);
+        umma_commit(&bars->dp_full[u % kRegions]);
+        umma_commit(&bars->v_empty[u % VS]);  // V(u): its only MMA has been issued
       };
-      // dQ += dS(u) K_u: 64 keys, 16 per MMA (16 K rows = 2 KB down the unit's boxes).
+      // dQ += dS(u) K_u: 128 keys, 16 per MMA (16 K rows = 2 KB down the unit's boxes).
       auto issue_dq = [=](int u) {
-        const uint64_t bk = dkmn0 + (uint64_t)(u % ST) * kUnitDesc;
+        const uint32_t src = tbase + 128u * (uint32_t)(u % kRegions);
+        const uint64_t bk = dkmn0 + (uint64_t)(u % KS) * kStageDesc;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_ts(tbase + C::kDQCol, tbase + 128u * (u & 1) + (uint32_t)kk * 8u, bk + (uint64_t)((kk * 2048) >> 4),
-                  idesc_q, (u > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kUnit / 16; ++kk)
+          umma_ts(tbase + C::kDQCol, src + (uint32_t)kk * 8u, bk + (uint64_t)((kk * 2048) >> 4), idesc_q,
+                  (u > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->k_empty[u % KS]);  // K(u): every MMA reading it has been issued
       };
-      // S and dP of unit u once its K and V have landed.
-      auto issue_sdp = [&](int u) {
-        if (!mbar_wait(&bars->k_full[u % ST], (u / ST) & 1, wg)) return false;
-        tc_fence_after();
-        issue_s(u);
-        if (!mbar_wait(&bars->v_full[u % ST], (u / ST) & 1, wg)) return false;
-        tc_fence_after();
-        issue_dp(u);
-        return true;
-      };
+      // ns, np, nq: the next unit whose S, dP, dQ is to be issued (nq <= np <= ns).
+      // S(u) overwrites region u % 3, last read by dQ(u - 3): issued before it, and the
+      // MMA pipe runs in issue order. Every barrier polled here is at most one phase
+      // ahead of the last one this thread saw complete, so parity identifies the phase.
+      int ns = 0, np = 0, nq = 0;
       bool ok = mbar_wait(&bars->qdo_full, 0, wg);
       if (ok) tc_fence_after();
-      for (int u = 0; ok && u < 2 && u < n_units; ++u) ok = issue_sdp(u);
-      for (int u = 0; ok && u < n_units; ++u) {
-        if (!(ok = mbar_wait(&bars->ds_full[u & 1], (u >> 1) & 1, wg))) break;
-        tc_fence_after();
-        issue_dq(u);
-        umma_commit(&bars->kv_empty[u % ST]);  // K_u, V_u: every MMA reading them has been issued
-        // S(u+2) overwrites dS(u), which dQ(u) just read: the MMA pipe runs in issue order.
-        if (u + 2 < n_units) ok = issue_sdp(u + 2);
+      uint64_t t_last = globaltimer_ns();
+      uint32_t idle = 0;
+      while (ok && nq < n_units) {
+        bool issued = false;
+        if (np < ns && mbar_test_wait(&bars->s_free[np % kRegions], (np / kRegions) & 1) &&
+            mbar_test_wait(&bars->v_full[np % VS], (np / VS) & 1)) {
+          tc_fence_after();
+          issue_dp(np++);
+          issued = true;
+        } else if (nq < np && mbar_test_wait(&bars->ds_full[nq % kRegions], (nq / kRegions) & 1)) {
+          tc_fence_after();
+          issue_dq(nq++);
+          issued = true;
+        } else if (ns < n_units && ns - nq < kRegions &&
+                   mbar_test_wait(&bars->k_full[ns % KS], (ns / KS) & 1)) {
+          tc_fence_after();
+          issue_s(ns++);
+          issued = true;
+        }
+        if (issued) {
+          idle = 0;
+        } else if ((++idle & 15u) == 0) {
+          if (idle == 16u) t_last = globaltimer_ns();
+          if (*wg.abort_flag) {
+            ok = false;
+          } else if (globaltimer_ns() - t_last > kWaitLimitNs) {
+            *wg.abort_flag = 1;
+            atomicOr(p.status, STATUS_TIMEOUT);
+            ok = false;
+          }
+        }
       }
       umma_commit(&bars->dq_done);
       umma_commit(&bars->drain);
@@ -247,15 +307,16 @@ __global__ void __launch_bounds__(320, 1)
     const int hh = warp >> 2;  // this warpgroup takes units hh, hh + 2, ...
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_tmem = tbase + lane_off + 128u * hh;
-    const uint32_t dp_tmem = s_tmem + 64u;
     const int qrow = qt * kTile + row;
     const size_t ridx = (size_t)bh * p.S_pad + qrow;  // rows past S: LSE2 = +inf, so P = 0
     const float neg_lse2 = -p.lse2[ridx];
     const float dval = p.dvec[ridx];
     const float c = p.scale_log2;
     bool ok = true;
-    for (int u = hh, it = 0; u < n_units; u += 2, ++it) {
+    for (int u = hh; u < n_units; u += 2) {
+      const int rg = u % kRegions;
+      const uint32_t ph = (uint32_t)(u / kRegions) & 1u;
+      const uint32_t reg_tmem = tbase + lane_off + 128u * (uint32_t)rg;
       const int kv0 = u * kUnit;
       // last visible key of this row within the unit (causal diagonal, or keys past S)
       int last = kUnit - 1;
@@ -263,47 +324,60 @@ __global__ void __launch_bounds__(320, 1)
       if (kv0 + kUnit > p.S) last = min(last, p.S - 1 - kv0);
       const bool masked = last < kUnit - 1;
 
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[hh], it & 1, wg));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[rg], ph, wg));
       if (!ok) break;
       tc_fence_after();
-      float P[64];
-      {
+      // P = exp2(S c - LSE2), packed to bf16 pairs: pp[x] holds keys 2x, 2x + 1.
+      uint32_t pp[kUnit / 2];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
         uint32_t r[64];
-        tmem_ld_32x32b_x32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        tmem_ld_32x32b_x32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_ld_32x32b_x32(reg_tmem + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld_32x32b_x32(reg_tmem + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
         tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         if (masked) {
 #pragma unroll
-          for (int x = 0; x < 64; ++x) {
-            const float e = ex2_approx(fmaf(__uint_as_float(r[x]), c, neg_lse2));
-            P[x] = (x <= last) ? e : 0.f;
+          for (int x = 0; x < 32; ++x) {
+            const int k0 = 64 * half + 2 * x;
+            const float e0 = ex2_approx(fmaf(__uint_as_float(r[2 * x]), c, neg_lse2));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(r[2 * x + 1]), c, neg_lse2));
+            pp[32 * half + x] = pack_bf16(k0 <= last ? e0 : 0.f, k0 + 1 <= last ? e1 : 0.f);
           }
         } else {
 #pragma unroll
-          for (int x = 0; x < 64; ++x) P[x] = ex2_approx(fmaf(__uint_as_float(r[x]), c, neg_lse2));
+          for (int x = 0; x < 32; ++x)
+            pp[32 * half + x] = pack_bf16(ex2_approx(fmaf(__uint_as_float(r[2 * x]), c, neg_lse2)),
+                                          ex2_approx(fmaf(__uint_as_float(r[2 * x + 1]), c, neg_lse2)));
         }
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->dp_full[hh], it & 1, wg));
+      tc_fence_before();
+      mbar_arrive_warp(&bars->s_free[rg]);  // the region may now take dP(u)
+
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->dp_full[rg], ph, wg));
       if (!ok) break;
       tc_fence_after();
-      uint32_t pk[32];
+      // dS = P (dP - D), packed: keys 64 half .. 64 half + 63 go to columns 32 half .. 32 half + 31,
+      // which hold dP columns that have already been read.
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t d[32];
-        tmem_ld_32x32b_x32(dp_tmem + q * 32, d);
-        tmem_wait_ld_x32(d);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t d[64];
+        tmem_ld_32x32b_x32(reg_tmem + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&d[0]));
+        tmem_ld_32x32b_x32(reg_tmem + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&d[32]));
+        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&d[0]));
+        tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&d[32]));
+        uint32_t pk[32];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int c0 = q * 32 + 2 * x;
-          pk[q * 16 + x] = pack_bf16(P[c0] * (__uint_as_float(d[2 * x]) - dval),
-                                     P[c0 + 1] * (__uint_as_float(d[2 * x + 1]) - dval));
+        for (int x = 0; x < 32; ++x) {
+          const uint32_t w = pp[32 * half + x];
+          pk[x] = pack_bf16(bf16_lo(w) * (__uint_as_float(d[2 * x]) - dval),
+                            bf16_hi(w) * (__uint_as_float(d[2 * x + 1]) - dval));
         }
+        tmem_st_32x32b_x32(reg_tmem + 32 * half, pk);
       }
-      tmem_st_32x32b_x32(s_tmem, pk);  // dS, packed bf16, over the first 32 columns of S
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(&bars->ds_full[hh]);
+      mbar_arrive_warp(&bars->ds_full[rg]);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_done, 0, wg));
     if (ok) {
@@ -366,7 +440,7 @@ cudaError_t launch_bwd_dq_d(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(a.B * a.Hq), (unsigned)n_tiles);
   trace_begin(kKernelBwdDq, stream);
-  bwd_dq_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k64, *a.map_v64, *a.map_do,
+  bwd_dq_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_do,
                                                                  *a.map_dq, p);
   e = cudaGetLastError();
   trace_end(kKernelBwdDq, stream);
