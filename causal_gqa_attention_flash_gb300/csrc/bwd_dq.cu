@@ -17,12 +17,15 @@
 //
 // One CTA = one (batch, query head, 128-row query tile). Keys stream in
 // 128-row units u (keys 128u .. 128u+127), so that every contraction is a
-// full-rate 128 x N x 16 MMA. Unit u is worked on by element-wise warpgroup
-// u % 2 in TMEM region u % 3 (128 columns): S(u) lands there; the warpgroup
-// turns it into P (bf16, kept in registers) and releases the region; dP(u)
-// is written over it; the warpgroup forms dS = P (dP - D), packs it to bf16
-// over the region's first 64 columns; dQ(u) reads it from there. A third
-// region lets S(u+2) be computed while unit u is still in flight.
+// full-rate 128 x N x 16 MMA. Q and dO are copied once into TMEM, so that all
+// three contractions take their A operand from TMEM: the tensor core reads
+// only K or V from shared memory (which leaves shared-memory bandwidth to the
+// TMA copies), and shared memory holds nothing but the K and V rings.
+// Unit u is worked on by element-wise warpgroup u % 2 in TMEM region u % R
+// (128 columns; R = 2 at D = 128, 3 at D = 64): S(u) lands there; the
+// warpgroup turns it into P (bf16, kept in registers) and releases the
+// region; dP(u) is written over it; the warpgroup forms dS = P (dP - D), packs
+// it to bf16 over the region's first 64 columns; dQ(u) reads it from there.
 // The MMA thread does not follow a fixed order: it polls which of dP, dQ and S
 // of the oldest pending units is ready and issues the first that is (dP before
 // dQ before S), so that no warpgroup's wait is queued behind an MMA that could
@@ -32,11 +35,13 @@
 //   warps 4..7  element-wise, odd units;
 //   warp 8      TMA producer: Q and dO once, then K and V units into two rings;
 //   warp 9      MMA issuer (one thread) and TMEM owner.
-// TMEM columns: regions [0,128), [128,256), [256,384); dQ [384, 384+D).
-// A unit's K stays resident from S(u) to dQ(u), its V from dP(u) only: the K
-// ring has more stages than the V ring.
-// Epilogue: dQ * scale in bf16 into the (no longer read) Q buffer in the TMA box
-// layout, stored by TMA; rows past S are clipped.
+// TMEM columns: regions [0, 128R); dQ [128R, 128R+D); Q (bf16 pairs)
+// [128R+D, 128R+3D/2); dO [128R+3D/2, 128R+2D) -- 512 in all at D = 128 and 64.
+// Q and dO arrive by TMA in the last stage of the K and V rings, which the
+// ring takes over once they are in TMEM. A unit's K stays resident from S(u)
+// to dQ(u), its V from dP(u) only: the K ring has more stages than the V ring.
+// Epilogue: dQ * scale in bf16 into the (no longer used) first K stage in the
+// TMA box layout, stored by TMA; rows past S are clipped.
 #include "common.h"
 #include "ptx.cuh"
 
@@ -44,37 +49,42 @@ namespace gqa {
 namespace {
 
 constexpr int kUnit = kTile;  // keys per unit (128)
-constexpr int kRegions = 3;
+constexpr int kMaxRegions = 3;
 
 template <int D>
 struct DqCfg {
   static constexpr int kChunks = D / kChunk;
   static constexpr int kTileBytes = kTile * D * 2;  // a Q or dO tile, a K or V unit
-  static constexpr int kKStages = (D == 64) ? 6 : 3;
-  static constexpr int kVStages = (D == 64) ? 4 : 2;
-  static constexpr int kQOff = 0;  // Q, then the dQ staging
-  static constexpr int kDOOff = kQOff + kTileBytes;
-  static constexpr int kKOff = kDOOff + kTileBytes;
+  static constexpr int kRegions = (D == 64) ? 3 : 2;
+  static constexpr int kKStages = (D == 64) ? 8 : 4;
+  static constexpr int kVStages = (D == 64) ? 5 : 3;
+  static constexpr int kKOff = 0;  // K ring (its first stage: the dQ staging at the end)
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kQStage = kKOff + (kKStages - 1) * kTileBytes;   // Q lands here first
+  static constexpr int kDOStage = kVOff + (kVStages - 1) * kTileBytes;  // dO lands here first
   static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // barriers + alignment slack
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kDQCol = kRegions * 128;
+  static constexpr uint32_t kQCol = kDQCol + D;
+  static constexpr uint32_t kDOCol = kQCol + D / 2;
+  static_assert(kDOCol + D / 2 <= kTmemCols, "dQ kernel TMEM columns");
 };
 
 template <int KS, int VS>
 struct DqBars {
-  uint64_t qdo_full;
+  uint64_t qdo_full;  // Q and dO in shared memory (TMA)
+  uint64_t qdo_tmem;  // Q and dO copied into TMEM (8 warp arrivals)
   uint64_t k_full[KS];
   uint64_t k_empty[KS];
   uint64_t v_full[VS];
   uint64_t v_empty[VS];
-  uint64_t s_full[kRegions];   // S(u) in region u % 3 (MMA commit)
-  uint64_t s_free[kRegions];   // S(u) read into registers (4 warp arrivals)
-  uint64_t dp_full[kRegions];  // dP(u) over it (MMA commit)
-  uint64_t ds_full[kRegions];  // dS(u) packed over it (4 warp arrivals)
+  uint64_t s_full[kMaxRegions];   // S(u) in region u % R (MMA commit)
+  uint64_t s_free[kMaxRegions];   // S(u) read into registers (4 warp arrivals)
+  uint64_t dp_full[kMaxRegions];  // dP(u) over it (MMA commit)
+  uint64_t ds_full[kMaxRegions];  // dS(u) packed over it (4 warp arrivals)
   uint64_t dq_done;
   uint64_t drain;
   uint64_t epi_bar;
@@ -88,7 +98,6 @@ using DqBarsOf = DqBars<DqCfg<D>::kKStages, DqCfg<D>::kVStages>;
 static_assert(sizeof(DqBarsOf<64>) <= DqCfg<64>::kBarBytes && sizeof(DqBarsOf<128>) <= DqCfg<128>::kBarBytes,
               "dQ kernel barriers exceed the bytes reserved for them");
 static_assert(DqCfg<64>::kSmemBytes <= 232448 && DqCfg<128>::kSmemBytes <= 232448, "dQ kernel smem over the limit");
-static_assert(DqCfg<128>::kDQCol + 128 <= DqCfg<128>::kTmemCols, "dQ kernel TMEM columns");
 
 struct DqKParams {
   const float* lse2;  // f32 [B*Hq, S_pad]: LSE * log2(e), +inf past S
@@ -130,6 +139,7 @@ __global__ void __launch_bounds__(320, 1)
   using C = DqCfg<D>;
   constexpr int KS = C::kKStages;
   constexpr int VS = C::kVStages;
+  constexpr int R = C::kRegions;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   auto* bars = reinterpret_cast<DqBarsOf<D>*>(smem + C::kBarOff);
@@ -148,6 +158,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (tid == 0) {
     mbar_init(&bars->qdo_full, 1);
+    mbar_init(&bars->qdo_tmem, 8);
     for (int s = 0; s < KS; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
@@ -156,7 +167,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int i = 0; i < kRegions; ++i) {
+    for (int i = 0; i < R; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], 4);  // one arrival per warp of the unit's warpgroup
       mbar_init(&bars->dp_full[i], 1);
@@ -185,14 +196,16 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&map_v);
       mbar_arrive_expect_tx(&bars->qdo_full, 2 * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(smem + C::kQOff + c * kBoxBytes, &map_q, &bars->qdo_full, c * kChunk, qt * kTile, bh);
-        tma_load_3d(smem + C::kDOOff + c * kBoxBytes, &map_do, &bars->qdo_full, c * kChunk, qt * kTile, bh);
+        tma_load_3d(smem + C::kQStage + c * kBoxBytes, &map_q, &bars->qdo_full, c * kChunk, qt * kTile, bh);
+        tma_load_3d(smem + C::kDOStage + c * kBoxBytes, &map_do, &bars->qdo_full, c * kChunk, qt * kTile, bh);
       }
-      // K(u) may reuse its stage once dQ(u - KS) has run, V(u) once dP(u - VS) has.
+      // K(u) may reuse its stage once dQ(u - KS) has run, V(u) once dP(u - VS) has; the
+      // last stage of each ring is first taken once Q and dO have been copied out of it.
       int k_issued = 0, v_issued = 0;
       for (int u = 0; u < n_units; ++u) {
         const int ks = u % KS;
         if (u >= KS && !mbar_wait(&bars->k_empty[ks], ((u / KS) - 1) & 1, wg)) break;
+        if (u == KS - 1 && !mbar_wait(&bars->qdo_tmem, 0, wg)) break;
         mbar_arrive_expect_tx(&bars->k_full[ks], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kKOff + ks * C::kTileBytes + c * kBoxBytes, &map_k, &bars->k_full[ks], c * kChunk,
@@ -200,6 +213,7 @@ __global__ void __launch_bounds__(320, 1)
         k_issued = u + 1;
         const int vs = u % VS;
         if (u >= VS && !mbar_wait(&bars->v_empty[vs], ((u / VS) - 1) & 1, wg)) break;
+        if (u == VS - 1 && !mbar_wait(&bars->qdo_tmem, 0, wg)) break;
         mbar_arrive_expect_tx(&bars->v_full[vs], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kVOff + vs * C::kTileBytes + c * kBoxBytes, &map_v, &bars->v_full[vs], c * kChunk,
@@ -218,40 +232,38 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, kUnit, false, false);  // S, dP: 128 keys, both K-major
+      constexpr uint32_t idesc_s = idesc_bf16(128, kUnit, false, false);  // S, dP: A in TMEM, B K-major
       constexpr uint32_t idesc_q = idesc_bf16(128, D, false, true);        // dQ: A = dS in TMEM, B = K MN-major
       constexpr uint64_t kStageDesc = (uint64_t)(C::kTileBytes >> 4);
-      const uint64_t dq0 = sdesc_sw128(smem_addr(smem + C::kQOff), 16, 1024);
-      const uint64_t ddo0 = sdesc_sw128(smem_addr(smem + C::kDOOff), 16, 1024);
       const uint64_t dk0 = sdesc_sw128(smem_addr(smem + C::kKOff), 16, 1024);
       const uint64_t dv0 = sdesc_sw128(smem_addr(smem + C::kVOff), 16, 1024);
       const uint64_t dkmn0 = sdesc_sw128(smem_addr(smem + C::kKOff), kBoxBytes, 1024);
-      // S(u) = Q K_u^T and dP(u) = dO V_u^T into region u % 3. Both operands are 128-row
-      // boxes of 64 columns, 16 KB apart; 16 columns per MMA.
+      // S(u) = Q K_u^T and dP(u) = dO V_u^T into region u % R. A: 16 columns of Q (dO) per
+      // MMA, 8 TMEM columns of bf16 pairs; B: 128-row boxes of 64 columns, 16 KB apart.
       auto issue_s = [=](int u) {
-        const uint32_t dst = tbase + 128u * (uint32_t)(u % kRegions);
+        const uint32_t dst = tbase + 128u * (uint32_t)(u % R);
         const uint64_t bk = dk0 + (uint64_t)(u % KS) * kStageDesc;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
-          umma_ss(dst, dq0 + off, bk + off, idesc_s, kk > 0 ? 1u : 0u);
+          umma_ts(dst, tbase + C::kQCol + (uint32_t)kk * 8u, bk + off, idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->s_full[u % kRegions]);
+        umma_commit(&bars->s_full[u % R]);
       };
       auto issue_dp = [=](int u) {
-        const uint32_t dst = tbase + 128u * (uint32_t)(u % kRegions);
+        const uint32_t dst = tbase + 128u * (uint32_t)(u % R);
         const uint64_t bv = dv0 + (uint64_t)(u % VS) * kStageDesc;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
-          umma_ss(dst, ddo0 + off, bv + off, idesc_s, kk > 0 ? 1u : 0u);
+          umma_ts(dst, tbase + C::kDOCol + (uint32_t)kk * 8u, bv + off, idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->dp_full[u % kRegions]);
+        umma_commit(&bars->dp_full[u % R]);
         umma_commit(&bars->v_empty[u % VS]);  // V(u): its only MMA has been issued
       };
       // dQ += dS(u) K_u: 128 keys, 16 per MMA (16 K rows = 2 KB down the unit's boxes).
       auto issue_dq = [=](int u) {
-        const uint32_t src = tbase + 128u * (uint32_t)(u % kRegions);
+        const uint32_t src = tbase + 128u * (uint32_t)(u % R);
         const uint64_t bk = dkmn0 + (uint64_t)(u % KS) * kStageDesc;
 #pragma unroll
         for (int kk = 0; kk < kUnit / 16; ++kk)
@@ -260,26 +272,26 @@ __global__ void __launch_bounds__(320, 1)
         umma_commit(&bars->k_empty[u % KS]);  // K(u): every MMA reading it has been issued
       };
       // ns, np, nq: the next unit whose S, dP, dQ is to be issued (nq <= np <= ns).
-      // S(u) overwrites region u % 3, last read by dQ(u - 3): issued before it, and the
+      // S(u) overwrites region u % R, last read by dQ(u - R): issued before it, and the
       // MMA pipe runs in issue order. Every barrier polled here is at most one phase
       // ahead of the last one this thread saw complete, so parity identifies the phase.
       int ns = 0, np = 0, nq = 0;
-      bool ok = mbar_wait(&bars->qdo_full, 0, wg);
+      bool ok = mbar_wait(&bars->qdo_tmem, 0, wg);
       if (ok) tc_fence_after();
       uint64_t t_last = globaltimer_ns();
       uint32_t idle = 0;
       while (ok && nq < n_units) {
         bool issued = false;
-        if (np < ns && mbar_test_wait(&bars->s_free[np % kRegions], (np / kRegions) & 1) &&
+        if (np < ns && mbar_test_wait(&bars->s_free[np % R], (np / R) & 1) &&
             mbar_test_wait(&bars->v_full[np % VS], (np / VS) & 1)) {
           tc_fence_after();
           issue_dp(np++);
           issued = true;
-        } else if (nq < np && mbar_test_wait(&bars->ds_full[nq % kRegions], (nq / kRegions) & 1)) {
+        } else if (nq < np && mbar_test_wait(&bars->ds_full[nq % R], (nq / R) & 1)) {
           tc_fence_after();
           issue_dq(nq++);
           issued = true;
-        } else if (ns < n_units && ns - nq < kRegions &&
+        } else if (ns < n_units && ns - nq < R &&
                    mbar_test_wait(&bars->k_full[ns % KS], (ns / KS) & 1)) {
           tc_fence_after();
           issue_s(ns++);
@@ -312,10 +324,32 @@ __global__ void __launch_bounds__(320, 1)
     const float neg_lse2 = -p.lse2[ridx];
     const float dval = p.dvec[ridx];
     const float c = p.scale_log2;
-    bool ok = true;
-    for (int u = hh; u < n_units; u += 2) {
-      const int rg = u % kRegions;
-      const uint32_t ph = (uint32_t)(u / kRegions) & 1u;
+    // Q (warpgroup 0) or dO (warpgroup 1) into TMEM: thread r copies row r out of the
+    // 128B-swizzled boxes as bf16 pairs, the layout of an MMA A operand in TMEM.
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->qdo_full, 0, wg));
+    if (ok) {
+      const uint8_t* src = smem + (hh == 0 ? C::kQStage : C::kDOStage);
+      const uint32_t dst = tbase + lane_off + (hh == 0 ? C::kQCol : C::kDOCol);
+#pragma unroll
+      for (int cb = 0; cb < C::kChunks; ++cb) {
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 x = *reinterpret_cast<const uint4*>(src + cb * kBoxBytes + row * 128 + ((j ^ (row & 7)) << 4));
+          w[4 * j] = x.x;
+          w[4 * j + 1] = x.y;
+          w[4 * j + 2] = x.z;
+          w[4 * j + 3] = x.w;
+        }
+        tmem_st_32x32b_x32(dst + 32u * (uint32_t)cb, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_warp(&bars->qdo_tmem);  // the MMA may read them; the ring may reuse the stages
+    }
+    for (int u = hh; ok && u < n_units; u += 2) {
+      const int rg = u % R;
+      const uint32_t ph = (uint32_t)(u / R) & 1u;
       const uint32_t reg_tmem = tbase + lane_off + 128u * (uint32_t)rg;
       const int kv0 = u * kUnit;
       // last visible key of this row within the unit (causal diagonal, or keys past S)
@@ -383,7 +417,7 @@ __global__ void __launch_bounds__(320, 1)
     if (ok) {
       tc_fence_after();
       // Warp w stores rows of its lane quarter, columns [hh * D/2, hh * D/2 + D/2).
-      uint8_t* stage = smem + C::kQOff;  // Q is no longer read by any MMA
+      uint8_t* stage = smem + C::kKOff;  // no MMA reads the K ring any more
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         const int col0 = hh * (D / 2) + cc * 32;
