@@ -78,7 +78,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {"bwd_main": ("bwd.cu", "ptx.cuh", "common.h"), "fwd": ("fwd.cu", "ptx.cuh", "common.h"),
-                  "decode_split": ("decode.cu", "ptx.cuh", "common.h")}
+                  "decode_split": ("decode.cu", "ptx.cuh", "common.h"),
+                  "bwd_dq": ("bwd_dq.cu", "ptx.cuh", "common.h")}
 
 
 def kernel_source_hash(kernel_name):
@@ -386,7 +387,7 @@ def deterministic_measurement(g, torch, w, peaks, peak_src, steps, warmup, bufs)
             "value": (fwd_fl + bwd_fl) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "kernels": {k_: {"launches": n_, "avg_ms": avg[k_]} for k_, (n_, _) in tr.items() if n_},
             "roofline": {"kernel": "bwd_dq", "bound": "tensor", "achieved": dq_tf, "peak": peak, "unit": "TFLOP/s",
-                         "frac": dq_tf / peak, "traffic": None,
+                         "frac": dq_tf / peak, "traffic": profiled_traffic("bwd_dq", w.name),
                          "peak_source": f"{peak_src} bf16 dense, sustained (kernel timed inside back-to-back steps)",
                          "bwd_dkdv_kernel": {"achieved": dkdv_tf, "frac": dkdv_tf / peak}}}
 
