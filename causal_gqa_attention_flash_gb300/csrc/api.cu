@@ -290,14 +290,6 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
   cudaError_t e;
   if ((e = encode_bf16(&mq, q, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
   if ((e = encode_bf16(&mdq, dq, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
-  // 64-row K / V boxes: the query-major dQ kernel streams keys in 64-row units.
-  CUtensorMap mk64, mv64;
-  if ((e = encode_3d(&mk64, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, S, B * Hkv, kChunk, CU_TENSOR_MAP_SWIZZLE_128B,
-                     64)) != cudaSuccess)
-    return fail_cuda(e);
-  if ((e = encode_3d(&mv64, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, S, B * Hkv, kChunk, CU_TENSOR_MAP_SWIZZLE_128B,
-                     64)) != cudaSuccess)
-    return fail_cuda(e);
   if ((e = encode_bf16(&mk, k, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
   if ((e = encode_bf16(&mv, v, D, S, B * Hkv)) != cudaSuccess) return fail_cuda(e);
   if ((e = encode_bf16(&mdo, dO, D, S, B * Hq)) != cudaSuccess) return fail_cuda(e);
@@ -313,8 +305,6 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
   a.map_do = &mdo;
   a.map_dqacc = &macc;
   a.map_dq = &mdq;
-  a.map_k64 = &mk64;
-  a.map_v64 = &mv64;
   a.deterministic = deterministic;
   a.rope_cos = rope_cos;
   a.rope_sin = rope_sin;
@@ -428,8 +418,6 @@ int gqa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void*
   a.map_do = &mdo;
   a.map_dqacc = &macc;
   a.map_dq = nullptr;
-  a.map_k64 = nullptr;
-  a.map_v64 = nullptr;
   a.deterministic = 0;
   a.rope_cos = nullptr;
   a.rope_sin = nullptr;

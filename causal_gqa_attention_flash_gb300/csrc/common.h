@@ -46,8 +46,6 @@ struct BwdArgs {
   const CUtensorMap* map_do;   // [B*Hq, S, D] bf16
   const CUtensorMap* map_dqacc;// [B*Hq, S, D] f32, box {32, 128, 1}, 128B swizzle
   const CUtensorMap* map_dq;   // [B*Hq, S, D] bf16 (deterministic path: dQ stored by TMA)
-  const CUtensorMap* map_k64;  // [B*Hkv, S, D] bf16, box {64, 64, 1} (deterministic path)
-  const CUtensorMap* map_v64;
   const void* o;               // bf16 [B, Hq, S, D]
   const void* dO;              // bf16 [B, Hq, S, D]
   const float* lse;            // f32 [B, Hq, S]
