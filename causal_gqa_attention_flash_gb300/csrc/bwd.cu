@@ -152,6 +152,7 @@ struct BwdKParams {
   // Dense: S rows per (b, head), D / LSE2 rows padded to S_pad per head. Packed: S = total rows
   // T, row stride of D / LSE2 = T (S_pad = T), sequences of at most max_seqlen rows.
   int Hq, Hkv, S, S_pad, causal, max_seqlen;
+  int n_ktiles;   // packed batch: key tiles of the longest sequence (the 1-D grid's inner extent)
   float scale, scale_log2;
   int* status;
   const float* rope_cos;  // rotary tables [S, D/2] (nullptr: none): K is rotated in shared memory,
@@ -198,17 +199,24 @@ __global__ void __launch_bounds__(352, 1)
     if (tid == 0) atomicOr(p.status, STATUS_MISALIGNED_SMEM);
     return;
   }
-  const int jt = blockIdx.y;   // key tile; tile 0 sees the most query tiles when causal
+  // Key tile jt (tile 0 sees the most query tiles when causal) of group grp = (batch entry or
+  // sequence, KV head). Dense: grid (groups, key tiles), the groups fastest, so that each wave
+  // holds ~9 neighbouring key tiles of every group. Packed: a 1-D grid that walks each group's key
+  // tiles consecutively, so that a sequence's key tiles run together and share its Q, dO and
+  // dQ-accumulator tiles in L2; with the groups fastest, a wave would hold about one key tile of
+  // every sequence and nearly every load and reduce-add would go to DRAM.
+  const int jt = kPacked ? (int)(blockIdx.x % (unsigned)p.n_ktiles) : (int)blockIdx.y;
+  const int grp = kPacked ? (int)(blockIdx.x / (unsigned)p.n_ktiles) : (int)blockIdx.x;
   const int G = p.Hq / p.Hkv;
-  const int b = (int)blockIdx.x / p.Hkv;  // batch entry (dense) or sequence (packed)
-  const int hkv = (int)blockIdx.x - b * p.Hkv;
+  const int b = grp / p.Hkv;  // batch entry (dense) or sequence (packed)
+  const int hkv = grp - b * p.Hkv;
   // L rows in this CTA's sequence, starting at row0 of the tensor maps; the KV head's map
   // coordinate, the first query head's, and the row stride of the D / LSE2 arrays.
   int L, row0, kv_coord, bhq0;
   if (!kPacked) {
     L = p.S;
     row0 = 0;
-    kv_coord = (int)blockIdx.x;
+    kv_coord = grp;
     bhq0 = b * p.Hq + hkv * G;
   } else {
     const int s0 = __ldg(p.cu + b), s1 = __ldg(p.cu + b + 1);
@@ -673,6 +681,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     p.S_pad = S_pad;
     p.causal = a.causal;
     p.max_seqlen = a.max_seqlen;
+    p.n_ktiles = n_tiles;
     p.rope_cos = a.rope_cos;
     p.rope_sin = a.rope_sin;
     p.scale = a.scale;
@@ -684,7 +693,9 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     const KernelKind kind = det ? kKernelBwdDkdv : kKernelBwdMain;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)(a.B * a.Hkv), (unsigned)n_tiles);
+    const long long packed_ctas = (long long)a.B * a.Hkv * n_tiles;
+    if (packed && packed_ctas >= (1ll << 31)) return cudaErrorInvalidValue;
+    const dim3 grid = packed ? dim3((unsigned)packed_ctas) : dim3((unsigned)(a.B * a.Hkv), (unsigned)n_tiles);
     trace_begin(kind, stream);
     kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_do, *a.map_dqacc, p);
     e = cudaGetLastError();
