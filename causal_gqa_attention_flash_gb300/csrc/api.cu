@@ -499,12 +499,16 @@ int check_decode(int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale) {
   return GQA_OK;
 }
 
-size_t decode_workspace(int B, int Hq, int Hkv, int Sq, int Sk, int D, int num_splits, size_t* ml_off) {
+// Workspace: the chunks' partial accumulators, their (m, l) pairs, and one arrival ticket per
+// (batch, KV head).
+size_t decode_workspace(int B, int Hq, int Hkv, int Sq, int Sk, int D, int num_splits, size_t* ml_off,
+                        size_t* ticket_off) {
   int splits = 1, chunk = kDecodeKeys;
   decode_split_plan(B, Hkv, Sk, num_splits, &splits, &chunk);
   const size_t rows = (size_t)B * Hkv * splits * decode_rows_padded((Hq / Hkv) * Sq);
   *ml_off = align256(rows * D * sizeof(float));
-  return align256(*ml_off + rows * 2 * sizeof(float));
+  *ticket_off = align256(*ml_off + rows * 2 * sizeof(float));
+  return align256(*ticket_off + (size_t)B * Hkv * sizeof(unsigned));
 }
 
 }  // namespace
@@ -514,8 +518,8 @@ extern "C" {
 
 size_t gqa_attn_decode_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int num_splits) {
   if (check_decode(B, Hq, Hkv, Sq, Sk, D, 1.0f) != GQA_OK) return 0;
-  size_t ml = 0;
-  return decode_workspace(B, Hq, Hkv, Sq, Sk, D, num_splits, &ml);
+  size_t ml = 0, tk = 0;
+  return decode_workspace(B, Hq, Hkv, Sq, Sk, D, num_splits, &ml, &tk);
 }
 
 int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
@@ -527,8 +531,8 @@ int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       !aligned(workspace, 256))
     return GQA_ERR_INVALID_ARG;
-  size_t ml_off = 0;
-  const size_t need = decode_workspace(B, Hq, Hkv, Sq, Sk, D, num_splits, &ml_off);
+  size_t ml_off = 0, ticket_off = 0;
+  const size_t need = decode_workspace(B, Hq, Hkv, Sq, Sk, D, num_splits, &ml_off, &ticket_off);
   if (workspace_bytes < need) return GQA_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap mk, mv;
   cudaError_t e;
@@ -548,6 +552,7 @@ int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
   a.lse = lse;
   a.part_acc = static_cast<float*>(workspace);
   a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ml_off);
+  a.tickets = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + ticket_off);
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;

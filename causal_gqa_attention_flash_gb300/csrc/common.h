@@ -81,6 +81,7 @@ struct DecodeArgs {
   float* lse;                // f32 [B, Hq, Sq]
   float* part_acc;           // f32 [B*Hkv, splits, rows, D]
   float* part_ml;            // f32 [B*Hkv, splits, rows, 2]
+  unsigned* tickets;         // [B*Hkv] arrival counters of the chunks, zeroed by the launcher
   int B, Hq, Hkv, Sq, Sk, D, causal, splits, chunk;
   float scale_log2;
   int* status;

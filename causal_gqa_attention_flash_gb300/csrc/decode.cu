@@ -12,8 +12,10 @@
 //   decode_split    one CTA per (batch, KV head, key chunk): the state of
 //                   every query row of the KV head's group (G heads x Sq rows,
 //                   R <= 16 rows) over the chunk's keys, written as a partial;
-//   decode_combine  one warp per query row: merges the partials of all chunks,
-//                   writes O (bf16) and LSE (f32).
+//                   the CTA that finishes last among the chunks of its
+//                   (batch, KV head) (an arrival ticket taken after a fence)
+//                   merges all the partials in chunk order and writes O (bf16)
+//                   and LSE (f32), so that no second kernel is launched.
 //
 // The work is bound by HBM (each cached key and value is read once). The key /
 // value tiles are staged by TMA in the same 128B-swizzled 128-row boxes as the
@@ -52,6 +54,7 @@ template <int ST>
 struct DecBars {
   uint64_t k_full[ST], v_full[ST], kv_empty[ST];
   int abort_flag;
+  int last;  // this CTA took the last ticket of its (batch, KV head): it merges the partials
 };
 static_assert(sizeof(DecBars<DecCfg<64>::kStages>) <= DecCfg<64>::kBarBytes, "decode barriers exceed their space");
 static_assert(sizeof(DecBars<DecCfg<128>::kStages>) <= DecCfg<128>::kBarBytes, "decode barriers exceed their space");
@@ -59,8 +62,11 @@ static_assert(DecCfg<64>::kSmemBytes <= 232448 && DecCfg<128>::kSmemBytes <= 232
 
 struct DecKParams {
   const uint16_t* q;   // [B, Hq, Sq, D]
+  uint16_t* o;         // [B, Hq, Sq, D]
+  float* lse;          // [B, Hq, Sq]
   float* part_acc;     // [B*Hkv, splits, R, D]
   float* part_ml;      // [B*Hkv, splits, R, 2]: (m, l), m in log2 units
+  unsigned* tickets;   // [B*Hkv]: chunks of the (batch, KV head) finished so far (zeroed per call)
   int Hq, Hkv, Sq, Sk, causal, splits, chunk;
   float scale_log2;
   int* status;
@@ -312,44 +318,47 @@ __global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
       p.part_ml[pr_row * 2 + 1] = L;
     }
   }
-}
 
-// One warp per query row (b, h, i): merge the chunk partials of its KV head group.
-template <int D>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const float* __restrict__ part_acc,
-                                                             const float* __restrict__ part_ml, uint16_t* __restrict__ o,
-                                                             float* __restrict__ lse, int B, int Hq, int Hkv, int Sq,
-                                                             int splits, int R) {
+  // ---- arrival ticket: the last chunk of this (batch, KV head) to finish merges all partials.
+  __threadfence();  // this thread's partial stores are visible device-wide before the ticket
+  __syncthreads();
+  if (tid == 0) bars->last = (atomicAdd(p.tickets + kvh, 1u) == (unsigned)p.splits - 1u) ? 1 : 0;
+  __syncthreads();
+  if (!bars->last) return;
+  __threadfence();
+  // One warp per real query row r = (h % G) Sq + i of the group, lanes over the columns; the
+  // chunks are merged in chunk order whichever CTA arrives last, so the result is reproducible.
+  // The partials of the other CTAs are read from L2 (ld.global.cg).
   constexpr int kDC = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // (b * Hq + h) * Sq + i
-  if (row >= B * Hq * Sq) return;
-  const int i = row % Sq;
-  const int bh = row / Sq;
-  const int b = bh / Hq, h = bh - b * Hq;
-  const int G = Hq / Hkv;
-  const int kvh = b * Hkv + h / G;
-  const int r = (h % G) * Sq + i;
-  float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, part_ml[(((size_t)kvh * splits + s) * R + r) * 2]);
-  const float ref = (M == -INFINITY) ? 0.f : M;
-  float a[kDC] = {};
-  float L = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const size_t pr_row = ((size_t)kvh * splits + s) * R + r;
-    const float f = ex2_approx(part_ml[pr_row * 2] - ref);
-    L = fmaf(part_ml[pr_row * 2 + 1], f, L);
+  for (int r = warp; r < G * p.Sq; r += kDecThreads / 32) {
+    const size_t row0 = (size_t)kvh * p.splits * R + r;  // partial row of chunk s: row0 + s R
+    float M = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(p.part_ml + (row0 + (size_t)s * R) * 2));
+    const float ref = (M == -INFINITY) ? 0.f : M;
+    float acc_o[kDC];
 #pragma unroll
-    for (int c = 0; c < kDC; ++c) a[c] = fmaf(part_acc[pr_row * D + lane * kDC + c], f, a[c]);
+    for (int c = 0; c < kDC; ++c) acc_o[c] = 0.f;
+    float L = 0.f;
+    for (int s = 0; s < p.splits; ++s) {
+      const size_t pr = row0 + (size_t)s * R;
+      const float f = ex2_approx(__ldcg(p.part_ml + pr * 2) - ref);
+      L = fmaf(__ldcg(p.part_ml + pr * 2 + 1), f, L);
+#pragma unroll
+      for (int c = 0; c < kDC; ++c) acc_o[c] = fmaf(__ldcg(p.part_acc + pr * D + lane * kDC + c), f, acc_o[c]);
+    }
+    const float inv = 1.f / L;
+    const int h = g * G + r / p.Sq;
+    const int i = r - (r / p.Sq) * p.Sq;
+    const size_t orow = ((size_t)b * p.Hq + h) * p.Sq + i;
+    uint16_t* op = p.o + orow * D + lane * kDC;
+    if constexpr (kDC == 4) {
+      *reinterpret_cast<uint2*>(op) =
+          make_uint2(pack_bf16(acc_o[0] * inv, acc_o[1] * inv), pack_bf16(acc_o[2] * inv, acc_o[3] * inv));
+    } else {
+      *reinterpret_cast<uint32_t*>(op) = pack_bf16(acc_o[0] * inv, acc_o[1] * inv);
+    }
+    if (lane == 0) p.lse[orow] = (M + __log2f(L)) * 0.69314718055994530942f;
   }
-  const float inv = 1.f / L;
-  uint16_t* orow = o + (size_t)row * D + lane * kDC;
-  if constexpr (kDC == 4) {
-    *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16(a[0] * inv, a[1] * inv), pack_bf16(a[2] * inv, a[3] * inv));
-  } else {
-    *reinterpret_cast<uint32_t*>(orow) = pack_bf16(a[0] * inv, a[1] * inv);
-  }
-  if (lane == 0) lse[row] = (M + __log2f(L)) * 0.69314718055994530942f;
 }
 
 template <int D, int R>
@@ -367,8 +376,11 @@ template <int D>
 cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   DecKParams p;
   p.q = static_cast<const uint16_t*>(a.q);
+  p.o = static_cast<uint16_t*>(a.o);
+  p.lse = a.lse;
   p.part_acc = a.part_acc;
   p.part_ml = a.part_ml;
+  p.tickets = a.tickets;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.Sq = a.Sq;
@@ -379,7 +391,9 @@ cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale_log2;
   p.status = a.status;
   const int R = a.Sq * (a.Hq / a.Hkv);
-  cudaError_t e;
+  // The tickets start from zero on every call (the caller's workspace holds them).
+  cudaError_t e = cudaMemsetAsync(a.tickets, 0, sizeof(unsigned) * (size_t)a.B * a.Hkv, stream);
+  if (e != cudaSuccess) return e;
   trace_begin(kKernelDecodeSplit, stream);
   if (R <= 1)
     e = launch_split<D, 1>(a, p, stream);
@@ -392,15 +406,6 @@ cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   else
     e = launch_split<D, 16>(a, p, stream);
   trace_end(kKernelDecodeSplit, stream);
-  if (e != cudaSuccess) return e;
-  const int Rpad = R <= 1 ? 1 : R <= 2 ? 2 : R <= 4 ? 4 : R <= 8 ? 8 : 16;
-  const int rows = a.B * a.Hq * a.Sq;
-  trace_begin(kKernelDecodeCombine, stream);
-  decode_combine_kernel<D><<<(rows * 32 + 255) / 256, 256, 0, stream>>>(a.part_acc, a.part_ml,
-                                                                         static_cast<uint16_t*>(a.o), a.lse, a.B,
-                                                                         a.Hq, a.Hkv, a.Sq, a.splits, Rpad);
-  e = cudaGetLastError();
-  trace_end(kKernelDecodeCombine, stream);
   return e;
 }
 

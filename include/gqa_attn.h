@@ -154,7 +154,11 @@ int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
  *     from the device's SM count); the chunk states are merged with the
  *     associative (m, l, acc) combine.
  *   workspace: device memory of gqa_attn_decode_workspace_size() bytes (same
- *     num_splits), 256-byte aligned, owned by the caller (per-chunk partials).
+ *     num_splits), 256-byte aligned, owned by the caller (per-chunk partials
+ *     and one arrival counter per (batch, KV head), which the call zeroes
+ *     itself; its contents need no initialisation). The CTA that finishes the
+ *     last chunk of a (batch, KV head) merges the chunks in chunk order: one
+ *     kernel (after a small memset), and the same result whichever CTA is last.
  * Supported: D in {64, 128}; (Hq/Hkv) * Sq <= 16 query rows per KV head.
  * Errors as gqa_attn_fwd; GQA_ERR_UNSUPPORTED for more than 16 rows per KV head.
  * Passage: RustingBrain docs, "Training infrastructure" (KV-cached decoding);
@@ -286,7 +290,7 @@ int gqa_attn_selftest_wait_timeout(int limit_us, void* stream);
 #define GQA_KERNEL_BWD_MAIN 2
 #define GQA_KERNEL_BWD_CONVERT 3
 #define GQA_KERNEL_DECODE_SPLIT 4
-#define GQA_KERNEL_DECODE_COMBINE 5
+#define GQA_KERNEL_DECODE_COMBINE 5 /* no longer launched: the last chunk's CTA merges the partials */
 #define GQA_KERNEL_BWD_DKDV 6 /* the deterministic backward's dK/dV kernel */
 #define GQA_KERNEL_BWD_DQ 7   /* the deterministic backward's query-major dQ kernel */
 #define GQA_KERNEL_ROPE 8     /* the rotary embedding's rotation pass */
