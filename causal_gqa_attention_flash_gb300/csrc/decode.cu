@@ -326,25 +326,43 @@ __global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
   __syncthreads();
   if (!bars->last) return;
   __threadfence();
-  // One warp per real query row r = (h % G) Sq + i of the group, lanes over the columns; the
-  // chunks are merged in chunk order whichever CTA arrives last, so the result is reproducible.
-  // The partials of the other CTAs are read from L2 (ld.global.cg).
+  // One warp per real query row r = (h % G) Sq + i of the group. The reference max and the
+  // sum of l are taken with lanes over the chunks (fixed shuffle order), the accumulator with
+  // lanes over the columns and the chunks in order, four loads in flight; whichever CTA
+  // arrives last, the result is the same. Partials of other CTAs are read from L2 (ld.global.cg).
   constexpr int kDC = D / 32;
   for (int r = warp; r < G * p.Sq; r += kDecThreads / 32) {
     const size_t row0 = (size_t)kvh * p.splits * R + r;  // partial row of chunk s: row0 + s R
     float M = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(p.part_ml + (row0 + (size_t)s * R) * 2));
+    for (int s = lane; s < p.splits; s += 32) M = fmaxf(M, __ldcg(p.part_ml + (row0 + (size_t)s * R) * 2));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float ref = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f;
+    for (int s = lane; s < p.splits; s += 32) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (row0 + (size_t)s * R) * 2));
+      L = fmaf(ml.y, ex2_approx(ml.x - ref), L);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     float acc_o[kDC];
 #pragma unroll
     for (int c = 0; c < kDC; ++c) acc_o[c] = 0.f;
-    float L = 0.f;
+#pragma unroll 4
     for (int s = 0; s < p.splits; ++s) {
       const size_t pr = row0 + (size_t)s * R;
       const float f = ex2_approx(__ldcg(p.part_ml + pr * 2) - ref);
-      L = fmaf(__ldcg(p.part_ml + pr * 2 + 1), f, L);
-#pragma unroll
-      for (int c = 0; c < kDC; ++c) acc_o[c] = fmaf(__ldcg(p.part_acc + pr * D + lane * kDC + c), f, acc_o[c]);
+      if constexpr (kDC == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_acc + pr * D) + lane);
+        acc_o[0] = fmaf(v.x, f, acc_o[0]);
+        acc_o[1] = fmaf(v.y, f, acc_o[1]);
+        acc_o[2] = fmaf(v.z, f, acc_o[2]);
+        acc_o[3] = fmaf(v.w, f, acc_o[3]);
+      } else {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(p.part_acc + pr * D) + lane);
+        acc_o[0] = fmaf(v.x, f, acc_o[0]);
+        acc_o[1] = fmaf(v.y, f, acc_o[1]);
+      }
     }
     const float inv = 1.f / L;
     const int h = g * G + r / p.Sq;
