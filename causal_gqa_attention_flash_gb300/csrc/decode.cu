@@ -320,12 +320,17 @@ __global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
   }
 
   // ---- arrival ticket: the last chunk of this (batch, KV head) to finish merges all partials.
-  __threadfence();  // this thread's partial stores are visible device-wide before the ticket
+  // The barrier orders every thread's partial stores before thread 0's fence, which (being
+  // cumulative) makes them visible device-wide before its ticket; the last CTA's thread 0
+  // fences after reading the ticket and the barrier hands that on to the CTA's other threads.
   __syncthreads();
-  if (tid == 0) bars->last = (atomicAdd(p.tickets + kvh, 1u) == (unsigned)p.splits - 1u) ? 1 : 0;
+  if (tid == 0) {
+    __threadfence();
+    bars->last = (atomicAdd(p.tickets + kvh, 1u) == (unsigned)p.splits - 1u) ? 1 : 0;
+    __threadfence();
+  }
   __syncthreads();
   if (!bars->last) return;
-  __threadfence();
   // One warp per real query row r = (h % G) Sq + i of the group. The reference max and the
   // sum of l are taken with lanes over the chunks (fixed shuffle order), the accumulator with
   // lanes over the columns and the chunks in order, four loads in flight; whichever CTA
