@@ -65,3 +65,16 @@ def test_rejects_too_many_rows():
     k = torch.zeros(1, 1, 64, 128, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(g.GqaAttnError):
         g.gqa_attn_decode_fwd(q, k, k)  # 32 query heads on one KV head: 32 rows > 16
+
+
+def test_merge_bitwise_reproducible():
+    """The CTA that finishes its KV head's last chunk merges every chunk in chunk order, so repeated
+    calls give the same bits whichever CTA happens to finish last (many chunks per KV head)."""
+    g = gqa()
+    _, k, v, _ = make_inputs(2, 16, 4, 4096, 128, 31, with_do=False)
+    q = make_inputs(2, 16, 4, 2, 128, 1031, with_do=False)[0]
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    runs = [g.gqa_attn_decode_fwd(q, k, v, num_splits=64) for _ in range(4)]  # 64 chunks of 64 keys
+    assert g.gqa_attn_get_error() == 0
+    for o, lse in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(lse, runs[0][1])
