@@ -23,6 +23,8 @@
 // of mma.sync m16n8k16 bf16 products (S = Q K^T, O += P V) with operands read
 // by ldmatrix: a 128-row tcgen05 tile would be at least 4x padding here, and
 // the tensor work is a small fraction of the time the cache takes to stream.
+#include <type_traits>
+
 #include "common.h"
 #include "ptx.cuh"
 
@@ -331,20 +333,30 @@ __global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
   }
   __syncthreads();
   if (!bars->last) return;
-  // One warp per real query row r = (h % G) Sq + i of the group. The reference max and the
-  // sum of l are taken with lanes over the chunks (fixed shuffle order), the accumulator with
-  // lanes over the columns and the chunks in order, four loads in flight; whichever CTA
-  // arrives last, the result is the same. Partials of other CTAs are read from L2 (ld.global.cg).
+  // One warp per real query row r = (h % G) Sq + i of the group: lane s holds chunk s's (m, l)
+  // (chunks past 32 in further rounds), the lanes hold the accumulator's columns; the first
+  // kPre chunks' accumulators are loaded in the same round trip as the (m, l) pairs. The max
+  // and the sum of l use a fixed shuffle order and the accumulator takes the chunks in order,
+  // so the result does not depend on which CTA arrived last. Partials are read from L2.
   constexpr int kDC = D / 32;
+  constexpr int kPre = 8;
+  using Vec = typename std::conditional<kDC == 4, float4, float2>::type;
   for (int r = warp; r < G * p.Sq; r += kDecThreads / 32) {
     const size_t row0 = (size_t)kvh * p.splits * R + r;  // partial row of chunk s: row0 + s R
-    float M = -INFINITY;
-    for (int s = lane; s < p.splits; s += 32) M = fmaxf(M, __ldcg(p.part_ml + (row0 + (size_t)s * R) * 2));
+    Vec pre[kPre];
+#pragma unroll
+    for (int s = 0; s < kPre; ++s)
+      if (s < p.splits) pre[s] = __ldcg(reinterpret_cast<const Vec*>(p.part_acc + (row0 + (size_t)s * R) * D) + lane);
+    float2 mine = make_float2(-INFINITY, 0.f);  // (m, l) of chunk `lane` (splits <= 32)
+    if (lane < p.splits) mine = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (row0 + (size_t)lane * R) * 2));
+    float M = mine.x;
+    for (int s = lane + 32; s < p.splits; s += 32) M = fmaxf(M, __ldcg(p.part_ml + (row0 + (size_t)s * R) * 2));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float ref = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f;
-    for (int s = lane; s < p.splits; s += 32) {
+    const float f_mine = ex2_approx(mine.x - ref);  // 0 for lanes past the chunks
+    float L = mine.y * f_mine;
+    for (int s = lane + 32; s < p.splits; s += 32) {
       const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (row0 + (size_t)s * R) * 2));
       L = fmaf(ml.y, ex2_approx(ml.x - ref), L);
     }
@@ -353,21 +365,25 @@ __global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
     float acc_o[kDC];
 #pragma unroll
     for (int c = 0; c < kDC; ++c) acc_o[c] = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < p.splits; ++s) {
-      const size_t pr = row0 + (size_t)s * R;
-      const float f = ex2_approx(__ldcg(p.part_ml + pr * 2) - ref);
+    auto add = [&](const Vec& v, float f) {
       if constexpr (kDC == 4) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_acc + pr * D) + lane);
         acc_o[0] = fmaf(v.x, f, acc_o[0]);
         acc_o[1] = fmaf(v.y, f, acc_o[1]);
         acc_o[2] = fmaf(v.z, f, acc_o[2]);
         acc_o[3] = fmaf(v.w, f, acc_o[3]);
       } else {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(p.part_acc + pr * D) + lane);
         acc_o[0] = fmaf(v.x, f, acc_o[0]);
         acc_o[1] = fmaf(v.y, f, acc_o[1]);
       }
+    };
+#pragma unroll
+    for (int s = 0; s < kPre; ++s)
+      if (s < p.splits) add(pre[s], __shfl_sync(0xffffffffu, f_mine, s));
+#pragma unroll 4
+    for (int s = kPre; s < p.splits; ++s) {
+      const size_t pr = row0 + (size_t)s * R;
+      const float f = s < 32 ? __shfl_sync(0xffffffffu, f_mine, s & 31) : ex2_approx(__ldcg(p.part_ml + pr * 2) - ref);
+      add(__ldcg(reinterpret_cast<const Vec*>(p.part_acc + pr * D) + lane), f);
     }
     const float inv = 1.f / L;
     const int h = g * G + r / p.Sq;
