@@ -50,6 +50,8 @@ __all__ = [
     "lib_path",
 ]
 
+# Tracing slots in the header's GQA_KERNEL_* order. "decode_combine" is no longer launched (the last
+# split CTA of each KV head merges the chunks); its slot stays so that the numbering is stable.
 KERNEL_NAMES = ("fwd", "bwd_prep", "bwd_main", "bwd_convert", "decode_split", "decode_combine", "bwd_dkdv", "bwd_dq", "rope")
 
 GQA_OK = 0
