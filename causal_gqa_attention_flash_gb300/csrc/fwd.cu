@@ -488,17 +488,11 @@ __global__ void __launch_bounds__(384, 1)
       const bool rowwise = p.cu_q != nullptr && (qt + 1) * kTile > g.Sq;
       uint8_t* stage = smem + C::kQOff + x * C::kTileBytes;  // Q_X is no longer read by any MMA
       uint16_t* orow = p.o + ((size_t)g.q_coord * p.Tq + g.q_row0 + qrow) * D;
-      // The whole O row in one round of TMEM loads (one wait instead of one per 32 columns: the
-      // epilogue of the CTA's last tile is not hidden behind any other work).
-      uint32_t o_all[D];
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc)
-        tmem_ld_32x32b_x32(o_tmem + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&o_all[32 * cc]));
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&o_all[32 * cc]));
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
-        const uint32_t* o = &o_all[32 * cc];
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(o_tmem + cc * 32, o);
+        tmem_wait_ld_x32(o);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {  // 16-byte units of 8 columns
           uint4 w;
