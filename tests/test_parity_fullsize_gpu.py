@@ -4,6 +4,14 @@ The oracle cannot evaluate every element at S = 4096 / 16384 in seconds, so
 it evaluates sampled rows one by one (O, LSE and dQ rows need only their own
 row; dK/dV rows need every query row that sees them), and properties that
 hold at any size are checked on whole tensors.
+
+Every gradient bound is taken from oracle values only: 2e-2 times the largest
+|reference| over the sampled rows of that tensor (a subset of the whole
+tensor's rows, so never looser than the whole-tensor bound), plus the
+absolute floor of the small cases. The sampled key rows include rows 0..2 and
+127..129, whose dK/dV sum over every query tile of every head of the group
+(the longest f32 accumulation chains and the most dQ reduce-adds meet there),
+and rows near the end, which the fewest query tiles see.
 """
 
 import numpy as np
@@ -11,7 +19,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL_GRAD_REL, assert_fwd_close, gqa, max_abs
+from gpu_helpers import TOL_GRAD_ABS_FLOOR, TOL_GRAD_REL, assert_fwd_close, gqa, max_abs
 from gqa_inputs import WORKLOADS, to_f64, workload_inputs
 
 pytestmark = pytest.mark.gpu
@@ -20,6 +28,30 @@ pytestmark = pytest.mark.gpu
 def _sample_rows(S):
     rows = {0, 1, 2, 127, 128, 129, S // 3, S // 2, S - 130, S - 129, S - 2, S - 1}
     return np.array(sorted(r for r in rows if 0 <= r < S))
+
+
+def _key_rows(S):
+    rows = {0, 1, 2, 127, 128, 129, (3 * S) // 4, S - 300, S - 129, S - 1}
+    return np.array(sorted(r for r in rows if 0 <= r < S))
+
+
+def grad_bound(refs):
+    """2e-2 * max|ref| over the oracle's sampled values (plus the absolute floor)."""
+    return TOL_GRAD_REL * max(float(np.max(np.abs(r))) for r in refs) + TOL_GRAD_ABS_FLOOR
+
+
+def group_f64(q, k, v, dO, b, gh, G):
+    """The f64 operands of KV head gh of batch entry b and its G query heads, as a 1 x G x 1 problem
+    (the definition couples nothing outside a (batch entry, KV head) group)."""
+    hs = slice(gh * G, (gh + 1) * G)
+    return (to_f64(q[b:b + 1, hs]), to_f64(k[b:b + 1, gh:gh + 1]), to_f64(v[b:b + 1, gh:gh + 1]),
+            to_f64(dO[b:b + 1, hs]))
+
+
+# (b, query head) pairs for O / LSE / dQ rows; (b, KV head) groups for dK / dV rows. Long16k's
+# key-row oracle costs ~30 s per group (row 0 is seen by all 16384 query rows of 4 heads), so it
+# takes one group; qwen3_8b takes two.
+KV_GROUPS = {"qwen3_8b": [(0, 0), (0, 7)], "long16k": [(1, 7)]}
 
 
 @pytest.mark.parametrize("name", ["qwen3_8b", "long16k"])
@@ -35,29 +67,31 @@ def test_fullsize_sampled(name):
     # properties on whole tensors
     for t in (o, lse, dq, dk, dv):
         assert torch.isfinite(t.float()).all()
-    # row 0 of every head attends to key 0 only: O = v_0, LSE = scale q_0 . k_0 (exact up to rounding)
+    # row 0 of every head attends to key 0 only: O = v_0 (exact up to the f32 arithmetic)
     G = w.G
     v0 = vd[:, :, 0].float().repeat_interleave(G, dim=1)
     assert (o[:, :, 0].float() - v0).abs().max().item() <= 1e-2
-    # sum over keys of dK is zero (rows of dS sum to zero), relative to the size of dK
-    colsum = dk.float().sum(dim=2).abs().max().item()
-    assert colsum <= 2e-2 * dk.float().abs().sum(dim=2).max().item()
 
     O, L = o.float().cpu().numpy(), lse.cpu().numpy()
     dQ, dK, dV = (t.float().cpu().numpy() for t in (dq, dk, dv))
-    qf, kf, vf, dOf = (to_f64(t) for t in (q, k, v, dO))
     rows = _sample_rows(w.S)
-    heads = [(0, 0), (w.B - 1, w.Hq - 1), (0, w.Hq // 2 + 1)]
-    for (b, h) in heads:
-        O_ref, L_ref = oracle.forward_rows(qf, kf, vf, b, h, rows, True, w.scale)
+    for (b, h) in [(0, 0), (w.B - 1, w.Hq - 1), (0, w.Hq // 2 + 1)]:
+        gh = h // G
+        qf, kf, vf, dOf = group_f64(q, k, v, dO, b, gh, G)
+        hl = h - gh * G
+        O_ref, L_ref = oracle.forward_rows(qf, kf, vf, 0, hl, rows, True, w.scale)
         assert_fwd_close(O[b, h, rows], L[b, h, rows], O_ref, L_ref, f"{name} b={b} h={h}")
-        dQ_ref = oracle.backward_dq_rows(qf, kf, vf, dOf, b, h, rows, True, w.scale)
+        dQ_ref = oracle.backward_dq_rows(qf, kf, vf, dOf, 0, hl, rows, True, w.scale)
         err = max_abs(dQ[b, h, rows], dQ_ref)
-        assert err <= TOL_GRAD_REL * np.max(np.abs(dQ[b, h])), f"{name} dQ rows b={b} h={h}: {err:.3e}"
-    # dK/dV rows: key rows near the end (few query rows see them) and one in the last quarter
-    kv_rows = np.array([w.S - 1, w.S - 129, w.S - 300, (3 * w.S) // 4])
-    for (b, gh) in [(0, 0), (w.B - 1, w.Hkv - 1)]:
-        dK_ref, dV_ref = oracle.backward_dkdv_rows(qf, kf, vf, dOf, b, gh, kv_rows, True, w.scale)
-        for nm, X, R, full in (("dK", dK, dK_ref, dK), ("dV", dV, dV_ref, dV)):
+        assert err <= grad_bound([dQ_ref]), f"{name} dQ rows b={b} h={h}: {err:.3e}"
+
+    kv_rows = _key_rows(w.S)
+    for (b, gh) in KV_GROUPS[name]:
+        qf, kf, vf, dOf = group_f64(q, k, v, dO, b, gh, G)
+        dK_ref, dV_ref = oracle.backward_dkdv_rows(qf, kf, vf, dOf, 0, 0, kv_rows, True, w.scale)
+        for nm, X, R in (("dK", dK, dK_ref), ("dV", dV, dV_ref)):
             err = max_abs(X[b, gh, kv_rows], R)
-            assert err <= TOL_GRAD_REL * np.max(np.abs(full[b, gh])), f"{name} {nm} rows b={b} g={gh}: {err:.3e}"
+            assert err <= grad_bound([R]), f"{name} {nm} rows b={b} g={gh}: {err:.3e} (rows {kv_rows})"
+        # sum over keys of dK is zero (each row of dS sums to zero): S elements, each within the gate
+        colsum = float(np.abs(dK[b, gh].astype(np.float64).sum(axis=0)).max())
+        assert colsum <= w.S * grad_bound([dK_ref])
