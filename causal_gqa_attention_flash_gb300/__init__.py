@@ -13,6 +13,10 @@ kernels; if the library is missing, the call raises.
 Layout is BHSD: q, o, dO, dq are [B, Hq, S, D] bf16; k, v, dk, dv are
 [B, Hkv, S, D] bf16; lse is [B, Hq, S] float32. Query head h reads KV head
 h // (Hq // Hkv).
+
+Every tensor the caller passes, inputs and outputs alike, is checked before
+the call: contiguous, of the expected dtype and shape, on the device of q;
+the call then runs with that device current.
 """
 
 from __future__ import annotations
@@ -61,6 +65,7 @@ GQA_ERR_WORKSPACE_TOO_SMALL = -3
 GQA_ERR_CUDA = -4
 GQA_ERR_TIMEOUT = -5
 GQA_ERR_INTERNAL = -6
+GQA_ERR_BOUNDS = -7
 NOALLOC_SCRATCH_BYTES = 64 << 20  # GQA_NOALLOC_SCRATCH_BYTES of include/gqa_attn.h
 
 
@@ -85,9 +90,9 @@ def gqa_attn_last_cuda_error() -> int:
     return int(_lib.load().gqa_attn_last_cuda_error())
 
 
-def _stream_handle(stream) -> int:
+def _stream_handle(stream, device=None) -> int:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     if isinstance(stream, torch.cuda.Stream):
         return int(stream.cuda_stream)
     return int(stream)
@@ -98,28 +103,63 @@ def _check(rc: int, where: str) -> None:
         raise GqaAttnError(rc, where)
 
 
+def _want(name, t, shape, dtype, device):
+    """A caller-supplied tensor must be contiguous, of the given dtype and shape, on `device`:
+    the library writes through its pointer, so a mismatch is refused here, before any launch."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if (not t.is_cuda or t.device != device or t.dtype != dtype or tuple(t.shape) != tuple(shape)
+            or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous {dtype} CUDA tensor of shape {tuple(shape)} on {device}, got "
+                         f"{t.dtype} {tuple(t.shape)} on {t.device}"
+                         + ("" if t.is_contiguous() else " (not contiguous)"))
+    return t
+
+
+def _out(name, t, shape, dtype, device):
+    """Output buffer: the caller's (checked) or a new one."""
+    if t is None:
+        return torch.empty(tuple(shape), device=device, dtype=dtype)
+    return _want(name, t, shape, dtype, device)
+
+
+def _workspace(t, need, device):
+    """Workspace buffer: the caller's (a contiguous uint8 CUDA tensor on `device`; its size is
+    checked by the library) or a new one of `need` bytes."""
+    if t is None:
+        return torch.empty(max(int(need), 256), device=device, dtype=torch.uint8)
+    if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != device or t.dtype != torch.uint8
+            or not t.is_contiguous()):
+        raise ValueError(f"workspace must be a contiguous uint8 CUDA tensor on {device}")
+    return t
+
+
 def _dims(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+        if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4
+                or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous 4-D bfloat16 CUDA tensor (BHSD), got "
-                             f"{t.dtype} {tuple(t.shape)} on {t.device}")
+                             f"{getattr(t, 'dtype', None)} {tuple(getattr(t, 'shape', ()))} on "
+                             f"{getattr(t, 'device', None)}")
     B, Hq, S, D = q.shape
     if k.shape[0] != B or k.shape[2] != S or k.shape[3] != D or v.shape != k.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError(f"q, k, v must be on one device, got {q.device}, {k.device}, {v.device}")
     return B, Hq, k.shape[1], S, D
 
 
 def gqa_attn_fwd(q, k, v, causal: bool = True, scale: float | None = None, o=None, lse=None, stream=None):
     """Forward: returns (o [B,Hq,S,D] bf16, lse [B,Hq,S] f32). ``scale`` defaults to 1/sqrt(D)."""
     B, Hq, Hkv, S, D = _dims(q, k, v)
+    dev = q.device
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    if o is None:
-        o = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((B, Hq, S), device=q.device, dtype=torch.float32)
-    rc = _lib.load().gqa_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                  B, Hq, Hkv, S, D, int(bool(causal)), float(scale), _stream_handle(stream))
+    o = _out("o", o, q.shape, torch.bfloat16, dev)
+    lse = _out("lse", lse, (B, Hq, S), torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = _lib.load().gqa_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                      B, Hq, Hkv, S, D, int(bool(causal)), float(scale), _stream_handle(stream, dev))
     _check(rc, "gqa_attn_fwd")
     return o, lse
 
@@ -136,37 +176,43 @@ def gqa_attn_bwd(q, k, v, o, dO, lse, causal: bool = True, scale: float | None =
     ``gqa_attn_bwd_workspace_size(...)`` bytes; one is allocated if omitted.
     ``deterministic`` selects gqa_attn_bwd_deterministic (bitwise reproducible dQ).
     """
-    B, Hq, Hkv, S, D = _dims(q, k, v)
-    for name, t in (("o", o), ("dO", dO)):
-        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
-            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor shaped like q")
-    if lse.shape != (B, Hq, S) or lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
-        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, Hq, S]")
+    B, Hq, Hkv, S, D = _grad_inputs(q, k, v, o, dO, lse)
+    dev = q.device
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    need = gqa_attn_bwd_workspace_size(B, Hq, Hkv, S, D)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    dq = _out("dq", dq, q.shape, torch.bfloat16, dev)
+    dk = _out("dk", dk, k.shape, torch.bfloat16, dev)
+    dv = _out("dv", dv, v.shape, torch.bfloat16, dev)
+    workspace = _workspace(workspace, gqa_attn_bwd_workspace_size(B, Hq, Hkv, S, D), dev)
     nbytes = workspace.numel() * workspace.element_size()
     name = "gqa_attn_bwd_deterministic" if deterministic else "gqa_attn_bwd"
-    rc = getattr(_lib.load(), name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
-                                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                                    workspace.data_ptr(), nbytes, B, Hq, Hkv, S, D, int(bool(causal)),
-                                    float(scale), _stream_handle(stream))
+    with torch.cuda.device(dev):
+        rc = getattr(_lib.load(), name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
+                                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                        workspace.data_ptr(), nbytes, B, Hq, Hkv, S, D, int(bool(causal)),
+                                        float(scale), _stream_handle(stream, dev))
     _check(rc, name)
     return dq, dk, dv
 
 
+def _grad_inputs(q, k, v, o, dO, lse):
+    """Checks of a backward's inputs: q, k, v as the forward's, o and dO shaped like q, lse [B, Hq, S]."""
+    B, Hq, Hkv, S, D = _dims(q, k, v)
+    _want("o", o, q.shape, torch.bfloat16, q.device)
+    _want("dO", dO, q.shape, torch.bfloat16, q.device)
+    _want("lse", lse, (B, Hq, S), torch.float32, q.device)
+    return B, Hq, Hkv, S, D
+
+
 def gqa_attn_get_error(stream=None) -> int:
-    """Synchronise the stream and return (and clear) the device status: 0 or a negative code."""
+    """Synchronise the stream and return (and clear) its status word on the current device: 0 or a
+    negative code raised by kernels launched on that stream."""
     return int(_lib.load().gqa_attn_get_error(_stream_handle(stream)))
 
 
 def gqa_attn_selftest_wait_timeout(limit_us: int, stream=None) -> None:
-    """Launch the bounded-wait self-test (a wait nothing ends; it gives up after limit_us)."""
+    """Launch the bounded-wait self-test (a wait nothing ends; it gives up after limit_us).
+    A testing hook (gqa_attn_testing.h), not part of the stable interface."""
     _check(_lib.load().gqa_attn_selftest_wait_timeout(int(limit_us), _stream_handle(stream)),
            "gqa_attn_selftest_wait_timeout")
 
@@ -195,12 +241,18 @@ def gqa_attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, causal: bool = True, s
     NOALLOC_SCRATCH_BYTES; larger problems raise GqaAttnError (workspace too
     small). Calls that overlap on the GPU race on the shared array.
     """
-    B, Hq, Hkv, S, D = _dims(q, k, v)
+    B, Hq, Hkv, S, D = _grad_inputs(q, k, v, o, dO, lse)
+    dev = q.device
+    _want("dq", dq, q.shape, torch.bfloat16, dev)
+    _want("dk", dk, k.shape, torch.bfloat16, dev)
+    _want("dv", dv, v.shape, torch.bfloat16, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    rc = _lib.load().gqa_attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
-                                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                                          B, Hq, Hkv, S, D, int(bool(causal)), float(scale), _stream_handle(stream))
+    with torch.cuda.device(dev):
+        rc = _lib.load().gqa_attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                              dO.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                              dv.data_ptr(), B, Hq, Hkv, S, D, int(bool(causal)), float(scale),
+                                              _stream_handle(stream, dev))
     _check(rc, "gqa_attn_bwd_noalloc")
     return dq, dk, dv
 
@@ -213,24 +265,19 @@ def gqa_attn_decode_fwd(q, k_cache, v_cache, causal: bool = True, scale: float |
                         o=None, lse=None, workspace=None, stream=None):
     """Attention of q [B,Hq,Sq,D] against a cache k/v [B,Hkv,Sk,D] (Sq <= Sk, query i at position
     Sk - Sq + i). Returns (o [B,Hq,Sq,D] bf16, lse [B,Hq,Sq] f32)."""
-    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
-        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 4-D bfloat16 CUDA tensor (BHSD)")
-    B, Hq, Sq, D = q.shape
-    Hkv, Sk = k_cache.shape[1], k_cache.shape[2]
-    if k_cache.shape != (B, Hkv, Sk, D) or v_cache.shape != k_cache.shape:
-        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k_cache.shape)}, v {tuple(v_cache.shape)}")
+    B, Hq, Hkv, Sq, Sk, D = _cache_dims(q, k_cache, v_cache)
+    dev = q.device
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32) if lse is None else lse
-    need = gqa_attn_decode_workspace_size(B, Hq, Hkv, Sq, Sk, D, num_splits)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    o = _out("o", o, q.shape, torch.bfloat16, dev)
+    lse = _out("lse", lse, (B, Hq, Sq), torch.float32, dev)
+    workspace = _workspace(workspace, gqa_attn_decode_workspace_size(B, Hq, Hkv, Sq, Sk, D, num_splits), dev)
     nbytes = workspace.numel() * workspace.element_size()
-    rc = _lib.load().gqa_attn_decode_fwd(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o.data_ptr(),
-                                         lse.data_ptr(), workspace.data_ptr(), nbytes, B, Hq, Hkv, Sq, Sk, D,
-                                         int(bool(causal)), float(scale), int(num_splits), _stream_handle(stream))
+    with torch.cuda.device(dev):
+        rc = _lib.load().gqa_attn_decode_fwd(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o.data_ptr(),
+                                             lse.data_ptr(), workspace.data_ptr(), nbytes, B, Hq, Hkv, Sq, Sk, D,
+                                             int(bool(causal)), float(scale), int(num_splits),
+                                             _stream_handle(stream, dev))
     _check(rc, "gqa_attn_decode_fwd")
     return o, lse
 
@@ -239,31 +286,42 @@ def gqa_attn_fwd_cached(q, k_cache, v_cache, causal: bool = True, scale: float |
                         stream=None):
     """Forward of q [B,Hq,Sq,D] over k/v [B,Hkv,Sk,D] (Sq <= Sk, query r at position Sk - Sq + r),
     on the tensor cores. Returns (o [B,Hq,Sq,D] bf16, lse [B,Hq,Sq] f32)."""
+    B, Hq, Hkv, Sq, Sk, D = _cache_dims(q, k_cache, v_cache)
+    dev = q.device
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = _out("o", o, q.shape, torch.bfloat16, dev)
+    lse = _out("lse", lse, (B, Hq, Sq), torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = _lib.load().gqa_attn_fwd_cached(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o.data_ptr(),
+                                             lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), float(scale),
+                                             _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_fwd_cached")
+    return o, lse
+
+
+def _cache_dims(q, k_cache, v_cache):
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
-        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+        if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4
+                or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous 4-D bfloat16 CUDA tensor (BHSD)")
     B, Hq, Sq, D = q.shape
     Hkv, Sk = k_cache.shape[1], k_cache.shape[2]
     if k_cache.shape != (B, Hkv, Sk, D) or v_cache.shape != k_cache.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k_cache.shape)}, v {tuple(v_cache.shape)}")
-    if scale is None:
-        scale = 1.0 / math.sqrt(D)
-    o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((B, Hq, Sq), device=q.device, dtype=torch.float32) if lse is None else lse
-    rc = _lib.load().gqa_attn_fwd_cached(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o.data_ptr(),
-                                         lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), float(scale),
-                                         _stream_handle(stream))
-    _check(rc, "gqa_attn_fwd_cached")
-    return o, lse
+    if k_cache.device != q.device or v_cache.device != q.device:
+        raise ValueError("q, k_cache, v_cache must be on one device")
+    return B, Hq, Hkv, Sq, Sk, D
 
 
 def _check_packed(name, t):
-    if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
+    if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 3
+            or not t.is_contiguous()):
         raise ValueError(f"{name} must be a contiguous 3-D bfloat16 CUDA tensor ([H, T, D])")
 
 
 def _check_cu(name, cu, device):
-    if not cu.is_cuda or cu.dtype != torch.int32 or cu.dim() != 1 or not cu.is_contiguous() or cu.numel() < 2:
+    if not isinstance(cu, torch.Tensor) or not cu.is_cuda or cu.dtype != torch.int32 or cu.dim() != 1 or not cu.is_contiguous() or cu.numel() < 2:
         raise ValueError(f"{name} must be a contiguous 1-D int32 CUDA tensor of nseq + 1 bounds")
     if cu.device != device:
         raise ValueError(f"{name} is on {cu.device}, the tensors on {device}")
@@ -281,18 +339,22 @@ def gqa_attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, 
     Hkv, Tk = k.shape[0], k.shape[1]
     if k.shape != (Hkv, Tk, D) or v.shape != k.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
-    _check_cu("cu_seqlens_q", cu_seqlens_q, q.device)
-    _check_cu("cu_seqlens_k", cu_seqlens_k, q.device)
+    dev = q.device
+    if k.device != dev or v.device != dev:
+        raise ValueError("q, k, v must be on one device")
+    _check_cu("cu_seqlens_q", cu_seqlens_q, dev)
+    _check_cu("cu_seqlens_k", cu_seqlens_k, dev)
     if cu_seqlens_q.numel() != cu_seqlens_k.numel():
         raise ValueError("cu_seqlens_q and cu_seqlens_k must describe the same number of sequences")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((Hq, Tq), device=q.device, dtype=torch.float32) if lse is None else lse
-    rc = _lib.load().gqa_attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                         cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
-                                         cu_seqlens_q.numel() - 1, int(max_seqlen_q), Hq, Hkv, Tq, Tk, D,
-                                         int(bool(causal)), float(scale), _stream_handle(stream))
+    o = _out("o", o, q.shape, torch.bfloat16, dev)
+    lse = _out("lse", lse, (Hq, Tq), torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = _lib.load().gqa_attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                             cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                                             cu_seqlens_q.numel() - 1, int(max_seqlen_q), Hq, Hkv, Tq, Tk, D,
+                                             int(bool(causal)), float(scale), _stream_handle(stream, dev))
     _check(rc, "gqa_attn_fwd_varlen")
     return o, lse
 
@@ -313,31 +375,33 @@ def gqa_attn_bwd_varlen(q, k, v, o, dO, lse, cu_seqlens, max_seqlen: int, causal
     if k.shape != (Hkv, T, D) or v.shape != k.shape or o.shape != q.shape or dO.shape != q.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}, "
                          f"o {tuple(o.shape)}, dO {tuple(dO.shape)}")
-    if lse.shape != (Hq, T) or lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
-        raise ValueError("lse must be a contiguous float32 CUDA tensor [Hq, T]")
-    _check_cu("cu_seqlens", cu_seqlens, q.device)
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("o", o), ("dO", dO)):
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, q on {dev}")
+    _want("lse", lse, (Hq, T), torch.float32, dev)
+    _check_cu("cu_seqlens", cu_seqlens, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    need = gqa_attn_bwd_varlen_workspace_size(Hq, Hkv, T, D)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    dq = _out("dq", dq, q.shape, torch.bfloat16, dev)
+    dk = _out("dk", dk, k.shape, torch.bfloat16, dev)
+    dv = _out("dv", dv, v.shape, torch.bfloat16, dev)
+    workspace = _workspace(workspace, gqa_attn_bwd_varlen_workspace_size(Hq, Hkv, T, D), dev)
     nbytes = workspace.numel() * workspace.element_size()
-    rc = _lib.load().gqa_attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
-                                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                                         cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, int(max_seqlen),
-                                         workspace.data_ptr(), nbytes, Hq, Hkv, T, D, int(bool(causal)),
-                                         float(scale), _stream_handle(stream))
+    with torch.cuda.device(dev):
+        rc = _lib.load().gqa_attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
+                                             lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                             cu_seqlens.data_ptr(), cu_seqlens.numel() - 1, int(max_seqlen),
+                                             workspace.data_ptr(), nbytes, Hq, Hkv, T, D, int(bool(causal)),
+                                             float(scale), _stream_handle(stream, dev))
     _check(rc, "gqa_attn_bwd_varlen")
     return dq, dk, dv
 
 
 def _check_tables(cos, sin, S, D, device):
     for name, t in (("rope_cos", cos), ("rope_sin", sin)):
-        if (not t.is_cuda or t.dtype != torch.float32 or tuple(t.shape) != (S, D // 2) or not t.is_contiguous()
-                or t.device != device):
+        if (not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32
+                or tuple(t.shape) != (S, D // 2) or not t.is_contiguous() or t.device != device):
             raise ValueError(f"{name} must be a contiguous float32 CUDA tensor [S, D/2] = [{S}, {D // 2}]")
 
 
@@ -356,18 +420,19 @@ def gqa_attn_fwd_rope(q, k, v, rope_cos, rope_sin, causal: bool = True, scale: f
     """Forward over rotary-embedded q and k (rotate-half pairing, f32 tables [S, D/2]):
     returns (o, lse) like gqa_attn_fwd."""
     B, Hq, Hkv, S, D = _dims(q, k, v)
-    _check_tables(rope_cos, rope_sin, S, D, q.device)
+    dev = q.device
+    _check_tables(rope_cos, rope_sin, S, D, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((B, Hq, S), device=q.device, dtype=torch.float32) if lse is None else lse
-    need = gqa_attn_fwd_rope_workspace_size(B, Hkv, S, D)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    o = _out("o", o, q.shape, torch.bfloat16, dev)
+    lse = _out("lse", lse, (B, Hq, S), torch.float32, dev)
+    workspace = _workspace(workspace, gqa_attn_fwd_rope_workspace_size(B, Hkv, S, D), dev)
     nbytes = workspace.numel() * workspace.element_size()
-    rc = _lib.load().gqa_attn_fwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), rope_cos.data_ptr(),
-                                       rope_sin.data_ptr(), o.data_ptr(), lse.data_ptr(), workspace.data_ptr(), nbytes,
-                                       B, Hq, Hkv, S, D, int(bool(causal)), float(scale), _stream_handle(stream))
+    with torch.cuda.device(dev):
+        rc = _lib.load().gqa_attn_fwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), rope_cos.data_ptr(),
+                                           rope_sin.data_ptr(), o.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+                                           nbytes, B, Hq, Hkv, S, D, int(bool(causal)), float(scale),
+                                           _stream_handle(stream, dev))
     _check(rc, "gqa_attn_fwd_rope")
     return o, lse
 
@@ -375,25 +440,20 @@ def gqa_attn_fwd_rope(q, k, v, rope_cos, rope_sin, causal: bool = True, scale: f
 def gqa_attn_bwd_rope(q, k, v, o, dO, lse, rope_cos, rope_sin, causal: bool = True, scale: float | None = None,
                       dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Backward of the rotary-embedded forward: (dq, dk, dv) with respect to the unrotated q, k."""
-    B, Hq, Hkv, S, D = _dims(q, k, v)
-    _check_tables(rope_cos, rope_sin, S, D, q.device)
-    for name, t in (("o", o), ("dO", dO)):
-        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
-            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor shaped like q")
-    if lse.shape != (B, Hq, S) or lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
-        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, Hq, S]")
+    B, Hq, Hkv, S, D = _grad_inputs(q, k, v, o, dO, lse)
+    dev = q.device
+    _check_tables(rope_cos, rope_sin, S, D, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    need = gqa_attn_bwd_rope_workspace_size(B, Hq, Hkv, S, D)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    dq = _out("dq", dq, q.shape, torch.bfloat16, dev)
+    dk = _out("dk", dk, k.shape, torch.bfloat16, dev)
+    dv = _out("dv", dv, v.shape, torch.bfloat16, dev)
+    workspace = _workspace(workspace, gqa_attn_bwd_rope_workspace_size(B, Hq, Hkv, S, D), dev)
     nbytes = workspace.numel() * workspace.element_size()
-    rc = _lib.load().gqa_attn_bwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
-                                       lse.data_ptr(), rope_cos.data_ptr(), rope_sin.data_ptr(), dq.data_ptr(),
-                                       dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), nbytes, B, Hq, Hkv, S, D,
-                                       int(bool(causal)), float(scale), _stream_handle(stream))
+    with torch.cuda.device(dev):
+        rc = _lib.load().gqa_attn_bwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(),
+                                           lse.data_ptr(), rope_cos.data_ptr(), rope_sin.data_ptr(), dq.data_ptr(),
+                                           dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), nbytes, B, Hq, Hkv, S,
+                                           D, int(bool(causal)), float(scale), _stream_handle(stream, dev))
     _check(rc, "gqa_attn_bwd_rope")
     return dq, dk, dv

@@ -1,11 +1,16 @@
-"""ctypes declarations of libgqa_attn.so (the C ABI in include/gqa_attn.h)."""
+"""ctypes declarations of libgqa_attn.so: the C ABI of include/gqa_attn.h and the testing hooks of
+include/gqa_attn_testing.h."""
 
 from __future__ import annotations
 
 import ctypes
 import os
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgqa_attn.so")
+_HERE = os.path.dirname(os.path.abspath(__file__))
+# GQA_ATTN_DEBUG=1 selects the checking build (every kernel checks its computed coordinates and
+# reports a failed check as GQA_ERR_BOUNDS); it is read once, when the library is first loaded.
+DEBUG = os.environ.get("GQA_ATTN_DEBUG", "0") == "1"
+LIB_PATH = os.path.join(_HERE, "libgqa_attn_debug.so" if DEBUG else "libgqa_attn.so")
 
 _c_int, _c_float, _vp, _sz = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
@@ -42,7 +47,7 @@ def load() -> ctypes.CDLL:
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(
-                f"{LIB_PATH} is missing: build it with `python -m causal_gqa_attention_flash_gb300.build` "
+                f"{LIB_PATH} is missing: build it with `python -m causal_gqa_attention_flash_gb300.build --all` "
                 "(the CUDA library is the only implementation; there is no CPU fallback)")
         lib = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in SIGNATURES.items():

@@ -7,12 +7,17 @@
 #include <vector>
 
 #include "../../include/gqa_attn.h"
+#include "../../include/gqa_attn_testing.h"
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.h"
 #include "ptx.cuh"
 
-// Device status word (one per device that loads the library). Kernels OR
-// STATUS_* bits into it; gqa_attn_get_error() reads and clears it.
-__device__ int g_gqa_status;
+// Device status words, one per stream that has called into the library on a
+// device (GQA_STATUS_STREAMS of them; slot 0 is shared by any further
+// streams). Kernels OR STATUS_* bits into the word of the stream they were
+// launched on; gqa_attn_get_error(stream) reads and clears that word only.
+__device__ int g_gqa_status[GQA_STATUS_STREAMS];
 
 namespace gqa {
 namespace {
@@ -26,22 +31,34 @@ int fail_cuda(cudaError_t e) {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-int* g_status_ptr[kMaxDevices] = {};
+int* g_status_base[kMaxDevices] = {};
+// Streams that own a status word, per device: entry i owns word i + 1.
+std::vector<void*> g_status_streams[kMaxDevices];
 
-// Address of g_gqa_status on the current device (looked up once per device).
-cudaError_t status_ptr(int** out) {
+// Address of the status word of `stream` on the current device. The array's address is looked
+// up once per device (with that device current); a stream is given the next free word on its
+// first call, and streams beyond the array share word 0.
+cudaError_t status_ptr(void* stream, int** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_ptr[dev]) {
+  if (!g_status_base[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_gqa_status);
     if (e != cudaSuccess) return e;
-    g_status_ptr[dev] = static_cast<int*>(p);
+    g_status_base[dev] = static_cast<int*>(p);
   }
-  *out = g_status_ptr[dev];
+  std::vector<void*>& owners = g_status_streams[dev];
+  size_t slot = 0;
+  for (size_t i = 0; i < owners.size(); ++i)
+    if (owners[i] == stream) slot = i + 1;
+  if (slot == 0 && owners.size() + 1 < (size_t)GQA_STATUS_STREAMS) {
+    owners.push_back(stream);
+    slot = owners.size();
+  }
+  *out = g_status_base[dev] + slot;
   return cudaSuccess;
 }
 
@@ -83,6 +100,8 @@ cudaError_t encode_bf16(CUtensorMap* m, const void* ptr, int D, int S, int nhead
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+}  // namespace
+
 int check_common(int B, int Hq, int Hkv, int S, int D, float scale) {
   if (B < 1 || Hq < 1 || Hkv < 1 || S < 1) return GQA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
@@ -90,10 +109,12 @@ int check_common(int B, int Hq, int Hkv, int S, int D, float scale) {
   if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
   const long long tiles = (S + kTile - 1) / kTile;
   if (tiles > 65535) return GQA_ERR_UNSUPPORTED;
-  if ((long long)B * Hq * tiles >= (1ll << 31) || (long long)B * Hq * (long long)S >= (1ll << 31))
-    return GQA_ERR_UNSUPPORTED;
+  // the padded D / LSE rows of the backward (B * Hq * tiles * 128) index with 32-bit ints
+  if ((long long)B * Hq * tiles * kTile >= (1ll << 31)) return GQA_ERR_UNSUPPORTED;
   return GQA_OK;
 }
+
+namespace {
 
 // ------------------------------------------------------------------ tracing
 
@@ -106,11 +127,67 @@ thread_local std::vector<TraceRec> t_trace;
 thread_local size_t t_trace_used = 0;
 thread_local int t_trace_error = 0;
 
+struct SetupRec {
+  const void* func;
+  int dev;
+  cudaError_t result;
+};
+std::mutex g_setup_mu;
+std::vector<SetupRec> g_setup;  // a few dozen kernel instances at most
+int g_sm_count[kMaxDevices] = {};
+
 }  // namespace
 
 int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
 
+cudaError_t kernel_setup(const void* func, int smem_bytes, int threads, int regs_needed) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_setup_mu);
+  for (const SetupRec& r : g_setup)
+    if (r.func == func && r.dev == dev) return r.result;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e == cudaSuccess && regs_needed > 0) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, func);
+    if (e == cudaSuccess && (long long)fa.numRegs * threads < regs_needed) e = cudaErrorInvalidConfiguration;
+  }
+  g_setup.push_back(SetupRec{func, dev, e});
+  return e;
+}
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  int n = __atomic_load_n(&g_sm_count[dev], __ATOMIC_RELAXED);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    __atomic_store_n(&g_sm_count[dev], n, __ATOMIC_RELAXED);
+  }
+  return n;
+}
+
+namespace {
+
+const char* const kKernelRangeNames[kKernelCount] = {
+    "fwd_kernel",          "bwd_prep_kernel",  "bwd_main_kernel",   "bwd_convert_kernel", "decode_split_kernel",
+    "decode_combine",      "bwd_dkdv_kernel",  "bwd_dq_kernel",     "rope_rotate_kernel"};
+
+// NVTX range over one entry point (a no-op unless a profiling tool is attached).
+struct NvtxScope {
+  explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+  ~NvtxScope() { nvtxRangePop(); }
+  NvtxScope(const NvtxScope&) = delete;
+  NvtxScope& operator=(const NvtxScope&) = delete;
+};
+
+}  // namespace
+
+// Every launch is bracketed by an NVTX range named after its kernel and, when this host thread
+// armed tracing, by two CUDA events on the launch's stream.
 void trace_begin(int kind, cudaStream_t s) {
+  nvtxRangePushA(kind >= 0 && kind < kKernelCount ? kKernelRangeNames[kind] : "gqa_kernel");
   if (!t_trace_armed) return;
   if (t_trace_used == t_trace.size()) {
     TraceRec r{kind, nullptr, nullptr};
@@ -126,6 +203,7 @@ void trace_begin(int kind, cudaStream_t s) {
 }
 
 void trace_end(int kind, cudaStream_t s) {
+  nvtxRangePop();
   if (!t_trace_armed) return;
   (void)kind;
   if (cudaEventRecord(t_trace[t_trace_used].end, s) != cudaSuccess) t_trace_error = 1;
@@ -159,7 +237,7 @@ int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
   if ((e = encode_bf16(&mv, v, D, Sk, B * Hkv)) != cudaSuccess) return fail_cuda(e);
   if ((e = encode_bf16(&mo, o, D, Sq, B * Hq)) != cudaSuccess) return fail_cuda(e);
   int* status = nullptr;
-  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  if ((e = status_ptr(stream, &status)) != cudaSuccess) return fail_cuda(e);
   FwdArgs a;
   a.map_q = &mq;
   a.map_k = &mk;
@@ -191,11 +269,13 @@ extern "C" {
 
 int gqa_attn_fwd_cached(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                         int Sq, int Sk, int D, int causal, float scale, void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_fwd_cached");
   return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, nullptr, nullptr, stream);
 }
 
 int gqa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int S,
                  int D, int causal, float scale, void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_fwd");
   return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, nullptr, nullptr, stream);
 }
 
@@ -207,6 +287,7 @@ size_t gqa_attn_fwd_rope_workspace_size(int B, int Hkv, int S, int D) {
 int gqa_attn_fwd_rope(const void* q, const void* k, const void* v, const float* rope_cos, const float* rope_sin,
                       void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S,
                       int D, int causal, float scale, void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_fwd_rope");
   if (!k || !rope_cos || !rope_sin || !workspace) return GQA_ERR_INVALID_ARG;
   int rc = check_common(B, Hq, Hkv, S, D, scale);
   if (rc != GQA_OK) return rc;
@@ -214,8 +295,11 @@ int gqa_attn_fwd_rope(const void* q, const void* k, const void* v, const float* 
     return GQA_ERR_INVALID_ARG;
   if (workspace_bytes < gqa_attn_fwd_rope_workspace_size(B, Hkv, S, D)) return GQA_ERR_WORKSPACE_TOO_SMALL;
   // The keys are re-read by every query tile of their group: rotate them once, here.
-  cudaError_t e = launch_rope_rotate(k, workspace, rope_cos, rope_sin, (long long)B * Hkv * S, S, D,
-                                     static_cast<cudaStream_t>(stream));
+  int* status = nullptr;
+  cudaError_t e = status_ptr(stream, &status);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = launch_rope_rotate(k, workspace, rope_cos, rope_sin, (long long)B * Hkv * S, S, D, status,
+                         static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   return fwd_dense(q, workspace, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, rope_cos, rope_sin, stream);
 }
@@ -223,6 +307,7 @@ int gqa_attn_fwd_rope(const void* q, const void* k, const void* v, const float* 
 int gqa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
                         const int* cu_seqlens_k, int nseq, int max_seqlen_q, int Hq, int Hkv, int Tq, int Tk, int D,
                         int causal, float scale, void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_fwd_varlen");
   if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return GQA_ERR_INVALID_ARG;
   if (nseq < 1 || Tq < 1 || Tk < 1 || max_seqlen_q < 1 || max_seqlen_q > Tq) return GQA_ERR_INVALID_ARG;
   int rc = check_common(1, Hq, Hkv, Tq > Tk ? Tq : Tk, D, scale);
@@ -238,7 +323,7 @@ int gqa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
   if ((e = encode_bf16(&mv, v, D, Tk, Hkv)) != cudaSuccess) return fail_cuda(e);
   if ((e = encode_bf16(&mo, o, D, Tq, Hq)) != cudaSuccess) return fail_cuda(e);
   int* status = nullptr;
-  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  if ((e = status_ptr(stream, &status)) != cudaSuccess) return fail_cuda(e);
   FwdArgs a;
   a.map_q = &mq;
   a.map_k = &mk;
@@ -297,7 +382,7 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
                      CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return fail_cuda(e);
   int* status = nullptr;
-  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  if ((e = status_ptr(stream, &status)) != cudaSuccess) return fail_cuda(e);
   BwdArgs a;
   a.map_q = &mq;
   a.map_k = &mk;
@@ -339,6 +424,7 @@ extern "C" {
 int gqa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S,
                  int D, int causal, float scale, void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_bwd");
   return bwd_dense(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, S, D, causal, scale, 0,
                    nullptr, nullptr, stream);
 }
@@ -347,6 +433,7 @@ int gqa_attn_bwd_deterministic(const void* q, const void* k, const void* v, cons
                                const float* lse, void* dq, void* dk, void* dv, void* workspace,
                                size_t workspace_bytes, int B, int Hq, int Hkv, int S, int D, int causal, float scale,
                                void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_bwd_deterministic");
   return bwd_dense(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, S, D, causal, scale, 1,
                    nullptr, nullptr, stream);
 }
@@ -360,6 +447,7 @@ int gqa_attn_bwd_rope(const void* q, const void* k, const void* v, const void* o
                       const float* rope_cos, const float* rope_sin, void* dq, void* dk, void* dv, void* workspace,
                       size_t workspace_bytes, int B, int Hq, int Hkv, int S, int D, int causal, float scale,
                       void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_bwd_rope");
   if (!q || !rope_cos || !rope_sin || !workspace) return GQA_ERR_INVALID_ARG;
   int rc = check_common(B, Hq, Hkv, S, D, scale);
   if (rc != GQA_OK) return rc;
@@ -370,8 +458,11 @@ int gqa_attn_bwd_rope(const void* q, const void* k, const void* v, const void* o
   // backward's own workspace sections.
   const size_t bwd_bytes = bwd_workspace_layout(B, Hq, S, D).total;
   void* q_rot = static_cast<uint8_t*>(workspace) + bwd_bytes;
-  cudaError_t e = launch_rope_rotate(q, q_rot, rope_cos, rope_sin, (long long)B * Hq * S, S, D,
-                                     static_cast<cudaStream_t>(stream));
+  int* status = nullptr;
+  cudaError_t e = status_ptr(stream, &status);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = launch_rope_rotate(q, q_rot, rope_cos, rope_sin, (long long)B * Hq * S, S, D, status,
+                         static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   return bwd_dense(q_rot, k, v, o, dO, lse, dq, dk, dv, workspace, bwd_bytes, B, Hq, Hkv, S, D, causal, scale, 0,
                    rope_cos, rope_sin, stream);
@@ -387,6 +478,7 @@ int gqa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void*
                         void* dq, void* dk, void* dv, const int* cu_seqlens, int nseq, int max_seqlen, void* workspace,
                         size_t workspace_bytes, int Hq, int Hkv, int T, int D, int causal, float scale,
                         void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_bwd_varlen");
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !cu_seqlens || !workspace)
     return GQA_ERR_INVALID_ARG;
   if (nseq < 1 || T < 1 || max_seqlen < 1 || max_seqlen > T) return GQA_ERR_INVALID_ARG;
@@ -410,7 +502,7 @@ int gqa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void*
                      CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return fail_cuda(e);
   int* status = nullptr;
-  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  if ((e = status_ptr(stream, &status)) != cudaSuccess) return fail_cuda(e);
   BwdArgs a;
   a.map_q = &mq;
   a.map_k = &mk;
@@ -452,13 +544,6 @@ int gqa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void*
 namespace gqa {
 namespace {
 
-int device_sms() {
-  int dev = 0, v = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-    return v;
-  return 148;
-}
-
 // Key chunk per split (a multiple of the 128-key tile) and the number of non-empty splits.
 // Automatic choice: the split count that minimises (waves of CTAs) x (key tiles per CTA + one
 // tile's worth of per-CTA overhead), one decode CTA per SM, so that the last wave is not mostly
@@ -468,7 +553,7 @@ void decode_split_plan(int B, int Hkv, int Sk, int num_splits, int* splits, int*
   int s = num_splits;
   if (s <= 0) {
     const long long units = (long long)B * Hkv;
-    const long long sms = (long long)device_sms() * kDecodeCtasPerSm;  // CTAs resident at once
+    const long long sms = (long long)device_sm_count() * kDecodeCtasPerSm;  // CTAs resident at once
     long long best = -1;
     s = 1;
     for (int c = 1; c <= tiles && c <= 512; ++c) {
@@ -525,6 +610,7 @@ size_t gqa_attn_decode_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, in
 int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
                         void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int Sq, int Sk, int D,
                         int causal, float scale, int num_splits, void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_decode_fwd");
   if (!q || !k_cache || !v_cache || !o || !lse || !workspace) return GQA_ERR_INVALID_ARG;
   int rc = check_decode(B, Hq, Hkv, Sq, Sk, D, scale);
   if (rc != GQA_OK) return rc;
@@ -543,7 +629,7 @@ int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
                      CU_TENSOR_MAP_SWIZZLE_128B, kDecodeKeys)) != cudaSuccess)
     return fail_cuda(e);
   int* status = nullptr;
-  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  if ((e = status_ptr(stream, &status)) != cudaSuccess) return fail_cuda(e);
   DecodeArgs a;
   a.map_k = &mk;
   a.map_v = &mv;
@@ -568,15 +654,17 @@ int gqa_attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache,
 }
 
 int gqa_attn_get_error(void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_get_error");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail_cuda(e);
   int* status = nullptr;
-  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  if ((e = status_ptr(stream, &status)) != cudaSuccess) return fail_cuda(e);
   int h = 0;
   if ((e = cudaMemcpyAsync(&h, status, sizeof(int), cudaMemcpyDeviceToHost, s)) != cudaSuccess) return fail_cuda(e);
   if ((e = cudaMemsetAsync(status, 0, sizeof(int), s)) != cudaSuccess) return fail_cuda(e);
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail_cuda(e);
+  if (h & STATUS_BOUNDS) return GQA_ERR_BOUNDS;
   if (h & STATUS_TIMEOUT) return GQA_ERR_TIMEOUT;
   if (h & STATUS_MISALIGNED_SMEM) return GQA_ERR_INTERNAL;
   if (h & STATUS_BAD_SEQLENS) return GQA_ERR_INVALID_ARG;
@@ -592,6 +680,7 @@ const char* gqa_attn_strerror(int code) {
     case GQA_ERR_CUDA: return "CUDA error";
     case GQA_ERR_TIMEOUT: return "device-side wait exceeded its time limit";
     case GQA_ERR_INTERNAL: return "kernel layout self-check failed (no work was done)";
+    case GQA_ERR_BOUNDS: return "debug build: a computed coordinate fell outside its tensor (the access was skipped)";
     default: return "unknown error code";
   }
 }
@@ -627,10 +716,11 @@ int gqa_attn_trace_collect(int* launches, double* total_ms) {
 }
 
 int gqa_attn_selftest_wait_timeout(int limit_us, void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_selftest_wait_timeout");
   if (limit_us < 1 || limit_us > 1000000) return GQA_ERR_INVALID_ARG;
   int* status = nullptr;
   cudaError_t e;
-  if ((e = status_ptr(&status)) != cudaSuccess) return fail_cuda(e);
+  if ((e = status_ptr(stream, &status)) != cudaSuccess) return fail_cuda(e);
   if ((e = launch_wait_selftest(status, (uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream))) !=
       cudaSuccess)
     return fail_cuda(e);

@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
                                                        const float* __restrict__ lse, float* __restrict__ dvec,
                                                        float* __restrict__ lse2, float* __restrict__ dq_acc,
                                                        int rows_total, int rows_valid, int S, int S_pad,
-                                                       float log2e, long long acc_vec4) {
+                                                       float log2e, long long acc_vec4, int* status) {
   constexpr int TPR = D / 8;            // threads per row
   constexpr int RPW = 32 / TPR;          // rows per warp and iteration
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
     const bool live = r < rows_total;
     const bool real = r < rows_valid && s < S;  // a row of O / dO (not padding)
     float acc = 0.f;
-    if (live && real) {
+    if (live && real && dbg_range(((long long)bh * S + s) * D + sub * 8, 8, (long long)(rows_valid / S_pad) * S * D,
+                                  status)) {
       const size_t base = ((size_t)bh * S + s) * D + sub * 8;
       const uint4 a = *reinterpret_cast<const uint4*>(o + base);
       const uint4 b = *reinterpret_cast<const uint4*>(dO + base);
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
     }
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
-    if (live && sub == 0) {
+    if (live && sub == 0 && dbg_range(r, 1, rows_total, status)) {
       dvec[r] = acc;
       lse2[r] = real ? lse[(size_t)bh * S + s] * log2e : INFINITY;
     }
@@ -153,6 +154,7 @@ struct BwdKParams {
   // T, row stride of D / LSE2 = T (S_pad = T), sequences of at most max_seqlen rows.
   int Hq, Hkv, S, S_pad, causal, max_seqlen;
   int n_ktiles;   // packed batch: key tiles of the longest sequence (the 1-D grid's inner extent)
+  int rows_total; // rows of the D / LSE2 arrays (padding included)
   float scale, scale_log2;
   int* status;
   const float* rope_cos;  // rotary tables [S, D/2] (nullptr: none): K is rotated in shared memory,
@@ -230,6 +232,10 @@ __global__ void __launch_bounds__(352, 1)
     bhq0 = hkv * G;
   }
   if (jt * kTile >= L) return;  // a packed batch's short sequence: this key tile does not exist
+  // Extents for the debug build's coordinate checks: heads of the query and key maps, and the
+  // rows of this CTA's sequence.
+  const int heads_q = kPacked ? p.Hq : (int)gridDim.x * G;
+  const int heads_kv = kPacked ? p.Hkv : (int)gridDim.x;
   const int n_tiles = (L + kTile - 1) / kTile;
   const int i_start = p.causal ? jt : 0;
   const int n_i = n_tiles - i_start;
@@ -276,8 +282,12 @@ __global__ void __launch_bounds__(352, 1)
       tma_prefetch_desc(&map_do);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(smem + C::kKOff + c * kBoxBytes, &map_k, &bars->kv_full, c * kChunk, row0 + jt * kTile, kv_coord);
-        tma_load_3d(smem + C::kVOff + c * kBoxBytes, &map_v, &bars->kv_full, c * kChunk, row0 + jt * kTile, kv_coord);
+        const bool kv_ok =
+            dbg_tile(c * kChunk, row0 + jt * kTile, kv_coord, D, kChunk, row0, row0 + L, heads_kv, p.status);
+        tma_load_3d_chk(smem + C::kKOff + c * kBoxBytes, &map_k, &bars->kv_full, c * kChunk, row0 + jt * kTile,
+                        kv_coord, kv_ok);
+        tma_load_3d_chk(smem + C::kVOff + c * kBoxBytes, &map_v, &bars->kv_full, c * kChunk, row0 + jt * kTile,
+                        kv_coord, kv_ok);
       }
       int issued = 0;
       for (int t = 0; t < n_steps; ++t) {
@@ -290,15 +300,20 @@ __global__ void __launch_bounds__(352, 1)
         uint64_t* bar = &bars->qdo_full[st];
         mbar_arrive_expect_tx(bar, 2 * C::kTileBytes + 2 * n_rowfl * 4);
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(smem + C::kQOff + st * C::kTileBytes + c * kBoxBytes, &map_q, bar, c * kChunk,
-                      row0 + i * kTile, bhq);
-          tma_load_3d(smem + C::kDOOff + st * C::kTileBytes + c * kBoxBytes, &map_do, bar, c * kChunk,
-                      row0 + i * kTile, bhq);
+          const bool q_ok = dbg_tile(c * kChunk, row0 + i * kTile, bhq, D, kChunk, row0, row0 + L, heads_q, p.status);
+          tma_load_3d_chk(smem + C::kQOff + st * C::kTileBytes + c * kBoxBytes, &map_q, bar, c * kChunk,
+                          row0 + i * kTile, bhq, q_ok);
+          tma_load_3d_chk(smem + C::kDOOff + st * C::kTileBytes + c * kBoxBytes, &map_do, bar, c * kChunk,
+                          row0 + i * kTile, bhq, q_ok);
         }
         float* srow = reinterpret_cast<float*>(smem + C::kRowOff) + st * 2 * C::kRowFl;
         const size_t roff = rows_at(hl, i) & ~size_t(3);
-        bulk_load(srow, p.lse2 + roff, n_rowfl * 4, bar);
-        bulk_load(srow + C::kRowFl, p.dvec + roff, n_rowfl * 4, bar);
+        if (dbg_range((long long)roff, n_rowfl, p.rows_total, p.status)) {
+          bulk_load(srow, p.lse2 + roff, n_rowfl * 4, bar);
+          bulk_load(srow + C::kRowFl, p.dvec + roff, n_rowfl * 4, bar);
+        } else {
+          mbar_complete_tx(bar, 2 * n_rowfl * 4);
+        }
         issued = t + 1;
       }
       if (bars->abort_flag) {
@@ -401,7 +416,8 @@ __global__ void __launch_bounds__(352, 1)
         for (int s2 = 0; s2 < D / 32; ++s2) {
           const uint8_t* stage = s2 < C::kChunks ? smem + C::kQOff + st * C::kTileBytes + s2 * kBoxBytes
                                                  : smem + C::kDOOff + st * C::kTileBytes + (s2 - C::kChunks) * kBoxBytes;
-          tma_reduce_add_3d(&map_acc, stage, s2 * 32, row0 + i * kTile, bhq);
+          if (dbg_tile(s2 * 32, row0 + i * kTile, bhq, D, 32, row0, row0 + L, heads_q, p.status))
+            tma_reduce_add_3d(&map_acc, stage, s2 * 32, row0 + i * kTile, bhq);
         }
         bulk_commit_group();
         bulk_wait_group_read<0>();
@@ -425,7 +441,7 @@ __global__ void __launch_bounds__(352, 1)
     if (kRope) {
       // Rotary embedding: thread (row, hf) turns half of its key row's pairs in shared memory.
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->kv_full, 0, wg));
-      if (ok && kv_valid) {
+      if (ok && kv_valid && dbg_range((long long)(row0 + kv_row) * (D / 2), D / 2, (long long)p.S * (D / 2), p.status)) {
         const int pos = row0 + kv_row;  // position within the (dense) sequence
         rope_rotate_row_smem<D>(smem + C::kKOff, row, p.rope_cos + (size_t)pos * (D / 2),
                                 p.rope_sin + (size_t)pos * (D / 2), 1.f, hf * (D / 32), (hf + 1) * (D / 32));
@@ -568,7 +584,9 @@ __global__ void __launch_bounds__(352, 1)
         tmem_wait_ld_x16(lo);
         tmem_wait_ld_x16(hi);
       }
-      if (kv_valid) {
+      if (kv_valid && dbg_range(((long long)kv_coord * p.S + row0 + kv_row) * D, D, (long long)heads_kv * p.S * D,
+                                p.status) &&
+          dbg_range((long long)(row0 + kv_row) * (D / 2), D / 2, (long long)p.S * (D / 2), p.status)) {
         const int pos = row0 + kv_row;
         const float* cs = p.rope_cos + (size_t)pos * (D / 2) + i0;
         const float* sn = p.rope_sin + (size_t)pos * (D / 2) + i0;
@@ -602,7 +620,7 @@ __global__ void __launch_bounds__(352, 1)
         tmem_ld_32x32b_x32(tbase + lane_off + C::kDKCol + col, dk);
         tmem_wait_ld_x32(dv);
         tmem_wait_ld_x32(dk);
-        if (kv_valid) {
+        if (kv_valid && dbg_range((long long)orow + col, 32, (long long)heads_kv * p.S * D, p.status)) {
           uint4* dstv = reinterpret_cast<uint4*>(p.dv + orow + col);
           uint4* dstk = reinterpret_cast<uint4*>(p.dk + orow + col);
 #pragma unroll
@@ -632,19 +650,6 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
-                                                  cudaSuccess)
-      n = v;
-    else
-      n = 148;
-  }
-  return n;
-}
-
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
@@ -655,7 +660,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   const int rows_valid = packed ? a.Hq * a.S : a.B * a.Hq * S_pad;
   const int rows_total = packed ? rows_valid + kRowPad : rows_valid;
   const long long acc_elems = det ? 0 : (long long)(packed ? 1 : a.B) * a.Hq * a.S * D;
-  const int sms = num_sms();
+  const int sms = device_sm_count();
   {
     const int threads = 256;
     long long want = ((long long)rows_total * (D / 8) + threads - 1) / threads;
@@ -663,7 +668,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     trace_begin(kKernelBwdPrep, stream);
     bwd_prep_kernel<D><<<blocks, threads, 0, stream>>>(
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse, a.dvec, a.lse2, a.dq_acc,
-        rows_total, rows_valid, a.S, S_pad, 1.4426950408889634f, acc_elems / 4);
+        rows_total, rows_valid, a.S, S_pad, 1.4426950408889634f, acc_elems / 4, a.status);
     cudaError_t e = cudaGetLastError();
     trace_end(kKernelBwdPrep, stream);
     if (e != cudaSuccess) return e;
@@ -682,6 +687,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     p.causal = a.causal;
     p.max_seqlen = a.max_seqlen;
     p.n_ktiles = n_tiles;
+    p.rows_total = rows_total;
     p.rope_cos = a.rope_cos;
     p.rope_sin = a.rope_sin;
     p.scale = a.scale;
@@ -691,7 +697,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
                 : det ? bwd_main_kernel<D, false, false, false>
                       : (a.rope_cos ? bwd_main_kernel<D, true, true, false> : bwd_main_kernel<D, true, false, false>);
     const KernelKind kind = det ? kKernelBwdDkdv : kKernelBwdMain;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads, 0);
     if (e != cudaSuccess) return e;
     const long long packed_ctas = (long long)a.B * a.Hkv * n_tiles;
     if (packed && packed_ctas >= (1ll << 31)) return cudaErrorInvalidValue;
@@ -705,7 +711,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   if (det) return launch_bwd_dq(a, stream);
   if (a.rope_cos)  // dQ of the unrotated queries
     return launch_rope_convert(a.dq_acc, a.dq, a.rope_cos, a.rope_sin, (long long)a.B * a.Hq * a.S, a.S, D, a.scale,
-                               stream);
+                               a.status, stream);
   {
     const long long n8 = acc_elems / 8;
     const int threads = 256;

@@ -155,6 +155,8 @@ __global__ void __launch_bounds__(320, 1)
   // key units this query tile visits: causal, keys up to the tile's last row; else all S keys
   const int n_units = p.causal ? qt + 1 : (p.S + kUnit - 1) / kUnit;
   const WaitGuard wg{&bars->abort_flag, p.status, kWaitLimitNs};
+  const int heads_q = (int)gridDim.x;                     // extents for the debug build's checks
+  const int heads_kv = heads_q / (p.Hq / p.Hkv);
 
   if (tid == 0) {
     mbar_init(&bars->qdo_full, 1);
@@ -196,8 +198,10 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&map_v);
       mbar_arrive_expect_tx(&bars->qdo_full, 2 * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(smem + C::kQStage + c * kBoxBytes, &map_q, &bars->qdo_full, c * kChunk, qt * kTile, bh);
-        tma_load_3d(smem + C::kDOStage + c * kBoxBytes, &map_do, &bars->qdo_full, c * kChunk, qt * kTile, bh);
+        const bool q_ok = dbg_tile(c * kChunk, qt * kTile, bh, D, kChunk, 0, p.S, heads_q, p.status);
+        tma_load_3d_chk(smem + C::kQStage + c * kBoxBytes, &map_q, &bars->qdo_full, c * kChunk, qt * kTile, bh, q_ok);
+        tma_load_3d_chk(smem + C::kDOStage + c * kBoxBytes, &map_do, &bars->qdo_full, c * kChunk, qt * kTile, bh,
+                        q_ok);
       }
       // K(u) may reuse its stage once dQ(u - KS) has run, V(u) once dP(u - VS) has; the
       // last stage of each ring is first taken once Q and dO have been copied out of it.
@@ -208,16 +212,18 @@ __global__ void __launch_bounds__(320, 1)
         if (u == KS - 1 && !mbar_wait(&bars->qdo_tmem, 0, wg)) break;
         mbar_arrive_expect_tx(&bars->k_full[ks], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kKOff + ks * C::kTileBytes + c * kBoxBytes, &map_k, &bars->k_full[ks], c * kChunk,
-                      u * kUnit, kvh);
+          tma_load_3d_chk(smem + C::kKOff + ks * C::kTileBytes + c * kBoxBytes, &map_k, &bars->k_full[ks],
+                          c * kChunk, u * kUnit, kvh,
+                          dbg_tile(c * kChunk, u * kUnit, kvh, D, kChunk, 0, p.S, heads_kv, p.status));
         k_issued = u + 1;
         const int vs = u % VS;
         if (u >= VS && !mbar_wait(&bars->v_empty[vs], ((u / VS) - 1) & 1, wg)) break;
         if (u == VS - 1 && !mbar_wait(&bars->qdo_tmem, 0, wg)) break;
         mbar_arrive_expect_tx(&bars->v_full[vs], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kVOff + vs * C::kTileBytes + c * kBoxBytes, &map_v, &bars->v_full[vs], c * kChunk,
-                      u * kUnit, kvh);
+          tma_load_3d_chk(smem + C::kVOff + vs * C::kTileBytes + c * kBoxBytes, &map_v, &bars->v_full[vs],
+                          c * kChunk, u * kUnit, kvh,
+                          dbg_tile(c * kChunk, u * kUnit, kvh, D, kChunk, 0, p.S, heads_kv, p.status));
         v_issued = u + 1;
       }
       if (bars->abort_flag) {
@@ -321,8 +327,9 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int qrow = qt * kTile + row;
     const size_t ridx = (size_t)bh * p.S_pad + qrow;  // rows past S: LSE2 = +inf, so P = 0
-    const float neg_lse2 = -p.lse2[ridx];
-    const float dval = p.dvec[ridx];
+    const bool r_ok = dbg_range((long long)ridx, 1, (long long)heads_q * p.S_pad, p.status);
+    const float neg_lse2 = r_ok ? -p.lse2[ridx] : 0.f;
+    const float dval = r_ok ? p.dvec[ridx] : 0.f;
     const float c = p.scale_log2;
     // Q (warpgroup 0) or dO (warpgroup 1) into TMEM: thread r copies row r out of the
     // 128B-swizzled boxes as bf16 pairs, the layout of an MMA A operand in TMEM.
@@ -440,7 +447,9 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t phase = 0;
       ok = wg_barrier(&bars->epi_bar, phase, wg);
       if (ok && tid == 0) {
-        for (int cb = 0; cb < C::kChunks; ++cb) tma_store_3d(&map_dq, stage + cb * kBoxBytes, cb * kChunk, qt * kTile, bh);
+        for (int cb = 0; cb < C::kChunks; ++cb)
+          if (dbg_tile(cb * kChunk, qt * kTile, bh, D, kChunk, 0, p.S, heads_q, p.status))
+            tma_store_3d(&map_dq, stage + cb * kBoxBytes, cb * kChunk, qt * kTile, bh);
         bulk_commit_group();
         bulk_wait_group_read<0>();
       }
@@ -470,7 +479,7 @@ cudaError_t launch_bwd_dq_d(const BwdArgs& a, cudaStream_t stream) {
   p.scale = a.scale;
   p.scale_log2 = a.scale_log2;
   p.status = a.status;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = kernel_setup(reinterpret_cast<const void*>(bwd_dq_kernel<D>), C::kSmemBytes, C::kThreads, 0);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(a.B * a.Hq), (unsigned)n_tiles);
   trace_begin(kKernelBwdDq, stream);

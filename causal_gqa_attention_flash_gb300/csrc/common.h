@@ -137,14 +137,27 @@ void trace_end(int kind, cudaStream_t s);
 // Keeps e as this host thread's last CUDA error and returns GQA_ERR_CUDA (api.cu).
 int record_cuda_error(cudaError_t e);
 
+// Once per (kernel, device): raises the kernel's dynamic shared-memory limit to smem_bytes and,
+// when regs_needed > 0, checks that threads x (registers per thread at launch) covers
+// regs_needed (a setmaxnreg split that the launch cannot satisfy would wait forever). Later calls
+// return the cached result without calling CUDA (api.cu).
+cudaError_t kernel_setup(const void* func, int smem_bytes, int threads, int regs_needed);
+
+// Host-side size and scale checks shared by the dense entry points: GQA_OK or the error code the
+// entry point returns (api.cu).
+int check_common(int B, int Hq, int Hkv, int S, int D, float scale);
+
+// Number of SMs of the current device, looked up once per device (api.cu).
+int device_sm_count();
+
 // Host launchers (fwd.cu, bwd.cu). Return a cudaError_t.
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_rope_rotate(const void* x, void* y, const float* cs, const float* sn, long long rows, int S, int D,
-                               cudaStream_t stream);
+                               int* status, cudaStream_t stream);
 cudaError_t launch_rope_convert(const float* acc, void* dq, const float* cs, const float* sn, long long rows, int S,
-                                int D, float scale, cudaStream_t stream);
+                                int D, float scale, int* status, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

@@ -150,13 +150,14 @@ __global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
         if (use > 0 && !mbar_wait(&bars->kv_empty[st], (use - 1) & 1, wg)) break;
         const int y = key0 + t * kDecodeKeys;
         mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
+        const bool kv_ok = dbg_tile(0, y, kvh, D, kChunk, 0, p.Sk, (int)gridDim.y, p.status);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kKOff + st * C::kTileBytes + c * kDecBox, &map_k, &bars->k_full[st], c * kChunk,
-                      y, kvh);
+          tma_load_3d_chk(smem + C::kKOff + st * C::kTileBytes + c * kDecBox, &map_k, &bars->k_full[st], c * kChunk,
+                          y, kvh, kv_ok, kDecBox);
         mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kVOff + st * C::kTileBytes + c * kDecBox, &map_v, &bars->v_full[st], c * kChunk,
-                      y, kvh);
+          tma_load_3d_chk(smem + C::kVOff + st * C::kTileBytes + c * kDecBox, &map_v, &bars->v_full[st], c * kChunk,
+                          y, kvh, kv_ok, kDecBox);
       }
     }
   } else {
@@ -174,7 +175,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
       auto qword = [&](int r, int col) -> uint32_t {  // bf16 pair (col, col + 1) of query row r
         const int hl = r / p.Sq, i = r - hl * p.Sq;
         if (r >= R || hl >= G) return 0u;  // padding rows: zero queries, partials never read
-        return *reinterpret_cast<const uint32_t*>(p.q + (((size_t)b * p.Hq + g * G + hl) * p.Sq + i) * D + col);
+        const size_t at = (((size_t)b * p.Hq + g * G + hl) * p.Sq + i) * D + col;
+        if (!dbg_range((long long)at, 2, (long long)gridDim.y / p.Hkv * p.Hq * p.Sq * D, p.status)) return 0u;
+        return *reinterpret_cast<const uint32_t*>(p.q + at);
       };
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
@@ -314,6 +317,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
       L = fmaf(st[D + 1], f, L);
     }
     const size_t pr_row = ((size_t)kvh * p.splits + split) * R + r;
+    if (!dbg_range((long long)pr_row, 1, (long long)gridDim.y * p.splits * R, p.status)) continue;
     p.part_acc[pr_row * D + d] = a;
     if (d == 0) {
       p.part_ml[pr_row * 2] = M;
@@ -328,7 +332,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    bars->last = (atomicAdd(p.tickets + kvh, 1u) == (unsigned)p.splits - 1u) ? 1 : 0;
+    bars->last = dbg_ok(kvh < (int)gridDim.y && (int)gridDim.x == p.splits, p.status) &&
+                         atomicAdd(p.tickets + kvh, 1u) == (unsigned)p.splits - 1u
+                     ? 1
+                     : 0;
     __threadfence();
   }
   __syncthreads();
@@ -389,6 +396,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
     const int h = g * G + r / p.Sq;
     const int i = r - (r / p.Sq) * p.Sq;
     const size_t orow = ((size_t)b * p.Hq + h) * p.Sq + i;
+    if (!dbg_range((long long)orow, 1, (long long)gridDim.y / p.Hkv * p.Hq * p.Sq, p.status)) continue;
     uint16_t* op = p.o + orow * D + lane * kDC;
     if constexpr (kDC == 4) {
       *reinterpret_cast<uint2*>(op) =
@@ -403,8 +411,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecodeCtasPerSm)
 template <int D, int R>
 cudaError_t launch_split(const DecodeArgs& a, const DecKParams& p, cudaStream_t stream) {
   using C = DecCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  cudaError_t e = kernel_setup(reinterpret_cast<const void*>(decode_split_kernel<D, R>), C::kSmemBytes,
+                               kDecThreads, 0);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.splits, (unsigned)(a.B * a.Hkv));
   decode_split_kernel<D, R><<<grid, kDecThreads, C::kSmemBytes, stream>>>(*a.map_k, *a.map_v, p);

@@ -46,11 +46,15 @@ template <int D>
 struct FwdCfg {
   static constexpr int kChunks = D / kChunk;
   static constexpr int kTileBytes = kTile * D * 2;  // one 128-row bf16 tile of Q, K, V or O
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  // K and V ring depths. V_j is needed one MMA-pair later in the key step than K_j and its stage
+  // is released later (after both P V products), so at D = 128 the V ring takes the third stage
+  // that 227 KB of shared memory leave room for.
+  static constexpr int kKStages = (D == 64) ? 4 : 2;
+  static constexpr int kVStages = (D == 64) ? 4 : 3;
   static constexpr int kQOff = 0;                   // Q_A, Q_B (reused as O staging)
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
   static constexpr int kThreads = 384;
   static constexpr uint32_t kTmemCols = 512;
@@ -61,13 +65,13 @@ struct FwdCfg {
   static_assert(2 * 128 * kHighRegs + 128 * kLowRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 };
 
-template <int ST>
+template <int KST, int VST>
 struct FwdBars {
   uint64_t q_full;
-  uint64_t k_full[ST];
-  uint64_t v_full[ST];
-  uint64_t k_empty[ST];
-  uint64_t v_empty[ST];
+  uint64_t k_full[KST];
+  uint64_t v_full[VST];
+  uint64_t k_empty[KST];
+  uint64_t v_empty[VST];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
@@ -78,7 +82,8 @@ struct FwdBars {
   int abort_flag;
 };
 
-static_assert(sizeof(FwdBars<FwdCfg<64>::kStages>) <= 256 && sizeof(FwdBars<FwdCfg<128>::kStages>) <= 256,
+static_assert(sizeof(FwdBars<FwdCfg<64>::kKStages, FwdCfg<64>::kVStages>) <= 256 &&
+                  sizeof(FwdBars<FwdCfg<128>::kKStages, FwdCfg<128>::kVStages>) <= 256,
               "forward barriers exceed the 256 bytes reserved for them");
 static_assert(FwdCfg<64>::kSmemBytes <= 232448 && FwdCfg<128>::kSmemBytes <= 232448, "forward smem over the limit");
 
@@ -172,6 +177,33 @@ __device__ __forceinline__ float row_max(const uint32_t (&r)[128], int last) {
   return fmax3(a0, a1, fmaxf(a2, a3));
 }
 
+// Masked tiles by 32-column chunks. The visible keys of a row are the prefix [0, last]; lo and hi
+// are the smallest and largest `last` of the warp (warp-uniform). A chunk every row of the warp
+// sees in full takes the unmasked form, a chunk no row of the warp sees is skipped (its P is 0),
+// and only the chunk(s) between take the per-key select: on the causal diagonal one chunk of four.
+__device__ __forceinline__ float row_max_chunked(const uint32_t (&r)[128], int last, int lo, int hi) {
+  float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (32 * q > hi) continue;
+    const bool full = 32 * q + 31 <= lo;
+#pragma unroll
+    for (int i = 32 * q; i < 32 * q + 32; i += 8) {
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        v[k] = __uint_as_float(r[i + k]);
+        if (!full) v[k] = (i + k <= last) ? v[k] : -INFINITY;
+      }
+      a0 = fmax3(a0, v[0], v[1]);
+      a1 = fmax3(a1, v[2], v[3]);
+      a2 = fmax3(a2, v[4], v[5]);
+      a3 = fmax3(a3, v[6], v[7]);
+    }
+  }
+  return fmax3(a0, a1, fmaxf(a2, a3));
+}
+
 // P = exp2(S c - m) for one row, packed to bf16 pairs and stored into the
 // row's S columns (32 columns per tcgen05.st); returns the row sum of P. The
 // sum runs in eight independent partial sums: the pass is latency-bound, and a
@@ -201,6 +233,37 @@ __device__ __forceinline__ float exp_pack_store(const uint32_t (&r)[128], int la
   return ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
 }
 
+// exp_pack_store for a masked tile, by 32-column chunks as row_max_chunked.
+__device__ __forceinline__ float exp_pack_store_chunked(const uint32_t (&r)[128], int last, int lo, int hi, float c,
+                                                        float neg_m, uint32_t s_tmem) {
+  float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t pk[16];
+    if (32 * q > hi) {
+#pragma unroll
+      for (int x2 = 0; x2 < 16; ++x2) pk[x2] = 0u;
+    } else {
+      const bool full = 32 * q + 31 <= lo;
+#pragma unroll
+      for (int x2 = 0; x2 < 16; ++x2) {
+        const int i = q * 32 + 2 * x2;
+        float e0 = ex2_approx(fmaf(__uint_as_float(r[i]), c, neg_m));
+        float e1 = ex2_approx(fmaf(__uint_as_float(r[i + 1]), c, neg_m));
+        if (!full) {
+          e0 = (i <= last) ? e0 : 0.f;
+          e1 = (i + 1 <= last) ? e1 : 0.f;
+        }
+        sm[(x2 & 3) * 2] += e0;
+        sm[(x2 & 3) * 2 + 1] += e1;
+        pk[x2] = pack_bf16(e0, e1);
+      }
+    }
+    tmem_st_32x32b_x16(s_tmem + q * 16, pk);
+  }
+  return ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+}
+
 // Number of key tiles query tile qt visits; 0 if the tile lies past Sq.
 __device__ __forceinline__ int kv_tiles_of(int qt, const FwdGeom& g, int causal) {
   if (qt * kTile >= g.Sq) return 0;
@@ -216,10 +279,11 @@ __global__ void __launch_bounds__(384, 1)
                const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
                const FwdKParams p) {
   using C = FwdCfg<D>;
-  constexpr int ST = C::kStages;
+  constexpr int ST = C::kKStages;   // K ring
+  constexpr int VST = C::kVStages;  // V ring
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  auto* bars = reinterpret_cast<FwdBars<ST>*>(smem + C::kBarOff);
+  auto* bars = reinterpret_cast<FwdBars<ST, VST>*>(smem + C::kBarOff);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -237,13 +301,20 @@ __global__ void __launch_bounds__(384, 1)
   const int n_kv = nA > nB ? nA : nB;
   if (nA == 0) return;  // a packed batch's short sequence: no query tile of this CTA exists
   const WaitGuard wg{&bars->abort_flag, p.status, kWaitLimitNs};
+  // Extents of the tensors this CTA addresses, for the debug build's coordinate checks: heads of
+  // the query / key maps and their rows (a packed CTA stays within its own sequence's rows).
+  const int heads_q = p.cu_q ? p.Hq : (int)gridDim.x;
+  const int heads_kv = p.cu_q ? p.Hkv : (int)gridDim.x / (p.Hq / p.Hkv);
+  const int rows_q = p.cu_q ? p.Tq : p.Sq;
 
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -273,20 +344,29 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
-      mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * kBoxBytes, &map_q, &bars->q_full, c * kChunk,
-                      g.q_row0 + (qtA + t) * kTile, g.q_coord);
+      // Q_B only when tile B has rows (its buffer is otherwise never read)
+      const int nq = nB > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(&bars->q_full, nq * C::kTileBytes);
+      for (int t = 0; t < nq; ++t)
+        for (int c = 0; c < C::kChunks; ++c) {
+          const int r = g.q_row0 + (qtA + t) * kTile;
+          tma_load_3d_chk(smem + C::kQOff + t * C::kTileBytes + c * kBoxBytes, &map_q, &bars->q_full, c * kChunk, r,
+                          g.q_coord, dbg_tile(c * kChunk, r, g.q_coord, D, kChunk, g.q_row0, g.q_row0 + g.Sq,
+                                              heads_q, p.status));
+        }
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % ST;
         const int use = j / ST;
         if (use > 0 && !mbar_wait(&bars->k_empty[st], (use - 1) & 1, wg)) break;
         mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kKOff + st * C::kTileBytes + c * kBoxBytes, &map_k, &bars->k_full[st], c * kChunk,
-                      g.k_row0 + j * kTile, g.kv_coord);
+        for (int c = 0; c < C::kChunks; ++c) {
+          const int r = g.k_row0 + j * kTile;
+          tma_load_3d_chk(smem + C::kKOff + st * C::kTileBytes + c * kBoxBytes, &map_k, &bars->k_full[st],
+                          c * kChunk, r, g.kv_coord,
+                          dbg_tile(c * kChunk, r, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv,
+                                   p.status));
+        }
         issued = j + 1;
       }
       if (bars->abort_flag) {
@@ -302,18 +382,22 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&map_v);
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j % ST;
-        const int use = j / ST;
+        const int st = j % VST;
+        const int use = j / VST;
         if (use > 0 && !mbar_wait(&bars->v_empty[st], (use - 1) & 1, wg)) break;
         mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kVOff + st * C::kTileBytes + c * kBoxBytes, &map_v, &bars->v_full[st], c * kChunk,
-                      g.k_row0 + j * kTile, g.kv_coord);
+        for (int c = 0; c < C::kChunks; ++c) {
+          const int r = g.k_row0 + j * kTile;
+          tma_load_3d_chk(smem + C::kVOff + st * C::kTileBytes + c * kBoxBytes, &map_v, &bars->v_full[st],
+                          c * kChunk, r, g.kv_coord,
+                          dbg_tile(c * kChunk, r, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv,
+                                   p.status));
+        }
         issued = j + 1;
       }
       if (bars->abort_flag) {
-        for (int j = (issued > ST ? issued - ST : 0); j < issued; ++j)
-          mbar_wait_drain(&bars->v_full[j % ST], (j / ST) & 1, kWaitLimitNs);
+        for (int j = (issued > VST ? issued - VST : 0); j < issued; ++j)
+          mbar_wait_drain(&bars->v_full[j % VST], (j / VST) & 1, kWaitLimitNs);
       }
     }
   } else if (warp == 9) {
@@ -343,7 +427,7 @@ __global__ void __launch_bounds__(384, 1)
       };
       // O_X += P_X(j) V_j, P_X(j) read from the S columns of tile X.
       auto issue_pv = [=](int x, int j) {
-        const uint64_t bv = dv0 + (uint64_t)(j % ST) * kTileDesc;
+        const uint64_t bv = dv0 + (uint64_t)(j % VST) * kTileDesc;
         const uint32_t p_tmem = tbase + (uint32_t)x * 128u;
         const uint32_t o_tmem = tbase + C::kOCol + (uint32_t)x * D;
 #pragma unroll
@@ -365,10 +449,10 @@ __global__ void __launch_bounds__(384, 1)
         umma_commit(&bars->k_empty[0]);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % ST;
+        const int vst = j % VST;
         const int j1 = j + 1;
         const int st1 = j1 % ST;
-        if (!(ok = mbar_wait(&bars->v_full[st], (j / ST) & 1, wg))) break;
+        if (!(ok = mbar_wait(&bars->v_full[vst], (j / VST) & 1, wg))) break;
         if (j < nA) {
           if (!(ok = mbar_wait(&bars->p_full[0], j & 1, wg))) break;
           tc_fence_after();
@@ -390,7 +474,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         if (j1 < n_kv) umma_commit(&bars->k_empty[st1]);
-        umma_commit(&bars->v_empty[st]);
+        umma_commit(&bars->v_empty[vst]);
       }
       // Every MMA issued completes before TMEM is released.
       umma_commit(&bars->drain);
@@ -415,7 +499,7 @@ __global__ void __launch_bounds__(384, 1)
       // (rows past S hold zeros and have no table row).
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, wg));
       const int qpos = qt * kTile + row;
-      if (ok && qpos < g.Sq)
+      if (ok && qpos < g.Sq && dbg_range((long long)qpos * (D / 2), D / 2, (long long)p.Sq * (D / 2), p.status))
         rope_rotate_row_smem<D>(smem + C::kQOff + x * C::kTileBytes, row, p.rope_cos + (size_t)qpos * (D / 2),
                                 p.rope_sin + (size_t)qpos * (D / 2), 1.f);
       fence_proxy_async_smem();
@@ -441,8 +525,13 @@ __global__ void __launch_bounds__(384, 1)
       int last = kTile - 1;
       if (diag) last = min(last, qpos + row - kv0);
       if (tail) last = min(last, g.Sk - kv0 - 1);
-      const bool masked = diag || tail;
-      const float mx = masked ? row_max<true>(r, last) : row_max<false>(r, last);
+      const bool masked = diag || tail;  // uniform over the CTA's tile
+      int lo = last, hi = last;
+      if (masked) {
+        lo = __reduce_min_sync(0xffffffffu, last);
+        hi = __reduce_max_sync(0xffffffffu, last);
+      }
+      const float mx = masked ? row_max_chunked(r, last, lo, hi) : row_max<false>(r, last);
       const float m_tile = mx * c;
       float alpha = 1.f;
       bool need = false;
@@ -454,7 +543,7 @@ __global__ void __launch_bounds__(384, 1)
         need = true;
       }
       const float neg_m = -m_ref;
-      const float rsum = masked ? exp_pack_store<true>(r, last, c, neg_m, s_tmem)
+      const float rsum = masked ? exp_pack_store_chunked(r, last, lo, hi, c, neg_m, s_tmem)
                                 : exp_pack_store<false>(r, last, c, neg_m, s_tmem);
       l = l * alpha + rsum;
 
@@ -502,7 +591,10 @@ __global__ void __launch_bounds__(384, 1)
           w.w = pack_bf16(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
           const int col = cc * 32 + u * 8;      // first column of the unit
           if (rowwise) {
-            if (qrow < g.Sq) *reinterpret_cast<uint4*>(orow + col) = w;
+            if (qrow < g.Sq &&
+                dbg_range(((long long)g.q_coord * p.Tq + g.q_row0 + qrow) * D + col, 8, (long long)heads_q * rows_q * D,
+                          p.status))
+              *reinterpret_cast<uint4*>(orow + col) = w;
           } else {
             const int unit = (col & 63) >> 3;     // unit within the 128-byte row of its box
             *reinterpret_cast<uint4*>(stage + (col >> 6) * kBoxBytes + row * 128 + ((unit ^ (row & 7)) << 4)) = w;
@@ -515,11 +607,14 @@ __global__ void __launch_bounds__(384, 1)
         ok = wg_barrier(&bars->wg_bar[x], wg_phase, wg);
         if (ok && row == 0) {
           for (int cb = 0; cb < C::kChunks; ++cb)
-            tma_store_3d(&map_o, stage + cb * kBoxBytes, cb * kChunk, g.q_row0 + qt * kTile, g.q_coord);
+            if (dbg_tile(cb * kChunk, g.q_row0 + qt * kTile, g.q_coord, D, kChunk, g.q_row0, g.q_row0 + g.Sq, heads_q,
+                         p.status))
+              tma_store_3d(&map_o, stage + cb * kBoxBytes, cb * kChunk, g.q_row0 + qt * kTile, g.q_coord);
           bulk_commit_group();
         }
       }
-      if (qrow < g.Sq) p.lse[g.lse_base + qrow] = (m_ref + __log2f(l)) * 0.69314718055994530942f;
+      if (qrow < g.Sq && dbg_range((long long)g.lse_base + qrow, 1, (long long)heads_q * rows_q, p.status))
+        p.lse[g.lse_base + qrow] = (m_ref + __log2f(l)) * 0.69314718055994530942f;
       if (!rowwise && row == 0) bulk_wait_group_read<0>();
     }
     tc_fence_before();
@@ -555,13 +650,11 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale_log2;
   p.status = a.status;
   auto kern = a.rope_cos ? fwd_kernel<D, true> : fwd_kernel<D, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) return e;
   // The setmaxnreg split must fit the registers the block is launched with, or the
-  // increase would wait forever: refuse to launch otherwise.
-  cudaFuncAttributes fa;
-  if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-  if (fa.numRegs * C::kThreads < 2 * 128 * C::kHighRegs + 128 * C::kLowRegs) return cudaErrorInvalidConfiguration;
+  // increase would wait forever: kernel_setup refuses the launch otherwise.
+  cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kern), C::kSmemBytes, C::kThreads,
+                               2 * 128 * C::kHighRegs + 128 * C::kLowRegs);
+  if (e != cudaSuccess) return e;
   // Packed batch: one row of CTAs per (sequence, head), enough pairs for the longest sequence.
   const int rows = a.cu_q ? a.max_seqlen_q : a.Sq;
   dim3 grid((unsigned)(a.B * a.Hq), (unsigned)ceil_div(rows, 2 * kTile));

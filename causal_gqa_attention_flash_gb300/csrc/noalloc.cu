@@ -51,8 +51,11 @@ cudaError_t noalloc_scratch(void** out) {
 extern "C" int gqa_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                                     const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
                                     int D, int causal, float scale, void* stream) {
+  // The codes gqa_attn_bwd itself returns for null pointers and rejected sizes or scales.
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return GQA_ERR_INVALID_ARG;
+  const int rc = gqa::check_common(B, Hq, Hkv, S, D, scale);
+  if (rc != GQA_OK) return rc;
   const size_t need = gqa_attn_bwd_workspace_size(B, Hq, Hkv, S, D);
-  if (need == 0) return GQA_ERR_INVALID_ARG;  // sizes gqa_attn_bwd would reject
   if (need > (size_t)GQA_NOALLOC_SCRATCH_BYTES) return GQA_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   const cudaError_t e = noalloc_scratch(&scratch);

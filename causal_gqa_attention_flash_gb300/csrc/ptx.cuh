@@ -15,6 +15,17 @@ namespace gqa {
 constexpr int STATUS_TIMEOUT = 1;
 constexpr int STATUS_MISALIGNED_SMEM = 2;
 constexpr int STATUS_BAD_SEQLENS = 4;  // a packed batch's sequence bounds are not a valid packing
+constexpr int STATUS_BOUNDS = 8;       // debug build: a computed coordinate fell outside its tensor
+
+// Debug builds (GQA_DEBUG defined) check every computed TMA coordinate and global index against
+// the extent of the tensor it addresses; a failed check sets STATUS_BOUNDS and the access is
+// skipped (a skipped TMA load still completes its transaction bytes, so no wait is left hanging).
+// In other builds every check is the constant true and compiles away.
+#ifdef GQA_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -107,6 +118,39 @@ __device__ __forceinline__ bool wg_barrier(uint64_t* bar, uint32_t& phase, const
   return ok;
 }
 
+// True, or (debug builds) false with STATUS_BOUNDS set when ok is false.
+__device__ __forceinline__ bool dbg_ok(bool ok, int* status) {
+  if constexpr (kDebugChecks) {
+    if (!ok) {
+      atomicOr(status, STATUS_BOUNDS);
+      return false;
+    }
+  }
+  return true;
+}
+
+// A tiled copy's coordinates against its tensor: the inner coordinate c0 starts a whole box of
+// box_inner elements inside [0, inner) on a box boundary, the tile's first row c1 lies in
+// [row_lo, row_hi) and the outer coordinate c2 in [0, outer).
+__device__ __forceinline__ bool dbg_tile(int c0, int c1, int c2, int inner, int box_inner, long long row_lo,
+                                         long long row_hi, int outer, int* status) {
+  if constexpr (!kDebugChecks) return true;
+  return dbg_ok(c0 >= 0 && c0 % box_inner == 0 && c0 + box_inner <= inner && c1 >= row_lo && c1 < row_hi &&
+                    c2 >= 0 && c2 < outer,
+                status);
+}
+
+// An index range [i, i + n) against [0, size).
+__device__ __forceinline__ bool dbg_range(long long i, long long n, long long size, int* status) {
+  if constexpr (!kDebugChecks) return true;
+  return dbg_ok(i >= 0 && n >= 0 && i + n <= size, status);
+}
+
+// Completes `bytes` transaction bytes on *bar without a copy (a debug build's skipped load).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA / bulk copies
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -121,6 +165,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// tma_load_3d when ok (a debug build's coordinate check passed); otherwise no copy, and the box's
+// bytes are completed on *bar so that its waiters go on (with stale data; the status says why).
+__device__ __forceinline__ void tma_load_3d_chk(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                                int c2, bool ok, uint32_t box_bytes = 16384) {
+  if (ok)
+    tma_load_3d(dst, map, bar, c0, c1, c2);
+  else
+    mbar_complete_tx(bar, box_bytes);
 }
 
 // 3-D tiled store shared -> global (bulk group). Out-of-range rows are not written.

@@ -16,7 +16,7 @@ namespace {
 // One thread per (row, group of 8 pairs).
 __global__ void __launch_bounds__(256) rope_rotate_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
                                                           const float* __restrict__ cs, const float* __restrict__ sn,
-                                                          long long rows, int S, int D) {
+                                                          long long rows, int S, int D, int* status) {
   const int groups = D / 16;
   const long long n = rows * groups;
   for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (long long)gridDim.x * blockDim.x) {
@@ -24,6 +24,9 @@ __global__ void __launch_bounds__(256) rope_rotate_kernel(const uint16_t* __rest
     const int gi = (int)(t - row * groups);
     const int p = (int)(row % S);
     const size_t base = (size_t)row * D + gi * 8;
+    if (!dbg_range((long long)base, D / 2 + 8, rows * D, status) ||
+        !dbg_range((long long)p * (D / 2) + gi * 8, 8, (long long)S * (D / 2), status))
+      continue;
     uint4 lo = *reinterpret_cast<const uint4*>(x + base);
     uint4 hi = *reinterpret_cast<const uint4*>(x + base + D / 2);
     const float* c = cs + (size_t)p * (D / 2) + gi * 8;
@@ -38,7 +41,8 @@ __global__ void __launch_bounds__(256) rope_rotate_kernel(const uint16_t* __rest
 // dQ = bf16(unrotate(scale * acc)), one thread per (row, group of 8 pairs).
 __global__ void __launch_bounds__(256) rope_convert_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
                                                            const float* __restrict__ cs, const float* __restrict__ sn,
-                                                           long long rows, int S, int D, float scale) {
+                                                           long long rows, int S, int D, float scale,
+                                                           int* status) {
   const int groups = D / 16;
   const long long n = rows * groups;
   for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (long long)gridDim.x * blockDim.x) {
@@ -46,6 +50,9 @@ __global__ void __launch_bounds__(256) rope_convert_kernel(const float* __restri
     const int gi = (int)(t - row * groups);
     const int p = (int)(row % S);
     const size_t base = (size_t)row * D + gi * 8;
+    if (!dbg_range((long long)base, D / 2 + 8, rows * D, status) ||
+        !dbg_range((long long)p * (D / 2) + gi * 8, 8, (long long)S * (D / 2), status))
+      continue;
     const float4 a0 = *reinterpret_cast<const float4*>(acc + base);
     const float4 a1 = *reinterpret_cast<const float4*>(acc + base + 4);
     const float4 b0 = *reinterpret_cast<const float4*>(acc + base + D / 2);
@@ -71,8 +78,7 @@ __global__ void __launch_bounds__(256) rope_convert_kernel(const float* __restri
 }
 
 int grid_for(long long n) {
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sm_count();
   const long long want = (n + 255) / 256;
   const long long cap = (long long)sms * 8;
   return (int)(want < 1 ? 1 : (want < cap ? want : cap));
@@ -81,20 +87,21 @@ int grid_for(long long n) {
 }  // namespace
 
 cudaError_t launch_rope_rotate(const void* x, void* y, const float* cs, const float* sn, long long rows, int S, int D,
-                               cudaStream_t stream) {
+                               int* status, cudaStream_t stream) {
   trace_begin(kKernelRope, stream);
   rope_rotate_kernel<<<grid_for(rows * (D / 16)), 256, 0, stream>>>(static_cast<const uint16_t*>(x),
-                                                                    static_cast<uint16_t*>(y), cs, sn, rows, S, D);
+                                                                    static_cast<uint16_t*>(y), cs, sn, rows, S, D,
+                                                                    status);
   cudaError_t e = cudaGetLastError();
   trace_end(kKernelRope, stream);
   return e;
 }
 
 cudaError_t launch_rope_convert(const float* acc, void* dq, const float* cs, const float* sn, long long rows, int S,
-                                int D, float scale, cudaStream_t stream) {
+                                int D, float scale, int* status, cudaStream_t stream) {
   trace_begin(kKernelBwdConvert, stream);
   rope_convert_kernel<<<grid_for(rows * (D / 16)), 256, 0, stream>>>(acc, static_cast<uint16_t*>(dq), cs, sn, rows,
-                                                                     S, D, scale);
+                                                                     S, D, scale, status);
   cudaError_t e = cudaGetLastError();
   trace_end(kKernelBwdConvert, stream);
   return e;

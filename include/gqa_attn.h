@@ -25,7 +25,7 @@
  * Causal: key j is visible to query i iff j <= i (queries and keys share the
  * length S). causal = 0 makes every key visible.
  * Supported: D in {64, 128}; any S >= 1; B, Hq, Hkv >= 1 with Hq % Hkv == 0;
- * B * Hq * ceil(S / 128) and B * Hkv * ceil(S / 128) below 2^31.
+ * B * Hq * ceil(S / 128) * 128 below 2^31.
  *
  * Ownership: the caller allocates and owns every buffer (device memory and
  * the stream). The library never allocates or frees device memory and never
@@ -42,7 +42,14 @@
  * fallback of any kind: a failure is an error code.
  *
  * Thread safety: entry points may be called concurrently from several host
- * threads. The device status word is shared by every call on a device.
+ * threads. Device-side errors are kept per stream (see gqa_attn_get_error).
+ *
+ * Profiling: every entry point and every kernel launch is bracketed by an
+ * NVTX range named after it (a no-op unless a profiling tool is attached).
+ *
+ * The self-test and tracing hooks used by this library's own tests and
+ * benchmark are declared in gqa_attn_testing.h; they are not part of this
+ * stable interface.
  */
 #ifndef GQA_ATTN_H
 #define GQA_ATTN_H
@@ -61,6 +68,11 @@ extern "C" {
 #define GQA_ERR_CUDA (-4)                /* a CUDA runtime/driver call failed; see gqa_attn_last_cuda_error() */
 #define GQA_ERR_TIMEOUT (-5)             /* a device-side wait gave up (reported by gqa_attn_get_error) */
 #define GQA_ERR_INTERNAL (-6)            /* a kernel's own layout check failed and it did no work (gqa_attn_get_error) */
+#define GQA_ERR_BOUNDS (-7)              /* debug build only: a computed coordinate fell outside its tensor (gqa_attn_get_error) */
+
+/* Device status words per device: one for each of the first GQA_STATUS_STREAMS - 1 streams that
+ * call into the library on that device; any further streams share one word. */
+#define GQA_STATUS_STREAMS 64
 
 /*
  * Forward: O = softmax(scale * Q K^T + causal mask) V and LSE per query row.
@@ -250,12 +262,18 @@ int gqa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void*
                         void* stream);
 
 /*
- * Synchronises `stream`, then reads and clears the device status word of the
- * current device. Returns GQA_OK, GQA_ERR_TIMEOUT if a kernel gave up on a
- * wait since the last call, GQA_ERR_INTERNAL if a kernel's own shared-memory
- * alignment check failed (it then returned without work), GQA_ERR_INVALID_ARG
- * if a packed batch's device-side sequence bounds were invalid (those
- * sequences were skipped), or GQA_ERR_CUDA if the stream reports an error.
+ * Synchronises `stream`, then reads and clears the status word of `stream` on
+ * the current device: the bits raised by kernels this library launched on
+ * that stream since the last call. Work on other streams is neither waited
+ * for nor reported (each of the first GQA_STATUS_STREAMS - 1 streams that call
+ * into the library on a device has a word of its own; streams beyond that
+ * share one word, and any of them may report, and clear, the others' bits).
+ * Returns GQA_OK, GQA_ERR_TIMEOUT if a kernel gave up on a wait,
+ * GQA_ERR_INTERNAL if a kernel's own shared-memory alignment check failed (it
+ * then returned without work), GQA_ERR_INVALID_ARG if a packed batch's
+ * device-side sequence bounds were invalid (those sequences were skipped),
+ * GQA_ERR_BOUNDS (debug build only) if a coordinate check failed (the access
+ * was skipped), or GQA_ERR_CUDA if the stream reports an error.
  */
 int gqa_attn_get_error(void* stream);
 
@@ -264,39 +282,6 @@ const char* gqa_attn_strerror(int code);
 
 /* The CUDA error code behind the last GQA_ERR_CUDA returned on this host thread (0 if none). */
 int gqa_attn_last_cuda_error(void);
-
-/*
- * Self-test of the bounded device wait (no counterpart on the pages): launches
- * one block that waits on an mbarrier nothing ever arrives at, with a limit of
- * limit_us microseconds (1..10^6). The kernel gives up, records the TIMEOUT
- * status bit and returns; a following gqa_attn_get_error() reports
- * GQA_ERR_TIMEOUT. It faults, traps or hangs nothing.
- */
-int gqa_attn_selftest_wait_timeout(int limit_us, void* stream);
-
-/*
- * Per-kernel tracing (no counterpart on the pages; used to time each kernel
- * of a call live, e.g. for a roofline). gqa_attn_trace_arm() arms the calling
- * host thread: every kernel that gqa_attn_fwd / gqa_attn_bwd then launch from
- * this thread is bracketed by two CUDA events recorded on the call's stream.
- * gqa_attn_trace_collect() disarms, waits for the last recorded event, and
- * writes, for each kernel kind k (GQA_KERNEL_*), launches[k] and total_ms[k]
- * (arrays of GQA_KERNEL_COUNT entries, host memory, owned by the caller).
- * Events are created on first use on the device current at that time and
- * reused afterwards; no device memory is allocated.
- */
-#define GQA_KERNEL_FWD 0
-#define GQA_KERNEL_BWD_PREP 1
-#define GQA_KERNEL_BWD_MAIN 2
-#define GQA_KERNEL_BWD_CONVERT 3
-#define GQA_KERNEL_DECODE_SPLIT 4
-#define GQA_KERNEL_DECODE_COMBINE 5 /* no longer launched: the last chunk's CTA merges the partials */
-#define GQA_KERNEL_BWD_DKDV 6 /* the deterministic backward's dK/dV kernel */
-#define GQA_KERNEL_BWD_DQ 7   /* the deterministic backward's query-major dQ kernel */
-#define GQA_KERNEL_ROPE 8     /* the rotary embedding's rotation pass */
-#define GQA_KERNEL_COUNT 9
-int gqa_attn_trace_arm(void);
-int gqa_attn_trace_collect(int* launches, double* total_ms);
 
 /*
  * Backward without caller-provided workspace and without any allocation (the

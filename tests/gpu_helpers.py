@@ -24,8 +24,9 @@ TOL_GRAD_ABS_FLOOR = 1e-5
 def gqa():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    from causal_gqa_attention_flash_gb300 import _lib
     from causal_gqa_attention_flash_gb300.build import build_library
-    build_library()
+    build_library(debug=_lib.DEBUG)  # the variant the binding loads (GQA_ATTN_DEBUG=1: the checking build)
     import causal_gqa_attention_flash_gb300 as g
     return g
 

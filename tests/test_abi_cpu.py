@@ -9,12 +9,16 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gqa_attn.h")
+# the stable interface and the hooks of the library's own tests and benchmark
+HEADERS = [HEADER, os.path.join(ROOT, "include", "gqa_attn_testing.h")]
+
+
+def _header_sources():
+    return "\n".join(re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S) for h in HEADERS)
 
 
 def _declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(gqa_attn_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(gqa_attn_[a-z_]+)\s*\(", _header_sources())))
 
 
 @pytest.fixture(scope="module")
@@ -26,10 +30,13 @@ def lib():
 
 
 def test_header_declares_the_boundary():
-    names = _declared_functions()
+    stable = re.findall(r"\b(gqa_attn_[a-z_]+)\s*\(", re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S))
     for n in ("gqa_attn_fwd", "gqa_attn_bwd", "gqa_attn_bwd_workspace_size", "gqa_attn_get_error",
               "gqa_attn_strerror"):
-        assert n in names
+        assert n in stable
+    # the testing hooks live outside the stable header
+    for n in ("gqa_attn_selftest_wait_timeout", "gqa_attn_trace_arm", "gqa_attn_trace_collect"):
+        assert n not in stable and n in _declared_functions()
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -43,7 +50,7 @@ def test_binding_declares_every_symbol():
 
 
 def _declared_arities():
-    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    src = _header_sources()
     out = {}
     for name, params in re.findall(r"\b(gqa_attn_[a-z_]+)\s*\(([^)]*)\)\s*;", src):
         params = params.strip()
@@ -61,8 +68,9 @@ def test_binding_arities_match_the_header():
 
 
 def test_strerror_and_workspace_size(lib):
-    for code in (0, -1, -2, -3, -4, -5, -99):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -99):
         assert isinstance(lib.gqa_attn_strerror(code), bytes)
+    assert b"debug build" in lib.gqa_attn_strerror(-7)
     assert lib.gqa_attn_bwd_workspace_size(1, 4, 2, 128, 96) == 0
     assert lib.gqa_attn_bwd_workspace_size(1, 4, 3, 128, 64) == 0
     n = lib.gqa_attn_bwd_workspace_size(2, 32, 8, 16384, 128)
@@ -87,6 +95,65 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.gqa_attn_bwd(*args, 0, 1, 4, 2, 128, 64, 1, 0.125, None) == -3
     assert lib.gqa_attn_bwd(*args[:9], A + 128, 1 << 30, 1, 4, 2, 128, 64, 1, 0.125, None) == -1
     assert lib.gqa_attn_selftest_wait_timeout(0, None) == -1
+
+
+def test_noalloc_returns_the_codes_of_the_workspace_backward(lib):
+    """Rejected sizes give the same code from gqa_attn_bwd_noalloc as from gqa_attn_bwd (no CUDA call)."""
+    A = 1 << 20
+    for (B, Hq, Hkv, S, D, scale, code) in ((1, 4, 2, 128, 96, 0.125, -2), (1, 4, 3, 128, 64, 0.125, -1),
+                                             (0, 4, 2, 128, 64, 0.125, -1), (1, 4, 2, 128, 64, float("nan"), -1),
+                                             (1, 4, 2, 128 * 65536, 64, 0.125, -2)):
+        assert lib.gqa_attn_bwd(*([A] * 10), 1 << 40, B, Hq, Hkv, S, D, 1, scale, None) == code
+        assert lib.gqa_attn_bwd_noalloc(*([A] * 9), B, Hq, Hkv, S, D, 1, scale, None) == code
+    assert lib.gqa_attn_bwd_noalloc(None, *([A] * 8), 1, 4, 2, 128, 64, 1, 0.125, None) == -1
+
+
+def test_padded_row_count_is_bounded(lib):
+    """B * Hq * (S rounded up to the 128-row tile) indexes the backward's padded rows in 32 bits."""
+    A = 1 << 20
+    # S = 1 pads to 128 rows: 2^24 heads x 128 rows = 2^31 padded rows, refused
+    assert lib.gqa_attn_fwd(A, A, A, A, A, 1 << 12, 1 << 12, 1 << 12, 1, 64, 1, 0.125, None) == -2
+    assert lib.gqa_attn_bwd_workspace_size(1 << 12, 1 << 12, 1 << 12, 1, 64) == 0
+
+
+def _fake_cuda():
+    torch = pytest.importorskip("torch")
+    from torch._subclasses.fake_tensor import FakeTensorMode
+    return torch, FakeTensorMode()
+
+
+def test_binding_checks_caller_buffers_before_any_launch():
+    """Every caller-supplied buffer is checked in Python before the library is called: wrong shape,
+    dtype or contiguity of an output raises ValueError (checked on fake CUDA tensors, no GPU)."""
+    torch, mode = _fake_cuda()
+    import causal_gqa_attention_flash_gb300 as g
+    with mode:
+        q = torch.empty(1, 4, 128, 64, device="cuda", dtype=torch.bfloat16)
+        k = torch.empty(1, 2, 128, 64, device="cuda", dtype=torch.bfloat16)
+        lse = torch.empty(1, 4, 128, device="cuda", dtype=torch.float32)
+        bad = {
+            "dq shape": dict(dq=torch.empty(1, 4, 128, 32, device="cuda", dtype=torch.bfloat16)),
+            "dq dtype": dict(dq=torch.empty(1, 4, 128, 64, device="cuda", dtype=torch.float16)),
+            "dk shape": dict(dk=torch.empty(1, 4, 128, 64, device="cuda", dtype=torch.bfloat16)),
+            "dv strided": dict(dv=torch.empty(1, 2, 64, 128, device="cuda", dtype=torch.bfloat16).transpose(2, 3)),
+            "workspace dtype": dict(workspace=torch.empty(1 << 20, device="cuda", dtype=torch.float32)),
+        }
+        for what, kw in bad.items():
+            with pytest.raises(ValueError):
+                g.gqa_attn_bwd(q, k, k, q, q, lse, **kw)
+        with pytest.raises(ValueError):
+            g.gqa_attn_bwd(q, k, k, q, q, torch.empty(1, 4, 127, device="cuda"))  # lse shape
+        with pytest.raises(ValueError):
+            g.gqa_attn_fwd(q, k, k, o=torch.empty(1, 4, 128, 64, device="cuda", dtype=torch.float32))
+        with pytest.raises(ValueError):
+            g.gqa_attn_fwd(q, k, k, lse=torch.empty(1, 4, 128, device="cuda", dtype=torch.float64))
+        with pytest.raises(ValueError):
+            g.gqa_attn_bwd_noalloc(q, k, k, q, q, lse, q, k, torch.empty(1, 2, 128, 32, device="cuda",
+                                                                      dtype=torch.bfloat16))
+        with pytest.raises(ValueError):
+            g.gqa_attn_decode_fwd(q[:, :, :1].contiguous(), k, k, lse=torch.empty(1, 4, 2, device="cuda"))
+        with pytest.raises(ValueError):  # CPU output for CUDA inputs
+            g.gqa_attn_fwd(q, k, k, o=torch.empty(1, 4, 128, 64, dtype=torch.bfloat16))
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):

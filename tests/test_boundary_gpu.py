@@ -70,3 +70,24 @@ def test_runs_on_a_side_stream():
     torch.cuda.synchronize()
     assert torch.equal(o0, o1) and torch.equal(l0, l1)
     assert torch.equal(r0[1], r1[1]) and torch.equal(r0[2], r1[2])
+
+
+def test_status_is_per_stream():
+    """A wait that gives up on stream A is reported by gqa_attn_get_error(A) only: stream B, which
+    ran ordinary work meanwhile, reports OK, and A's word is cleared by reading it."""
+    g = gqa()
+    from gqa_inputs import make_inputs
+    a, b = torch.cuda.Stream(), torch.cuda.Stream()
+    q, k, v, _ = (t.cuda() if t is not None else None for t in make_inputs(1, 4, 2, 200, 64, seed=5, with_do=False))
+    torch.cuda.synchronize()
+    assert g.gqa_attn_get_error(a) == 0 and g.gqa_attn_get_error(b) == 0
+    g.gqa_attn_selftest_wait_timeout(2000, stream=a)
+    with torch.cuda.stream(b):
+        o, lse = g.gqa_attn_fwd(q, k, v, stream=b)
+    assert g.gqa_attn_get_error(b) == 0
+    assert g.gqa_attn_get_error(a) == g.GQA_ERR_TIMEOUT
+    assert g.gqa_attn_get_error(a) == 0
+    assert g.gqa_attn_get_error() == 0  # the current stream's word was never touched
+    torch.cuda.synchronize()
+    o_ref, lse_ref = g.gqa_attn_fwd(q, k, v)
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
