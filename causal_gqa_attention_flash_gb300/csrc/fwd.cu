@@ -60,8 +60,8 @@ struct FwdCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 256;
   static constexpr int kLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
-  static constexpr int kLowRegs = 80;
-  static constexpr int kHighRegs = 208;
+  static constexpr int kLowRegs = 104;
+  static constexpr int kHighRegs = 200;
   static_assert(2 * 128 * kHighRegs + 128 * kLowRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 };
 
