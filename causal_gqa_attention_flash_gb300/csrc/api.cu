@@ -351,7 +351,7 @@ int gqa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
 
 size_t gqa_attn_bwd_workspace_size(int B, int Hq, int Hkv, int S, int D) {
   if (check_common(B, Hq, Hkv, S, D, 1.0f) != GQA_OK) return 0;
-  return bwd_workspace_layout(B, Hq, S, D).total;
+  return bwd_workspace_layout(B, Hq, Hkv, S, D).total;
 }
 
 }  // extern "C"
@@ -368,7 +368,7 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
     return GQA_ERR_INVALID_ARG;
-  const BwdWorkspace ws = bwd_workspace_layout(B, Hq, S, D);
+  const BwdWorkspace ws = bwd_workspace_layout(B, Hq, Hkv, S, D);
   if (workspace_bytes < ws.total) return GQA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   CUtensorMap mq, mk, mv, mdo, macc, mdq;
@@ -402,6 +402,8 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
   a.dvec = reinterpret_cast<float*>(wsb + ws.dvec_off);
   a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
   a.dq_acc = reinterpret_cast<float*>(wsb + ws.dqacc_off);
+  a.part = reinterpret_cast<float*>(wsb + ws.part_off);
+  a.tickets = reinterpret_cast<unsigned*>(wsb + ws.ticket_off);
   a.cu = nullptr;
   a.max_seqlen = 0;
   a.B = B;
@@ -440,7 +442,7 @@ int gqa_attn_bwd_deterministic(const void* q, const void* k, const void* v, cons
 
 size_t gqa_attn_bwd_rope_workspace_size(int B, int Hq, int Hkv, int S, int D) {
   if (check_common(B, Hq, Hkv, S, D, 1.0f) != GQA_OK) return 0;
-  return bwd_workspace_layout(B, Hq, S, D).total + align256((size_t)B * Hq * S * D * 2);
+  return bwd_workspace_layout(B, Hq, Hkv, S, D).total + align256((size_t)B * Hq * S * D * 2);
 }
 
 int gqa_attn_bwd_rope(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
@@ -456,7 +458,7 @@ int gqa_attn_bwd_rope(const void* q, const void* k, const void* v, const void* o
   if (workspace_bytes < gqa_attn_bwd_rope_workspace_size(B, Hq, Hkv, S, D)) return GQA_ERR_WORKSPACE_TOO_SMALL;
   // The queries are re-read by every key tile that sees them: rotate them once, after the
   // backward's own workspace sections.
-  const size_t bwd_bytes = bwd_workspace_layout(B, Hq, S, D).total;
+  const size_t bwd_bytes = bwd_workspace_layout(B, Hq, Hkv, S, D).total;
   void* q_rot = static_cast<uint8_t*>(workspace) + bwd_bytes;
   int* status = nullptr;
   cudaError_t e = status_ptr(stream, &status);
@@ -522,6 +524,8 @@ int gqa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void*
   a.dvec = reinterpret_cast<float*>(wsb + ws.dvec_off);
   a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
   a.dq_acc = reinterpret_cast<float*>(wsb + ws.dqacc_off);
+  a.part = nullptr;  // packed batches split no key tile
+  a.tickets = nullptr;
   a.cu = cu_seqlens;
   a.max_seqlen = max_seqlen;
   a.B = nseq;

@@ -25,6 +25,12 @@
 // then holds its packed bf16 P^T in [64h, 64h+32) and dS^T in [64h+32, 64h+64),
 // written only by the warpgroup that read those S^T columns; [128,256) dP^T
 // f32, then the dQ partial f32 [128, 128+D); [256,256+D) dV; [256+D,256+2D) dK.
+#include <algorithm>
+#include <functional>
+#include <mutex>
+#include <queue>
+#include <vector>
+
 #include "common.h"
 #include "ptx.cuh"
 #include "rope.cuh"
@@ -49,7 +55,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
                                                        const float* __restrict__ lse, float* __restrict__ dvec,
                                                        float* __restrict__ lse2, float* __restrict__ dq_acc,
                                                        int rows_total, int rows_valid, int S, int S_pad,
-                                                       float log2e, long long acc_vec4, int* status) {
+                                                       float log2e, long long acc_vec4, unsigned* tickets,
+                                                       int n_tickets, int* status) {
   constexpr int TPR = D / 8;            // threads per row
   constexpr int RPW = 32 / TPR;          // rows per warp and iteration
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
@@ -87,6 +94,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
   }
   float4* acc4 = reinterpret_cast<float4*>(dq_acc);
   for (long long i = gtid; i < acc_vec4; i += nthreads) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = gtid; i < n_tickets; i += nthreads) tickets[i] = 0u;  // split key tiles' arrival counters
 }
 
 // ------------------------------------------------------------------ convert
@@ -136,8 +144,10 @@ struct BwdBars {
   uint64_t qdo_empty[ST];
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free, stage_full, dkv_done, drain;
   uint64_t k_ready;  // rotary embedding: the key tile rotated in shared memory
+  uint64_t epi_bar;  // split key tiles: barrier of the element-wise warps around the partials' ticket
   uint32_t tmem_base;
   int abort_flag;
+  int last;          // split key tiles: this part arrived last and adds the parts up
 };
 
 static_assert(sizeof(BwdBars<BwdCfg<64>::kStages>) <= 256 && sizeof(BwdBars<BwdCfg<128>::kStages>) <= 256,
@@ -155,11 +165,34 @@ struct BwdKParams {
   int Hq, Hkv, S, S_pad, causal, max_seqlen;
   int n_ktiles;   // packed batch: key tiles of the longest sequence (the 1-D grid's inner extent)
   int rows_total; // rows of the D / LSE2 arrays (padding included)
+  // Dense batches with split key tiles (cap > 0): grid y enumerates each group's (key tile, part)
+  // pairs, ctas_per_group of them; a group keeps parts_per_group f32 dK / dV partials in `part`.
+  int cap, ctas_per_group, parts_per_group;
+  float* part;
+  unsigned* tickets;
   float scale, scale_log2;
   int* status;
   const float* rope_cos;  // rotary tables [S, D/2] (nullptr: none): K is rotated in shared memory,
   const float* rope_sin;  // the queries arrive rotated, dK is turned back in the epilogue
 };
+
+// Position of grid row x among a group's (key tile, part) pairs when key tiles are split (see
+// BwdSplit): key tile jt has ceil(steps(jt) / cap) parts; pidx is the index of the tile's first
+// partial among the group's partials (only split key tiles keep partials).
+struct SplitPos {
+  int jt, part, parts, pidx;
+};
+
+__device__ __forceinline__ SplitPos split_pos(int x, int n_tiles, int G, int causal, int cap) {
+  int pidx = 0;
+  for (int jt = 0; jt < n_tiles; ++jt) {
+    const int parts = (G * (causal ? n_tiles - jt : n_tiles) + cap - 1) / cap;
+    if (x < parts) return SplitPos{jt, x, parts, pidx};
+    x -= parts;
+    if (parts > 1) pidx += parts;
+  }
+  return SplitPos{n_tiles, 0, 1, 0};  // past the plan (no such grid row is launched)
+}
 
 // One CTA per (batch, KV head, 128-key tile jt), 352 threads:
 //   warps 0..7  element-wise work. Warp w owns TMEM lane quarter w % 4 (key
@@ -207,9 +240,12 @@ __global__ void __launch_bounds__(352, 1)
   // tiles consecutively, so that a sequence's key tiles run together and share its Q, dO and
   // dQ-accumulator tiles in L2; with the groups fastest, a wave would hold about one key tile of
   // every sequence and nearly every load and reduce-add would go to DRAM.
-  const int jt = kPacked ? (int)(blockIdx.x % (unsigned)p.n_ktiles) : (int)blockIdx.y;
-  const int grp = kPacked ? (int)(blockIdx.x / (unsigned)p.n_ktiles) : (int)blockIdx.x;
+  // Dense batches with split key tiles: grid y is the (key tile, part) pair of the group.
   const int G = p.Hq / p.Hkv;
+  SplitPos sp{kPacked ? (int)(blockIdx.x % (unsigned)p.n_ktiles) : (int)blockIdx.y, 0, 1, 0};
+  if (!kPacked && p.cap > 0) sp = split_pos((int)blockIdx.y, p.n_ktiles, G, p.causal, p.cap);
+  const int jt = sp.jt;
+  const int grp = kPacked ? (int)(blockIdx.x / (unsigned)p.n_ktiles) : (int)blockIdx.x;
   const int b = grp / p.Hkv;  // batch entry (dense) or sequence (packed)
   const int hkv = grp - b * p.Hkv;
   // L rows in this CTA's sequence, starting at row0 of the tensor maps; the KV head's map
@@ -239,7 +275,10 @@ __global__ void __launch_bounds__(352, 1)
   const int n_tiles = (L + kTile - 1) / kTile;
   const int i_start = p.causal ? jt : 0;
   const int n_i = n_tiles - i_start;
-  const int n_steps = G * n_i;
+  // Steps t_begin .. t_begin + n_steps - 1 of the key tile's G * n_i (query head, query tile)
+  // steps; the loops below count t from 0, step t being the key tile's step t_begin + t.
+  const int t_begin = (int)((long long)sp.part * (G * n_i) / sp.parts);
+  const int n_steps = (int)((long long)(sp.part + 1) * (G * n_i) / sp.parts) - t_begin;
   // D / LSE2 rows of query tile i of query head bhq0 + hl: copied from the 16-byte aligned row
   // below (the copy is 4 rows wider when a packed sequence starts off a multiple of 4 rows).
   constexpr int n_rowfl = kPacked ? kTile + 4 : kTile;
@@ -262,6 +301,7 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(&bars->dkv_done, 1);
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->k_ready, 8);
+    mbar_init(&bars->epi_bar, 8);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -294,8 +334,8 @@ __global__ void __launch_bounds__(352, 1)
         const int st = t % ST;
         const int use = t / ST;
         if (use > 0 && !mbar_wait(&bars->qdo_empty[st], (use - 1) & 1, wg)) break;
-        const int hl = t / n_i;
-        const int i = i_start + (t - hl * n_i);
+        const int hl = (t_begin + t) / n_i;
+        const int i = i_start + (t_begin + t - hl * n_i);
         const int bhq = bhq0 + hl;
         uint64_t* bar = &bars->qdo_full[st];
         mbar_arrive_expect_tx(bar, 2 * C::kTileBytes + 2 * n_rowfl * 4);
@@ -409,8 +449,8 @@ __global__ void __launch_bounds__(352, 1)
       for (int t = 0; t < n_steps; ++t) {
         if (!mbar_wait(&bars->stage_full, t & 1, wg)) break;
         const int st = t % ST;
-        const int hl = t / n_i;
-        const int i = i_start + (t - hl * n_i);
+        const int hl = (t_begin + t) / n_i;
+        const int i = i_start + (t_begin + t - hl * n_i);
         const int bhq = bhq0 + hl;
 #pragma unroll
         for (int s2 = 0; s2 < D / 32; ++s2) {
@@ -451,8 +491,8 @@ __global__ void __launch_bounds__(352, 1)
     }
     for (int t = 0; t < n_steps; ++t) {
       const int st = t % ST;
-      const int hl = t / n_i;
-      const int i = i_start + (t - hl * n_i);
+      const int hl = (t_begin + t) / n_i;
+      const int i = i_start + (t_begin + t - hl * n_i);
       const int roff = kPacked ? (int)(rows_at(hl, i) & 3) : 0;  // the rows' offset within their widened copy
       const float* slse = reinterpret_cast<const float*>(smem + C::kRowOff) + st * 2 * C::kRowFl + roff + hf * 64;
       const float* sdv = slse + C::kRowFl;
@@ -609,7 +649,83 @@ __global__ void __launch_bounds__(352, 1)
         }
       }
     }
-    if (ok) {
+    if (ok && sp.parts > 1) {
+      // Split key tile: this part's f32 dK (unscaled) and dV go to its partial slot; the part that
+      // takes the last ticket adds all parts in part order and writes dK, dV.
+      tc_fence_after();
+      constexpr size_t kSlot = (size_t)kTile * D * 2;  // a partial: dV [128][D], then dK [128][D]
+      float* slots = p.part + ((size_t)grp * p.parts_per_group + sp.pidx) * kSlot;
+      const size_t slot_end = (size_t)gridDim.x * p.parts_per_group * kSlot;  // the partials' extent
+#pragma unroll
+      for (int q = 0; q < D / 64; ++q) {
+        const int col = hf * (D / 2) + q * 32;
+        uint32_t dv[32], dk[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kDVCol + col, dv);
+        tmem_ld_32x32b_x32(tbase + lane_off + C::kDKCol + col, dk);
+        tmem_wait_ld_x32(dv);
+        tmem_wait_ld_x32(dk);
+        const size_t at = (size_t)sp.part * kSlot + (size_t)row * D + col;
+        if (kv_valid &&
+            dbg_range((long long)(slots - p.part) + (long long)at, (long long)kTile * D + 32, (long long)slot_end,
+                      p.status)) {
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            *reinterpret_cast<float4*>(slots + at + 4 * x) =
+                make_float4(__uint_as_float(dv[4 * x]), __uint_as_float(dv[4 * x + 1]), __uint_as_float(dv[4 * x + 2]),
+                            __uint_as_float(dv[4 * x + 3]));
+            *reinterpret_cast<float4*>(slots + at + (size_t)kTile * D + 4 * x) =
+                make_float4(__uint_as_float(dk[4 * x]), __uint_as_float(dk[4 * x + 1]), __uint_as_float(dk[4 * x + 2]),
+                            __uint_as_float(dk[4 * x + 3]));
+          }
+        }
+      }
+      // Every element-wise thread's partial stores precede thread 0's fence and ticket (the barrier
+      // orders them within the CTA, the fence is cumulative); the last part's fence after its ticket
+      // orders the other parts' stores before the reads that follow the second barrier.
+      uint32_t ephase = 0;
+      ok = wg_barrier(&bars->epi_bar, ephase, wg);
+      if (ok && tid == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(p.tickets + (size_t)grp * p.n_ktiles + jt, 1u);
+        bars->last = (prev == (unsigned)sp.parts - 1u) ? 1 : 0;
+        __threadfence();
+      }
+      if (ok) ok = wg_barrier(&bars->epi_bar, ephase, wg);
+      if (ok && bars->last && kv_valid) {
+        const size_t orow = ((size_t)kv_coord * p.S + row0 + kv_row) * D;
+#pragma unroll
+        for (int q = 0; q < D / 64; ++q) {
+          const int col = hf * (D / 2) + q * 32;
+          float sv[32], sk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sv[e] = sk[e] = 0.f;
+          for (int pp = 0; pp < sp.parts; ++pp) {  // part order, whichever part arrived last
+            const float* src = slots + (size_t)pp * kSlot + (size_t)row * D + col;
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              const float4 a = __ldcg(reinterpret_cast<const float4*>(src) + x);
+              const float4 b = __ldcg(reinterpret_cast<const float4*>(src + (size_t)kTile * D) + x);
+              sv[4 * x] += a.x; sv[4 * x + 1] += a.y; sv[4 * x + 2] += a.z; sv[4 * x + 3] += a.w;
+              sk[4 * x] += b.x; sk[4 * x + 1] += b.y; sk[4 * x + 2] += b.z; sk[4 * x + 3] += b.w;
+            }
+          }
+          if (dbg_range((long long)orow + col, 32, (long long)heads_kv * p.S * D, p.status)) {
+            uint4* dstv = reinterpret_cast<uint4*>(p.dv + orow + col);
+            uint4* dstk = reinterpret_cast<uint4*>(p.dk + orow + col);
+            const float sc = p.scale;
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              dstv[x] = make_uint4(pack_bf16(sv[8 * x], sv[8 * x + 1]), pack_bf16(sv[8 * x + 2], sv[8 * x + 3]),
+                                   pack_bf16(sv[8 * x + 4], sv[8 * x + 5]), pack_bf16(sv[8 * x + 6], sv[8 * x + 7]));
+              dstk[x] = make_uint4(pack_bf16(sk[8 * x] * sc, sk[8 * x + 1] * sc),
+                                   pack_bf16(sk[8 * x + 2] * sc, sk[8 * x + 3] * sc),
+                                   pack_bf16(sk[8 * x + 4] * sc, sk[8 * x + 5] * sc),
+                                   pack_bf16(sk[8 * x + 6] * sc, sk[8 * x + 7] * sc));
+            }
+          }
+        }
+      }
+    } else if (ok) {
       tc_fence_after();
       const size_t orow = ((size_t)kv_coord * p.S + row0 + kv_row) * D;
 #pragma unroll
@@ -650,6 +766,86 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
+// Plan selection for the split backward. The time of a CTA is modelled as its steps plus a fixed
+// cost of kCtaOverheadSteps steps (prologue, epilogue, partials; measured on GB300 at D = 64: a
+// 16-step CTA takes ~43 us, two 4-step CTAs in a row ~34 us), CTAs are dealt longest first onto
+// kPlanCtas SMs (the order of the grid), and the cap with the shortest estimated makespan wins if
+// it beats the unsplit grid by kSplitGain. Only grids of at most two waves are considered.
+constexpr int kPlanCtas = 152;  // a GB300's SM count: the plan, and the workspace, do not depend on the device
+constexpr int kCtaOverheadSteps = 4;
+constexpr double kSplitGain = 1.15;
+
+long long bwd_plan_makespan(int B, int Hkv, int G, int n_tiles, int causal, int cap) {
+  std::vector<int> sizes;
+  for (int jt = 0; jt < n_tiles; ++jt) {
+    const int steps = bwd_tile_steps(jt, n_tiles, G, causal);
+    const int parts = cap > 0 ? ceil_div(steps, cap) : 1;
+    for (int pp = 0; pp < parts; ++pp) {
+      const int sz = (int)((long long)(pp + 1) * steps / parts - (long long)pp * steps / parts);
+      for (int g = 0; g < B * Hkv; ++g) sizes.push_back(sz + kCtaOverheadSteps);
+    }
+  }
+  std::sort(sizes.begin(), sizes.end(), std::greater<int>());
+  std::priority_queue<long long, std::vector<long long>, std::greater<long long>> load;
+  for (int i = 0; i < kPlanCtas; ++i) load.push(0);
+  long long span = 0;
+  for (int sz : sizes) {
+    const long long t = load.top() + sz;
+    load.pop();
+    load.push(t);
+    span = t > span ? t : span;
+  }
+  return span;
+}
+
+BwdSplit bwd_split_plan_uncached(int B, int Hkv, int G, int n_tiles, int causal) {
+  BwdSplit sp{0, n_tiles, 0};
+  const int steps0 = bwd_tile_steps(0, n_tiles, G, causal);
+  if ((long long)B * Hkv * n_tiles > 2ll * kPlanCtas || steps0 < 2) return sp;
+  const long long unsplit = bwd_plan_makespan(B, Hkv, G, n_tiles, causal, 0);
+  long long best = unsplit;
+  int best_cap = 0;
+  for (int cap = steps0 - 1; cap >= 1; --cap) {
+    const long long m = bwd_plan_makespan(B, Hkv, G, n_tiles, causal, cap);
+    if (m < best) {
+      best = m;
+      best_cap = cap;
+    }
+  }
+  if (best_cap == 0 || (double)best * kSplitGain > (double)unsplit) return sp;
+  sp.cap = best_cap;
+  sp.ctas_per_group = 0;
+  for (int jt = 0; jt < n_tiles; ++jt) {
+    const int parts = ceil_div(bwd_tile_steps(jt, n_tiles, G, causal), sp.cap);
+    sp.ctas_per_group += parts;
+    if (parts > 1) sp.parts_per_group += parts;
+  }
+  return sp;
+}
+
+}  // namespace
+
+BwdSplit bwd_split_plan(int B, int Hkv, int G, int n_tiles, int causal) {
+  struct Entry {
+    int key[5];
+    BwdSplit plan;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  const int key[5] = {B, Hkv, G, n_tiles, causal ? 1 : 0};
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry& e : cache)
+      if (std::equal(key, key + 5, e.key)) return e.plan;
+  }
+  const BwdSplit plan = bwd_split_plan_uncached(B, Hkv, G, n_tiles, causal);
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache.size() < 256) cache.push_back(Entry{{key[0], key[1], key[2], key[3], key[4]}, plan});
+  return plan;
+}
+
+namespace {
+
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
@@ -661,6 +857,11 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   const int rows_total = packed ? rows_valid + kRowPad : rows_valid;
   const long long acc_elems = det ? 0 : (long long)(packed ? 1 : a.B) * a.Hq * a.S * D;
   const int sms = device_sm_count();
+  // A small dense problem has its heaviest key tiles split across CTAs (BwdSplit); the rotary
+  // variant, which turns dK back in the epilogue, and packed batches are not split.
+  const BwdSplit split = (!packed && !a.rope_cos) ? bwd_split_plan(a.B, a.Hkv, a.Hq / a.Hkv, n_tiles, a.causal)
+                                                  : BwdSplit{0, n_tiles, 0};
+  const int n_tickets = split.cap > 0 ? a.B * a.Hkv * n_tiles : 0;
   {
     const int threads = 256;
     long long want = ((long long)rows_total * (D / 8) + threads - 1) / threads;
@@ -668,7 +869,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     trace_begin(kKernelBwdPrep, stream);
     bwd_prep_kernel<D><<<blocks, threads, 0, stream>>>(
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse, a.dvec, a.lse2, a.dq_acc,
-        rows_total, rows_valid, a.S, S_pad, 1.4426950408889634f, acc_elems / 4, a.status);
+        rows_total, rows_valid, a.S, S_pad, 1.4426950408889634f, acc_elems / 4, a.tickets, n_tickets, a.status);
     cudaError_t e = cudaGetLastError();
     trace_end(kKernelBwdPrep, stream);
     if (e != cudaSuccess) return e;
@@ -688,6 +889,11 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     p.max_seqlen = a.max_seqlen;
     p.n_ktiles = n_tiles;
     p.rows_total = rows_total;
+    p.cap = split.cap;
+    p.ctas_per_group = split.ctas_per_group;
+    p.parts_per_group = split.parts_per_group;
+    p.part = a.part;
+    p.tickets = a.tickets;
     p.rope_cos = a.rope_cos;
     p.rope_sin = a.rope_sin;
     p.scale = a.scale;
@@ -701,7 +907,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const long long packed_ctas = (long long)a.B * a.Hkv * n_tiles;
     if (packed && packed_ctas >= (1ll << 31)) return cudaErrorInvalidValue;
-    const dim3 grid = packed ? dim3((unsigned)packed_ctas) : dim3((unsigned)(a.B * a.Hkv), (unsigned)n_tiles);
+    const dim3 grid = packed ? dim3((unsigned)packed_ctas)
+                             : dim3((unsigned)(a.B * a.Hkv), (unsigned)(split.cap > 0 ? split.ctas_per_group : n_tiles));
     trace_begin(kind, stream);
     kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_do, *a.map_dqacc, p);
     e = cudaGetLastError();

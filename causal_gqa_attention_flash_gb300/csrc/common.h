@@ -55,6 +55,8 @@ struct BwdArgs {
   float* dvec;                 // f32 [B*Hq, S_pad]: D_i = rowsum(dO * O)
   float* lse2;                 // f32 [B*Hq, S_pad]: LSE * log2(e), +inf past S
   float* dq_acc;               // f32 [B*Hq, S, D]
+  float* part;                 // split key tiles' f32 dK / dV partials (dense batches; see BwdSplit)
+  unsigned* tickets;           // [B*Hkv*ceil(S/128)] arrival counters of the split key tiles' parts
   const int* cu;               // packed batch: device int32 [B + 1] sequence bounds; nullptr = dense
   int max_seqlen;              // packed batch: bound on every sequence's length
   int deterministic;           // 1: dQ by the query-major kernel (dense batches only)
@@ -89,18 +91,45 @@ struct DecodeArgs {
 
 // Workspace sections of the backward (byte offsets, each 256-aligned).
 struct BwdWorkspace {
-  size_t dvec_off, lse2_off, dqacc_off, total;
+  size_t dvec_off, lse2_off, dqacc_off, part_off, ticket_off, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline BwdWorkspace bwd_workspace_layout(int B, int Hq, int S, int D) {
+// Split of the dense backward's key tiles. A key tile's CTA works through G * (visible query tiles)
+// steps; when the problem is small, the key tiles with the most steps are cut into parts of at
+// most `cap` consecutive steps, each part a CTA of its own, so that the grid fills the machine and
+// no CTA is much longer than the others. Each part of a split key tile writes its f32 dK / dV
+// partial to the workspace; the part that finishes last adds the parts up in part order (the
+// result does not depend on the order of arrival) and writes dK, dV. cap = 0: no key tile is split.
+struct BwdSplit {
+  int cap;              // steps per part (0: no split)
+  int ctas_per_group;   // CTAs of one (batch entry, KV head) group: sum over key tiles of their parts
+  int parts_per_group;  // partials one group keeps: the parts of its split key tiles
+};
+
+inline int bwd_tile_steps(int jt, int n_tiles, int G, int causal) { return G * (causal ? n_tiles - jt : n_tiles); }
+
+// The split the backward uses for these sizes (bwd.cu; computed once per size and cached). It does
+// not depend on the device, so neither does the workspace size.
+BwdSplit bwd_split_plan(int B, int Hkv, int G, int n_tiles, int causal);
+
+inline BwdWorkspace bwd_workspace_layout(int B, int Hq, int Hkv, int S, int D) {
   BwdWorkspace w;
-  const size_t rows_pad = (size_t)B * Hq * (size_t)ceil_div(S, kTile) * kTile;
+  const int n_tiles = ceil_div(S, kTile);
+  const size_t rows_pad = (size_t)B * Hq * (size_t)n_tiles * kTile;
   w.dvec_off = 0;
   w.lse2_off = align256(w.dvec_off + rows_pad * sizeof(float));
   w.dqacc_off = align256(w.lse2_off + rows_pad * sizeof(float));
-  w.total = align256(w.dqacc_off + (size_t)B * Hq * S * D * sizeof(float));
+  w.part_off = align256(w.dqacc_off + (size_t)B * Hq * S * D * sizeof(float));
+  // partials for the larger of the causal and the non-causal plan
+  int parts = 0;
+  for (int causal = 0; causal < 2; ++causal) {
+    const int pp = bwd_split_plan(B, Hkv, Hq / Hkv, n_tiles, causal).parts_per_group;
+    parts = pp > parts ? pp : parts;
+  }
+  w.ticket_off = align256(w.part_off + (size_t)B * Hkv * parts * kTile * D * 2 * sizeof(float));
+  w.total = align256(w.ticket_off + (size_t)B * Hkv * n_tiles * sizeof(unsigned));
   return w;
 }
 
@@ -114,7 +143,7 @@ inline BwdWorkspace bwd_workspace_layout_packed(int Hq, int T, int D) {
   w.dvec_off = 0;
   w.lse2_off = align256(w.dvec_off + rows * sizeof(float));
   w.dqacc_off = align256(w.lse2_off + rows * sizeof(float));
-  w.total = align256(w.dqacc_off + (size_t)Hq * T * D * sizeof(float));
+  w.part_off = w.ticket_off = w.total = align256(w.dqacc_off + (size_t)Hq * T * D * sizeof(float));
   return w;
 }
 

@@ -74,8 +74,9 @@ def test_strerror_and_workspace_size(lib):
     assert lib.gqa_attn_bwd_workspace_size(1, 4, 2, 128, 96) == 0
     assert lib.gqa_attn_bwd_workspace_size(1, 4, 3, 128, 64) == 0
     n = lib.gqa_attn_bwd_workspace_size(2, 32, 8, 16384, 128)
-    # D and LSE2 rows (f32, padded to 128) + f32 dQ accumulator, 256-byte aligned sections
-    assert n == 2 * 2 * 32 * 16384 * 4 + 2 * 32 * 16384 * 128 * 4
+    # D and LSE2 rows (f32, padded to 128) + f32 dQ accumulator + one arrival counter per key tile
+    # of each (batch entry, KV head), 256-byte aligned sections; no key tile of this size is split
+    assert n == 2 * 2 * 32 * 16384 * 4 + 2 * 32 * 16384 * 128 * 4 + 2 * 8 * 128 * 4
     n = lib.gqa_attn_bwd_workspace_size(1, 4, 2, 130, 64)
     rows_pad = 4 * 256
     assert n >= 2 * rows_pad * 4 + 4 * 130 * 64 * 4 and n % 256 == 0
@@ -172,3 +173,72 @@ def test_product_never_touches_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "oracle/" not in src, f
+
+
+def _tile_steps(jt, n_tiles, G, causal):
+    return G * (n_tiles - jt if causal else n_tiles)
+
+
+def _makespan(B, Hkv, G, n_tiles, causal, cap, overhead=4, sms=152):
+    import heapq
+    sizes = []
+    for jt in range(n_tiles):
+        st = _tile_steps(jt, n_tiles, G, causal)
+        parts = -(-st // cap) if cap else 1
+        sizes += [(p + 1) * st // parts - p * st // parts + overhead for p in range(parts)] * (B * Hkv)
+    load = [0] * sms
+    span = 0
+    for sz in sorted(sizes, reverse=True):
+        t = heapq.heappop(load) + sz
+        heapq.heappush(load, t)
+        span = max(span, t)
+    return span
+
+
+def _split_plan(B, Hkv, G, n_tiles, causal):
+    """The backward's key-tile split, restated: the cap with the shortest longest-first makespan
+    (CTAs cost their steps plus 4), taken if it beats the unsplit grid by 15%; then the parts of
+    every key tile with their step ranges. None: nothing is split."""
+    steps0 = _tile_steps(0, n_tiles, G, causal)
+    if B * Hkv * n_tiles > 2 * 152 or steps0 < 2:
+        return None, 0
+    unsplit = best = _makespan(B, Hkv, G, n_tiles, causal, 0)
+    best_cap = 0
+    for cap in range(steps0 - 1, 0, -1):
+        m = _makespan(B, Hkv, G, n_tiles, causal, cap)
+        if m < best:
+            best, best_cap = m, cap
+    if best_cap == 0 or best * 1.15 > unsplit:
+        return None, 0
+    plan = []
+    for jt in range(n_tiles):
+        st = _tile_steps(jt, n_tiles, G, causal)
+        parts = -(-st // best_cap)
+        plan.append((jt, [(p * st // parts, (p + 1) * st // parts) for p in range(parts)]))
+    return plan, best_cap
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,causal", [(4, 12, 4, 1024, 1), (8, 8, 2, 512, 1), (1, 32, 8, 4096, 1),
+                                               (1, 4, 2, 128, 1), (2, 6, 3, 300, 0), (2, 32, 8, 16384, 1)])
+def test_split_parts_cover_every_step_once(B, Hq, Hkv, S, causal):
+    """Host logic of the split backward: the parts of a key tile cover its steps exactly once, in
+    order, with at most `cap` steps each, and the workspace holds every partial."""
+    import math
+    G, n_tiles = Hq // Hkv, math.ceil(S / 128)
+    plan, cap = _split_plan(B, Hkv, G, n_tiles, causal)
+    if plan is None:
+        assert (B, Hq, S) not in ((4, 12, 1024), (8, 8, 512)), "the small workloads are expected to split"
+        return
+    parts_per_group = 0
+    for jt, parts in plan:
+        steps = G * (n_tiles - jt if causal else n_tiles)
+        assert parts[0][0] == 0 and parts[-1][1] == steps
+        for (a, b), (c, _) in zip(parts, parts[1:]):
+            assert b == c
+        assert all(0 < b - a <= cap for a, b in parts)
+        if len(parts) > 1:
+            parts_per_group += len(parts)
+    from causal_gqa_attention_flash_gb300 import _lib
+    lib = _lib.load()
+    n = lib.gqa_attn_bwd_workspace_size(B, Hq, Hkv, S, 64)
+    assert n >= B * Hkv * parts_per_group * 128 * 64 * 2 * 4

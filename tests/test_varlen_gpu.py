@@ -162,8 +162,9 @@ def test_packed_backward_many_random_lengths():
 
 
 def test_packed_backward_equals_dense_batch():
-    """At equal lengths the packed backward matches the dense one: dK, dV bitwise (both reduce
-    over the group in a fixed order in one CTA), dQ within f32 reduction-order noise."""
+    """At equal lengths the packed backward matches the dense one within f32 summation-order noise
+    (the dense backward of a problem this small splits its key tiles over several CTAs and adds
+    their partials; the packed one sums each key tile in one CTA)."""
     g = gqa()
     B, Hq, Hkv, S, D = 3, 8, 2, 333, 128
     q, k, v, dO = (t.cuda() for t in make_inputs(B, Hq, Hkv, S, D, 19))
@@ -177,8 +178,8 @@ def test_packed_backward_equals_dense_batch():
     lse_p = lse.permute(1, 0, 2).reshape(Hq, B * S).contiguous()
     dq_p, dk_p, dv_p = g.gqa_attn_bwd_varlen(pack(q), pack(k), pack(v), pack(o), pack(dO), lse_p, cu, S)
     assert g.gqa_attn_get_error() == 0
-    assert torch.equal(dk_p, pack(dk_d)) and torch.equal(dv_p, pack(dv_d))
-    assert (dq_p.float() - pack(dq_d).float()).abs().max().item() <= 1e-2 * pack(dq_d).float().abs().max().item()
+    for got, want in ((dk_p, pack(dk_d)), (dv_p, pack(dv_d)), (dq_p, pack(dq_d))):
+        assert (got.float() - want.float()).abs().max().item() <= 1e-2 * want.float().abs().max().item()
 
 
 def test_packed_backward_invalid_bounds_reported():
