@@ -41,6 +41,8 @@ __all__ = [
     "gqa_attn_bwd_noalloc",
     "gqa_attn_decode_fwd",
     "gqa_attn_fwd_cached",
+    "gqa_attn_fwd_splitkv",
+    "gqa_attn_fwd_splitkv_workspace_size",
     "gqa_attn_fwd_varlen",
     "gqa_attn_bwd_varlen",
     "gqa_attn_bwd_varlen_workspace_size",
@@ -56,7 +58,8 @@ __all__ = [
 
 # Tracing slots in the header's GQA_KERNEL_* order. "decode_combine" is no longer launched (the last
 # split CTA of each KV head merges the chunks); its slot stays so that the numbering is stable.
-KERNEL_NAMES = ("fwd", "bwd_prep", "bwd_main", "bwd_convert", "decode_split", "decode_combine", "bwd_dkdv", "bwd_dq", "rope")
+KERNEL_NAMES = ("fwd", "bwd_prep", "bwd_main", "bwd_convert", "decode_split", "decode_combine", "bwd_dkdv", "bwd_dq", "rope",
+                "fwd_combine")
 
 GQA_OK = 0
 GQA_ERR_INVALID_ARG = -1
@@ -297,6 +300,36 @@ def gqa_attn_fwd_cached(q, k_cache, v_cache, causal: bool = True, scale: float |
                                              lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)), float(scale),
                                              _stream_handle(stream, dev))
     _check(rc, "gqa_attn_fwd_cached")
+    return o, lse
+
+
+def gqa_attn_fwd_splitkv_workspace_size(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, D: int) -> int:
+    """Bytes of workspace gqa_attn_fwd_splitkv needs (0: these sizes are never split)."""
+    return int(_lib.load().gqa_attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Sq, Sk, D))
+
+
+def gqa_attn_fwd_splitkv(q, k_cache, v_cache, causal: bool = True, scale: float | None = None, o=None, lse=None,
+                         workspace=None, stream=None):
+    """Forward of q [B,Hq,Sq,D] over k/v [B,Hkv,Sk,D] (Sq <= Sk; Sq = Sk is the training forward)
+    whose key range is split across CTAs when the grid is small. Returns (o, lse) like
+    gqa_attn_fwd_cached; ``workspace`` (optional) is a uint8 CUDA tensor of at least
+    ``gqa_attn_fwd_splitkv_workspace_size(...)`` bytes."""
+    B, Hq, Hkv, Sq, Sk, D = _cache_dims(q, k_cache, v_cache)
+    dev = q.device
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = _out("o", o, q.shape, torch.bfloat16, dev)
+    lse = _out("lse", lse, (B, Hq, Sq), torch.float32, dev)
+    need = gqa_attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Sq, Sk, D)
+    ws_ptr, nbytes = 0, 0
+    if need > 0 or workspace is not None:
+        workspace = _workspace(workspace, need, dev)
+        ws_ptr, nbytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        rc = _lib.load().gqa_attn_fwd_splitkv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o.data_ptr(),
+                                              lse.data_ptr(), ws_ptr or None, nbytes, B, Hq, Hkv, Sq, Sk, D,
+                                              int(bool(causal)), float(scale), _stream_handle(stream, dev))
+    _check(rc, "gqa_attn_fwd_splitkv")
     return o, lse
 
 

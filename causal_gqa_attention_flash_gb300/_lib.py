@@ -17,6 +17,8 @@ _c_int, _c_float, _vp, _sz = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctyp
 SIGNATURES = {
     "gqa_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _vp]),
     "gqa_attn_fwd_cached": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
+    "gqa_attn_fwd_splitkv_workspace_size": (_sz, [_c_int] * 6),
+    "gqa_attn_fwd_splitkv": (_c_int, [_vp] * 6 + [_sz] + [_c_int] * 7 + [_c_float, _vp]),
     "gqa_attn_fwd_varlen": (_c_int, [_vp] * 7 + [_c_int] * 8 + [_c_float, _vp]),
     "gqa_attn_bwd_workspace_size": (_sz, [_c_int] * 5),
     "gqa_attn_bwd_varlen_workspace_size": (_sz, [_c_int] * 4),

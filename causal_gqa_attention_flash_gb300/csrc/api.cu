@@ -172,7 +172,7 @@ namespace {
 
 const char* const kKernelRangeNames[kKernelCount] = {
     "fwd_kernel",          "bwd_prep_kernel",  "bwd_main_kernel",   "bwd_convert_kernel", "decode_split_kernel",
-    "decode_combine",      "bwd_dkdv_kernel",  "bwd_dq_kernel",     "rope_rotate_kernel"};
+    "decode_combine",      "bwd_dkdv_kernel",  "bwd_dq_kernel",     "rope_rotate_kernel", "fwd_combine_kernel"};
 
 // NVTX range over one entry point (a no-op unless a profiling tool is attached).
 struct NvtxScope {
@@ -223,7 +223,8 @@ namespace {
 // Dense forward, Sq <= Sk; with rotary tables (Sq = Sk) Q is rotated on load and k must
 // already hold the rotated keys.
 int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk,
-              int D, int causal, float scale, const float* rope_cos, const float* rope_sin, void* stream) {
+              int D, int causal, float scale, const float* rope_cos, const float* rope_sin, void* stream,
+              void* workspace = nullptr, size_t workspace_bytes = 0) {
   if (!q || !k || !v || !o || !lse) return GQA_ERR_INVALID_ARG;
   if (Sq < 1 || Sq > Sk) return GQA_ERR_INVALID_ARG;
   int rc = check_common(B, Hq, Hkv, Sk, D, scale);
@@ -259,6 +260,14 @@ int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.causal = causal ? 1 : 0;
   a.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   a.status = status;
+  a.part = nullptr;
+  if (workspace) {  // the split forward's slots
+    const FwdWorkspace fw = fwd_workspace_layout(B, Hq, Sq, Sk, D);
+    if (fw.total > 0) {
+      if (workspace_bytes < fw.total) return GQA_ERR_WORKSPACE_TOO_SMALL;
+      a.part = static_cast<float*>(workspace);
+    }
+  }
   if ((e = launch_fwd(a, static_cast<cudaStream_t>(stream))) != cudaSuccess) return fail_cuda(e);
   return GQA_OK;
 }
@@ -277,6 +286,20 @@ int gqa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int D, int causal, float scale, void* stream) {
   NvtxScope nvtx_scope("gqa_attn_fwd");
   return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, S, S, D, causal, scale, nullptr, nullptr, stream);
+}
+
+size_t gqa_attn_fwd_splitkv_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D) {
+  if (Sq < 1 || Sq > Sk || check_common(B, Hq, Hkv, Sk, D, 1.0f) != GQA_OK) return 0;
+  return fwd_workspace_layout(B, Hq, Sq, Sk, D).total;
+}
+
+int gqa_attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                         size_t workspace_bytes, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                         void* stream) {
+  NvtxScope nvtx_scope("gqa_attn_fwd_splitkv");
+  if (workspace && !aligned(workspace, 256)) return GQA_ERR_INVALID_ARG;
+  return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, nullptr, nullptr, stream, workspace,
+                   workspace_bytes);
 }
 
 size_t gqa_attn_fwd_rope_workspace_size(int B, int Hkv, int S, int D) {
@@ -336,6 +359,7 @@ int gqa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
   a.max_seqlen_q = max_seqlen_q;
   a.rope_cos = nullptr;
   a.rope_sin = nullptr;
+  a.part = nullptr;  // packed batches are not split
   a.B = nseq;
   a.Hq = Hq;
   a.Hkv = Hkv;

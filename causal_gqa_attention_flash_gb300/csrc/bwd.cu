@@ -667,7 +667,8 @@ __global__ void __launch_bounds__(352, 1)
         const size_t at = (size_t)sp.part * kSlot + (size_t)row * D + col;
         if (kv_valid &&
             dbg_range((long long)(slots - p.part) + (long long)at, (long long)kTile * D + 32, (long long)slot_end,
-                      p.status)) {
+                      p.status) &&
+            dbg_ok((reinterpret_cast<uintptr_t>(slots + at) & 15u) == 0, p.status)) {
 #pragma unroll
           for (int x = 0; x < 8; ++x) {
             *reinterpret_cast<float4*>(slots + at + 4 * x) =
@@ -771,7 +772,6 @@ __global__ void __launch_bounds__(352, 1)
 // 16-step CTA takes ~43 us, two 4-step CTAs in a row ~34 us), CTAs are dealt longest first onto
 // kPlanCtas SMs (the order of the grid), and the cap with the shortest estimated makespan wins if
 // it beats the unsplit grid by kSplitGain. Only grids of at most two waves are considered.
-constexpr int kPlanCtas = 152;  // a GB300's SM count: the plan, and the workspace, do not depend on the device
 constexpr int kCtaOverheadSteps = 4;
 constexpr double kSplitGain = 1.15;
 

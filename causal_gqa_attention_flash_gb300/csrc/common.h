@@ -37,7 +37,36 @@ struct FwdArgs {
   int B, Hq, Hkv, Sq, Sk, D, causal;
   float scale_log2;          // scale * log2(e)
   int* status;               // device status word
+  float* part;               // split forward: the parts' O tiles and (m, l) (nullptr: never split)
 };
+
+// The split plans of the forward and the backward (small problems: see FwdSplit, BwdSplit) assume
+// one wave of kPlanCtas CTAs, a GB300's SM count, so that neither they nor the workspace sizes
+// depend on the device.
+constexpr int kPlanCtas = 152;
+
+// Key-range split of the dense forward (fwd.cu): on small grids the key tiles of the longest
+// query-tile pairs are cut into parts of at most kcap key tiles (of tile A), one CTA each, merged
+// by the associative (m, l, O) combine. kcap = 0: no pair is split.
+struct FwdSplit {
+  int kcap;          // key tiles of tile A per part (0: no split)
+  int n_pairs;       // query-tile pairs per (batch entry, head)
+  int ctas_y;        // grid rows: the pairs' parts
+  int parts_per_bh;  // slots one (batch entry, head) keeps: the parts of its split pairs
+  int split_pairs;   // pairs cut into more than one part (merged by the combine kernel)
+};
+
+// The split for these sizes (computed once per size and cached; it does not depend on the device).
+FwdSplit fwd_split_plan(int BH, int Sq, int Sk, int causal, int D);
+
+// Workspace of the split forward: one slot per part of a split pair, holding for its tiles A and B
+// the unnormalised O tile as float4 columns [D/4][128 rows] followed by m[128] and l[128];
+// sized for the larger of the causal and the non-causal plan. 0: never split.
+__host__ __device__ inline size_t fwd_slot_floats(int D) { return 2 * ((size_t)kTile * D + 2 * kTile); }
+struct FwdWorkspace {
+  size_t total;
+};
+FwdWorkspace fwd_workspace_layout(int B, int Hq, int Sq, int Sk, int D);
 
 struct BwdArgs {
   const CUtensorMap* map_q;    // [B*Hq, S, D] bf16
@@ -158,7 +187,8 @@ enum KernelKind {
   kKernelBwdDkdv = 6,
   kKernelBwdDq = 7,
   kKernelRope = 8,
-  kKernelCount = 9
+  kKernelFwdCombine = 9,
+  kKernelCount = 10
 };
 void trace_begin(int kind, cudaStream_t s);
 void trace_end(int kind, cudaStream_t s);

@@ -35,6 +35,12 @@
 // a batch may be packed: sequences of different lengths laid end to end along
 // the row axis, each CTA reading its sequence's bounds, the last ragged query
 // tile of a sequence storing its rows one by one.
+#include <algorithm>
+#include <functional>
+#include <mutex>
+#include <queue>
+#include <vector>
+
 #include "common.h"
 #include "ptx.cuh"
 #include "rope.cuh"
@@ -67,7 +73,7 @@ struct FwdCfg {
 
 template <int KST, int VST>
 struct FwdBars {
-  uint64_t q_full;
+  uint64_t q_full[2];  // Q_A, Q_B (separate, so that S_A(0) need not wait for Q_B)
   uint64_t k_full[KST];
   uint64_t v_full[VST];
   uint64_t k_empty[KST];
@@ -101,6 +107,19 @@ struct FwdKParams {
   int Hq, Hkv, Sq, Sk, koff, causal, n_ktiles;
   float scale_log2;
   int* status;
+  // Key-range split of a dense forward (kcap > 0): the key tiles of tile A of a query-tile pair
+  // are cut into ceil(nA / kcap) contiguous parts, one CTA each (the last part also takes tile B's
+  // extra key tile); grid y enumerates the (pair, part) pairs, longest pairs first. Each part
+  // writes tile A's and tile B's unnormalised O and (m, l) to its slot of `part`, and the combine
+  // kernel merges the slots of a pair with the monoid combine.
+  int kcap, n_pairs, parts_per_bh;
+  float* part;
+};
+
+// Position of grid row y in the split forward: pair, part, parts of the pair, and the index of
+// the pair's first slot among its head's slots (only split pairs keep slots).
+struct FwdSplitPos {
+  int pair, part, parts, pidx;
 };
 
 // The rows one CTA works on: its sequence's query and key counts and where they start.
@@ -272,6 +291,20 @@ __device__ __forceinline__ int kv_tiles_of(int qt, const FwdGeom& g, int causal)
   return (g.koff + last_row) / kTile + 1;
 }
 
+// The number of parts of a pair whose tile A visits nA key tiles (split forward).
+__device__ __forceinline__ int fwd_pair_parts(int nA, int kcap) { return nA > kcap ? (nA + kcap - 1) / kcap : 1; }
+
+__device__ __forceinline__ FwdSplitPos fwd_split_pos(int y, const FwdGeom& g, int causal, int n_pairs, int kcap) {
+  int pidx = 0;
+  for (int pr = n_pairs - 1; pr >= 0; --pr) {  // longest pairs first
+    const int parts = fwd_pair_parts(kv_tiles_of(2 * pr, g, causal), kcap);
+    if (y < parts) return FwdSplitPos{pr, y, parts, pidx};
+    y -= parts;
+    if (parts > 1) pidx += parts;
+  }
+  return FwdSplitPos{0, 0, 0, 0};  // past the plan (no such grid row is launched)
+}
+
 // kRope: queries are turned by the rotary embedding as they land in shared memory.
 template <int D, bool kRope>
 __global__ void __launch_bounds__(384, 1)
@@ -289,17 +322,29 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int bh = blockIdx.x;                                   // b * Hq + h
-  const int pair = (int)gridDim.y - 1 - (int)blockIdx.y;       // longest pairs first
   FwdGeom g;
   if (!fwd_geom(p, bh, g)) {
     if (tid == 0) atomicOr(p.status, STATUS_BAD_SEQLENS);
     return;
   }
+  // Query-tile pair (longest pairs first) and, in a split forward, the part of its key range.
+  FwdSplitPos sp{(int)gridDim.y - 1 - (int)blockIdx.y, 0, 1, 0};
+  if (p.kcap > 0) sp = fwd_split_pos((int)blockIdx.y, g, p.causal, p.n_pairs, p.kcap);
+  if (sp.parts == 0) return;
+  const int pair = sp.pair;
   const int qtA = 2 * pair, qtB = 2 * pair + 1;
-  const int nA = kv_tiles_of(qtA, g, p.causal);
-  const int nB = kv_tiles_of(qtB, g, p.causal);
-  const int n_kv = nA > nB ? nA : nB;
-  if (nA == 0) return;  // a packed batch's short sequence: no query tile of this CTA exists
+  const int nA_all = kv_tiles_of(qtA, g, p.causal);
+  const int nB_all = kv_tiles_of(qtB, g, p.causal);
+  if (nA_all == 0) return;  // a packed batch's short sequence: no query tile of this CTA exists
+  // This CTA's key tiles kb .. kb + n_kv - 1 (all of them unless the pair is split: part q takes
+  // [q nA / parts, (q + 1) nA / parts), the last part up to tile B's last key tile). Below, key
+  // tiles are numbered from kb: nA, nB count tile A's and tile B's tiles in the range.
+  const int n_all = nA_all > nB_all ? nA_all : nB_all;
+  const int kb = (int)((long long)sp.part * nA_all / sp.parts);
+  const int ke = sp.part == sp.parts - 1 ? n_all : (int)((long long)(sp.part + 1) * nA_all / sp.parts);
+  const int nA = (nA_all < ke ? nA_all : ke) - kb;  // >= 1: every part holds a key tile of tile A
+  const int nB = nB_all > 0 ? (nB_all < ke ? nB_all : ke) - kb : 0;
+  const int n_kv = ke - kb;
   const WaitGuard wg{&bars->abort_flag, p.status, kWaitLimitNs};
   // Extents of the tensors this CTA addresses, for the debug build's coordinate checks: heads of
   // the query / key maps and their rows (a packed CTA stays within its own sequence's rows).
@@ -308,7 +353,8 @@ __global__ void __launch_bounds__(384, 1)
   const int rows_q = p.cu_q ? p.Tq : p.Sq;
 
   if (tid == 0) {
-    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_full[0], 1);
+    mbar_init(&bars->q_full[1], 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
@@ -344,16 +390,19 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
-      // Q_B only when tile B has rows (its buffer is otherwise never read)
-      const int nq = nB > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(&bars->q_full, nq * C::kTileBytes);
-      for (int t = 0; t < nq; ++t)
+      // Q_A, then K_0, then Q_B (only when tile B has rows; its buffer is otherwise never read):
+      // the first S MMA waits for the first 64 KB, not for 96 KB.
+      auto load_q = [&](int t) {
+        mbar_arrive_expect_tx(&bars->q_full[t], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
           const int r = g.q_row0 + (qtA + t) * kTile;
-          tma_load_3d_chk(smem + C::kQOff + t * C::kTileBytes + c * kBoxBytes, &map_q, &bars->q_full, c * kChunk, r,
-                          g.q_coord, dbg_tile(c * kChunk, r, g.q_coord, D, kChunk, g.q_row0, g.q_row0 + g.Sq,
-                                              heads_q, p.status));
+          tma_load_3d_chk(smem + C::kQOff + t * C::kTileBytes + c * kBoxBytes, &map_q, &bars->q_full[t], c * kChunk,
+                          r, g.q_coord,
+                          dbg_tile(c * kChunk, r, g.q_coord, D, kChunk, g.q_row0, g.q_row0 + g.Sq, heads_q, p.status));
         }
+      };
+      load_q(0);
+      bool q_b_issued = false;
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % ST;
@@ -361,17 +410,22 @@ __global__ void __launch_bounds__(384, 1)
         if (use > 0 && !mbar_wait(&bars->k_empty[st], (use - 1) & 1, wg)) break;
         mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
-          const int r = g.k_row0 + j * kTile;
+          const int r = g.k_row0 + (kb + j) * kTile;
           tma_load_3d_chk(smem + C::kKOff + st * C::kTileBytes + c * kBoxBytes, &map_k, &bars->k_full[st],
                           c * kChunk, r, g.kv_coord,
                           dbg_tile(c * kChunk, r, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv,
                                    p.status));
         }
         issued = j + 1;
+        if (j == 0 && nB > 0) {
+          load_q(1);
+          q_b_issued = true;
+        }
       }
       if (bars->abort_flag) {
         // Let every copy already issued land before the CTA's shared memory goes away.
-        mbar_wait_drain(&bars->q_full, 0, kWaitLimitNs);
+        mbar_wait_drain(&bars->q_full[0], 0, kWaitLimitNs);
+        if (q_b_issued) mbar_wait_drain(&bars->q_full[1], 0, kWaitLimitNs);
         for (int j = (issued > ST ? issued - ST : 0); j < issued; ++j)
           mbar_wait_drain(&bars->k_full[j % ST], (j / ST) & 1, kWaitLimitNs);
       }
@@ -387,7 +441,7 @@ __global__ void __launch_bounds__(384, 1)
         if (use > 0 && !mbar_wait(&bars->v_empty[st], (use - 1) & 1, wg)) break;
         mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
-          const int r = g.k_row0 + j * kTile;
+          const int r = g.k_row0 + (kb + j) * kTile;
           tma_load_3d_chk(smem + C::kVOff + st * C::kTileBytes + c * kBoxBytes, &map_v, &bars->v_full[st],
                           c * kChunk, r, g.kv_coord,
                           dbg_tile(c * kChunk, r, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv,
@@ -438,16 +492,20 @@ __global__ void __launch_bounds__(384, 1)
       };
       // K_j is released once the last S MMA reading it completes, V_j once both P V MMAs do:
       // the K ring refills a full key tile earlier than a shared K/V stage would.
-      bool ok = mbar_wait(&bars->q_full, 0, wg) && mbar_wait(&bars->k_full[0], 0, wg);
-      if (kRope && ok) {  // the softmax warps rotate their tile's queries first
-        ok = (nA == 0 || mbar_wait(&bars->q_ready[0], 0, wg)) && (nB == 0 || mbar_wait(&bars->q_ready[1], 0, wg));
-      }
+      bool ok = mbar_wait(&bars->q_full[0], 0, wg) && mbar_wait(&bars->k_full[0], 0, wg);
+      if (kRope && ok) ok = mbar_wait(&bars->q_ready[0], 0, wg);  // the softmax warps rotate their queries first
       if (ok) {
         tc_fence_after();
-        if (nA > 0) issue_s(0, 0);
-        if (nB > 0) issue_s(1, 0);
-        umma_commit(&bars->k_empty[0]);
+        issue_s(0, 0);  // nA > 0 for every CTA that gets here
       }
+      if (ok && nB > 0) {
+        ok = mbar_wait(&bars->q_full[1], 0, wg) && (!kRope || mbar_wait(&bars->q_ready[1], 0, wg));
+        if (ok) {
+          tc_fence_after();
+          issue_s(1, 0);
+        }
+      }
+      if (ok) umma_commit(&bars->k_empty[0]);
       for (int j = 0; ok && j < n_kv; ++j) {
         const int vst = j % VST;
         const int j1 = j + 1;
@@ -467,8 +525,8 @@ __global__ void __launch_bounds__(384, 1)
           if (!(ok = mbar_wait(&bars->p_full[1], j & 1, wg))) break;
           tc_fence_after();
           issue_pv(1, j);
-          if (j1 < nB) {
-            if (!(ok = mbar_wait(&bars->k_full[st1], (j1 / ST) & 1, wg))) break;
+          if (j1 < nB) {  // K_{j+1} was already waited for when tile A uses it too
+            if (j1 >= nA && !(ok = mbar_wait(&bars->k_full[st1], (j1 / ST) & 1, wg))) break;
             tc_fence_after();
             issue_s(1, j1);
           }
@@ -492,12 +550,15 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t s_tmem = tbase + lane_off + (uint32_t)x * 128u;
     const uint32_t o_tmem = tbase + lane_off + C::kOCol + (uint32_t)x * D;
     const float c = p.scale_log2;
+    // Running reference max and sum; the reference is taken from the first key tile in which the
+    // row sees a key (a part of a split key range can start with a tile the row does not see yet).
     float m_ref = 0.f, l = 0.f;
+    bool have_ref = false;
     bool ok = true;
     if (kRope && n_x > 0) {
       // Rotary embedding: each thread turns its own query row of tile X in shared memory
       // (rows past S hold zeros and have no table row).
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, wg));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full[x], 0, wg));
       const int qpos = qt * kTile + row;
       if (ok && qpos < g.Sq && dbg_range((long long)qpos * (D / 2), D / 2, (long long)p.Sq * (D / 2), p.status))
         rope_rotate_row_smem<D>(smem + C::kQOff + x * C::kTileBytes, row, p.rope_cos + (size_t)qpos * (D / 2),
@@ -516,7 +577,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int q = 0; q < 4; ++q) tmem_wait_ld_x32(*reinterpret_cast<uint32_t(*)[32]>(&r[32 * q]));
 
-      const int kv0 = j * kTile;
+      const int kv0 = (kb + j) * kTile;  // the key tile's first key
       // last visible local key of this row in key tile j: the causal bound koff + q - kv0 and the
       // end of the keys; tiles where some row sees fewer than 128 keys take the masked path.
       const int qpos = g.koff + qt * kTile;  // absolute position of the tile's first row
@@ -535,8 +596,11 @@ __global__ void __launch_bounds__(384, 1)
       const float m_tile = mx * c;
       float alpha = 1.f;
       bool need = false;
-      if (j == 0) {
-        m_ref = m_tile;
+      if (!have_ref) {
+        if (m_tile > -INFINITY) {
+          m_ref = m_tile;
+          have_ref = true;
+        }
       } else if (m_tile > m_ref + 8.f) {
         alpha = ex2_approx(m_ref - m_tile);
         m_ref = m_tile;
@@ -568,7 +632,33 @@ __global__ void __launch_bounds__(384, 1)
       mbar_arrive_warp(&bars->p_full[x]);
     }
     if (ok && n_x > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[x], (n_x - 1) & 1, wg));
-    if (ok && n_x > 0) {
+    if (ok && n_x > 0 && sp.parts > 1) {
+      // Split key range: this part's unnormalised O tile X and its (m, l) go to the part's slot
+      // (m = -inf for a row that saw no key in the range). A warp's stores cover 32 consecutive
+      // rows of one float4 column: 512 contiguous bytes.
+      tc_fence_after();
+      const size_t slot_fl = fwd_slot_floats(D);
+      float* tile = p.part + ((size_t)bh * p.parts_per_bh + sp.pidx + sp.part) * slot_fl +
+                    (size_t)x * (slot_fl / 2);
+      const long long slot_end = (long long)gridDim.x * p.parts_per_bh * (long long)slot_fl;
+      if (dbg_range((long long)(tile - p.part), (long long)(slot_fl / 2), slot_end, p.status) &&
+          dbg_ok((reinterpret_cast<uintptr_t>(tile) & 15u) == 0, p.status)) {
+        float4* cols = reinterpret_cast<float4*>(tile);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(o_tmem + cc * 32, o);
+          tmem_wait_ld_x32(o);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            cols[(size_t)(cc * 8 + u) * kTile + row] =
+                make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]), __uint_as_float(o[4 * u + 2]),
+                            __uint_as_float(o[4 * u + 3]));
+        }
+        tile[(size_t)kTile * D + row] = have_ref ? m_ref : -INFINITY;
+        tile[(size_t)kTile * D + kTile + row] = l;
+      }
+    } else if (ok && n_x > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const int qrow = qt * kTile + row;
@@ -627,6 +717,220 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// Key tiles query tile qt of a dense batch sees (kv_tiles_of without the per-CTA geometry).
+__host__ __device__ inline int dense_kv_tiles(int qt, int Sq, int Sk, int causal) {
+  if (qt * kTile >= Sq) return 0;
+  const int n_ktiles = (Sk + kTile - 1) / kTile;
+  if (!causal) return n_ktiles;
+  const int last_row = Sq - 1 < qt * kTile + kTile - 1 ? Sq - 1 : qt * kTile + kTile - 1;
+  return (Sk - Sq + last_row) / kTile + 1;
+}
+
+struct FwdCombineParams {
+  const float* part;
+  uint16_t* o;  // [B*Hq, Sq, D] bf16
+  float* lse;   // [B*Hq, Sq]
+  int Sq, Sk, causal, kcap, n_pairs, parts_per_bh;
+  int* status;
+};
+
+// Merge of a split forward's parts: for row r of a tile cut into parts p with maxima m_p, sums
+// l_p and unnormalised rows O_p, M = max m_p, L = sum l_p 2^(m_p - M), O = sum O_p 2^(m_p - M) / L,
+// LSE = (M + log2 L) ln 2; parts are added in part order, so the result is reproducible. One CTA
+// takes 128 rows x 8 columns of one tile of one split pair: grid x = batch entry x head, grid y =
+// (split pair, tile, column chunk). A warp's loads cover 32 rows of one float4 column of a slot
+// (512 contiguous bytes); the part loops are unrolled so that a thread has many loads in flight.
+template <int D>
+__global__ void __launch_bounds__(128) fwd_combine_kernel(const FwdCombineParams p) {
+  constexpr int kChunks = D / 8;
+  const int bh = blockIdx.x;
+  const int cchunk = (int)blockIdx.y % kChunks;
+  const int x = ((int)blockIdx.y / kChunks) & 1;
+  int s = (int)blockIdx.y / (2 * kChunks);
+  const int row = threadIdx.x;
+  // the s-th split pair, longest pairs first, and the index of its first slot
+  int pair = -1, parts = 0, pidx = 0;
+  for (int pr = p.n_pairs - 1; pr >= 0; --pr) {
+    const int nA = dense_kv_tiles(2 * pr, p.Sq, p.Sk, p.causal);
+    const int np = nA > p.kcap ? (nA + p.kcap - 1) / p.kcap : 1;
+    if (np < 2) continue;
+    if (s == 0) {
+      pair = pr;
+      parts = np;
+      break;
+    }
+    --s;
+    pidx += np;
+  }
+  if (pair < 0) return;
+  const int qrow = (2 * pair + x) * kTile + row;
+  if (qrow >= p.Sq) return;
+  const size_t slot_fl = fwd_slot_floats(D);
+  const float* tile = p.part + ((size_t)bh * p.parts_per_bh + pidx) * slot_fl + (size_t)x * (slot_fl / 2);
+  const long long slot_end = (long long)gridDim.x * p.parts_per_bh * (long long)slot_fl;
+  if (!dbg_range((long long)(tile - p.part) + (long long)(parts - 1) * (long long)slot_fl, (long long)(slot_fl / 2),
+                 slot_end, p.status))
+    return;
+  const float* m_of = tile + (size_t)kTile * D + row;
+  const float* l_of = m_of + kTile;
+  // Loads are issued a group of parts at a time (predicated past the last part), then consumed.
+  constexpr int kGroup = 4;
+  float M = -INFINITY;
+  for (int p0 = 0; p0 < parts; p0 += 2 * kGroup) {
+    float mm[2 * kGroup];
+#pragma unroll
+    for (int i = 0; i < 2 * kGroup; ++i) mm[i] = p0 + i < parts ? m_of[(size_t)(p0 + i) * slot_fl] : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 2 * kGroup; ++i) M = fmaxf(M, mm[i]);
+  }
+  float L = 0.f;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const float4* cols = reinterpret_cast<const float4*>(tile) + (size_t)cchunk * 2 * kTile + row;
+  for (int p0 = 0; p0 < parts; p0 += kGroup) {  // part order
+    float mm[kGroup], ll[kGroup];
+    float4 a[kGroup], b[kGroup];
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) {
+      const size_t off = (size_t)(p0 + i) * slot_fl;
+      const bool in = p0 + i < parts;
+      mm[i] = in ? m_of[off] : -INFINITY;
+      ll[i] = in ? l_of[off] : 0.f;
+      a[i] = in ? cols[off / 4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      b[i] = in ? cols[off / 4 + kTile] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) {
+      const float w = ex2_approx(mm[i] - M);  // 0 for a part where the row saw no key, or none
+      L = fmaf(ll[i], w, L);
+      acc[0] = fmaf(a[i].x, w, acc[0]);
+      acc[1] = fmaf(a[i].y, w, acc[1]);
+      acc[2] = fmaf(a[i].z, w, acc[2]);
+      acc[3] = fmaf(a[i].w, w, acc[3]);
+      acc[4] = fmaf(b[i].x, w, acc[4]);
+      acc[5] = fmaf(b[i].y, w, acc[5]);
+      acc[6] = fmaf(b[i].z, w, acc[6]);
+      acc[7] = fmaf(b[i].w, w, acc[7]);
+    }
+  }
+  const float inv_l = 1.f / L;
+  const long long orow_off = ((long long)bh * p.Sq + qrow) * D + cchunk * 8;
+  if (dbg_range(orow_off, 8, (long long)gridDim.x * p.Sq * D, p.status))
+    *reinterpret_cast<uint4*>(p.o + orow_off) =
+        make_uint4(pack_bf16(acc[0] * inv_l, acc[1] * inv_l), pack_bf16(acc[2] * inv_l, acc[3] * inv_l),
+                   pack_bf16(acc[4] * inv_l, acc[5] * inv_l), pack_bf16(acc[6] * inv_l, acc[7] * inv_l));
+  if (cchunk == 0) p.lse[(size_t)bh * p.Sq + qrow] = (M + __log2f(L)) * 0.69314718055994530942f;
+}
+
+// Plan of the split forward. A CTA's time is modelled in key-tile units (one 128 x 128 tile of one
+// query tile, about 0.9 us at D = 128): its units, plus kFwdCtaOverheadUnits (prologue, epilogue),
+// plus kFwdPartWriteUnits for a part of a split pair (its slot write). CTAs are dealt longest first
+// onto kPlanCtas SMs; a split grid adds the combine kernel, kFwdCombineLaunchUnits plus one unit per
+// kFwdCombineBytesPerUnit of slots it reads. The kcap with the shortest estimate wins if it beats
+// the unsplit grid by kFwdSplitGain; only problems whose unsplit grid has at most two waves split.
+constexpr int kFwdCtaOverheadUnits = 4;
+constexpr int kFwdPartWriteUnits = 2;
+constexpr int kFwdCombineLaunchUnits = 4;
+constexpr long long kFwdCombineBytesPerUnit = 3ll << 20;
+constexpr double kFwdSplitGain = 1.15;
+
+long long fwd_plan_makespan(int BH, int Sq, int Sk, int causal, int D, int n_pairs, int kcap) {
+  std::vector<int> sizes;
+  long long slots = 0;  // per (batch entry, head)
+  for (int pr = 0; pr < n_pairs; ++pr) {
+    const int nA = dense_kv_tiles(2 * pr, Sq, Sk, causal), nB = dense_kv_tiles(2 * pr + 1, Sq, Sk, causal);
+    if (nA == 0) continue;
+    const int n_all = nA > nB ? nA : nB;
+    const int parts = kcap > 0 && nA > kcap ? ceil_div(nA, kcap) : 1;
+    if (parts > 1) slots += parts;
+    for (int q = 0; q < parts; ++q) {
+      const int kb = (int)((long long)q * nA / parts);
+      const int ke = q == parts - 1 ? n_all : (int)((long long)(q + 1) * nA / parts);
+      int units = kFwdCtaOverheadUnits + (parts > 1 ? kFwdPartWriteUnits : 0);
+      for (int j = kb; j < ke; ++j) units += (j < nA) + (j < nB);
+      for (int h = 0; h < BH; ++h) sizes.push_back(units);
+    }
+  }
+  std::sort(sizes.begin(), sizes.end(), std::greater<int>());
+  std::priority_queue<long long, std::vector<long long>, std::greater<long long>> load;
+  for (int i = 0; i < kPlanCtas; ++i) load.push(0);
+  long long span = 0;
+  for (int sz : sizes) {
+    const long long t = load.top() + sz;
+    load.pop();
+    load.push(t);
+    span = t > span ? t : span;
+  }
+  if (slots > 0)
+    span += kFwdCombineLaunchUnits +
+            (long long)(slots * BH * fwd_slot_floats(D) * sizeof(float)) / kFwdCombineBytesPerUnit;
+  return span;
+}
+
+FwdSplit fwd_split_plan_uncached(int BH, int Sq, int Sk, int causal, int D) {
+  const int n_pairs = ceil_div(Sq, 2 * kTile);
+  FwdSplit sp{0, n_pairs, n_pairs, 0, 0};
+  const int nA_first = dense_kv_tiles(0, Sq, Sk, causal), nA_last = dense_kv_tiles(2 * (n_pairs - 1), Sq, Sk, causal);
+  const int nA_max = nA_last > nA_first ? nA_last : nA_first;
+  if ((long long)BH * n_pairs > 2ll * kPlanCtas || nA_max < 2) return sp;
+  const long long unsplit = fwd_plan_makespan(BH, Sq, Sk, causal, D, n_pairs, 0);
+  long long best = unsplit;
+  int best_cap = 0;
+  for (int cap = nA_max - 1; cap >= 1; --cap) {
+    const long long m = fwd_plan_makespan(BH, Sq, Sk, causal, D, n_pairs, cap);
+    if (m < best) {
+      best = m;
+      best_cap = cap;
+    }
+  }
+  if (best_cap == 0 || (double)best * kFwdSplitGain > (double)unsplit) return sp;
+  sp.kcap = best_cap;
+  sp.ctas_y = 0;
+  for (int pr = 0; pr < n_pairs; ++pr) {
+    const int nA = dense_kv_tiles(2 * pr, Sq, Sk, causal);
+    const int parts = nA > best_cap ? ceil_div(nA, best_cap) : 1;
+    sp.ctas_y += parts;
+    if (parts > 1) {
+      sp.parts_per_bh += parts;
+      ++sp.split_pairs;
+    }
+  }
+  return sp;
+}
+
+}  // namespace
+
+FwdSplit fwd_split_plan(int BH, int Sq, int Sk, int causal, int D) {
+  struct Entry {
+    int key[5];
+    FwdSplit plan;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  const int key[5] = {BH, Sq, Sk, causal ? 1 : 0, D};
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry& e : cache)
+      if (std::equal(key, key + 5, e.key)) return e.plan;
+  }
+  const FwdSplit plan = fwd_split_plan_uncached(BH, Sq, Sk, causal, D);
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache.size() < 256) cache.push_back(Entry{{key[0], key[1], key[2], key[3], key[4]}, plan});
+  return plan;
+}
+
+FwdWorkspace fwd_workspace_layout(int B, int Hq, int Sq, int Sk, int D) {
+  FwdWorkspace w{0};
+  int slots = 0;
+  for (int causal = 0; causal < 2; ++causal) {
+    const FwdSplit sp = fwd_split_plan(B * Hq, Sq, Sk, causal, D);
+    if (sp.kcap > 0 && sp.parts_per_bh > slots) slots = sp.parts_per_bh;
+  }
+  if (slots > 0) w.total = align256((size_t)B * Hq * slots * fwd_slot_floats(D) * sizeof(float));
+  return w;
+}
+
+namespace {
+
 template <int D>
 cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
@@ -649,6 +953,13 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.n_ktiles = ceil_div(a.Sk, kTile);
   p.scale_log2 = a.scale_log2;
   p.status = a.status;
+  // Dense forward given a split workspace: the key ranges of the longest pairs may be split.
+  const FwdSplit split = (a.part && !a.cu_q) ? fwd_split_plan(a.B * a.Hq, a.Sq, a.Sk, a.causal, D)
+                                             : FwdSplit{0, ceil_div(a.Sq, 2 * kTile), ceil_div(a.Sq, 2 * kTile), 0, 0};
+  p.kcap = split.kcap;
+  p.n_pairs = split.n_pairs;
+  p.parts_per_bh = split.parts_per_bh;
+  p.part = a.part;
   auto kern = a.rope_cos ? fwd_kernel<D, true> : fwd_kernel<D, false>;
   // The setmaxnreg split must fit the registers the block is launched with, or the
   // increase would wait forever: kernel_setup refuses the launch otherwise.
@@ -657,11 +968,29 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   // Packed batch: one row of CTAs per (sequence, head), enough pairs for the longest sequence.
   const int rows = a.cu_q ? a.max_seqlen_q : a.Sq;
-  dim3 grid((unsigned)(a.B * a.Hq), (unsigned)ceil_div(rows, 2 * kTile));
+  dim3 grid((unsigned)(a.B * a.Hq), (unsigned)(split.kcap > 0 ? split.ctas_y : ceil_div(rows, 2 * kTile)));
   trace_begin(kKernelFwd, stream);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_o, p);
   e = cudaGetLastError();
   trace_end(kKernelFwd, stream);
+  if (e != cudaSuccess || split.split_pairs == 0) return e;
+  // The split pairs' slots are merged into O and LSE.
+  FwdCombineParams cp;
+  cp.part = a.part;
+  cp.o = static_cast<uint16_t*>(a.o);
+  cp.lse = a.lse;
+  cp.Sq = a.Sq;
+  cp.Sk = a.Sk;
+  cp.causal = a.causal;
+  cp.kcap = split.kcap;
+  cp.n_pairs = split.n_pairs;
+  cp.parts_per_bh = split.parts_per_bh;
+  cp.status = a.status;
+  const dim3 cgrid((unsigned)(a.B * a.Hq), (unsigned)(split.split_pairs * 2 * (D / 8)));
+  trace_begin(kKernelFwdCombine, stream);
+  fwd_combine_kernel<D><<<cgrid, 128, 0, stream>>>(cp);
+  e = cudaGetLastError();
+  trace_end(kKernelFwdCombine, stream);
   return e;
 }
 

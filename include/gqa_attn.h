@@ -101,6 +101,27 @@ int gqa_attn_fwd_cached(const void* q, const void* k, const void* v, void* o, fl
                         int Sq, int Sk, int D, int causal, float scale, void* stream);
 
 /*
+ * Forward over a key/value cache (as gqa_attn_fwd_cached; Sq = Sk is the training forward) that
+ * splits the key range of small grids across CTAs. When the grid of query-tile pairs is small (a
+ * prefill of a few hundred tokens over a long cache, short sequences), the key tiles of the longest
+ * pairs are cut into contiguous parts, one CTA each, which leave their running states (m, l, O) in
+ * the workspace; a second kernel on the same stream merges them by the associative combine in part
+ * order: the result equals the unsplit forward's up to f32 rounding and is the same on every call.
+ * Larger grids run the unsplit forward (one kernel).
+ *   workspace: device memory of gqa_attn_fwd_splitkv_workspace_size() bytes (the same sizes),
+ *   256-byte aligned, owned by the caller; its contents need no initialisation and are scratch
+ *   until the call's kernels complete. A size of 0 means no split for these sizes: workspace may
+ *   then be NULL (also accepted for other sizes: the call then runs unsplit).
+ * Errors as gqa_attn_fwd_cached; GQA_ERR_WORKSPACE_TOO_SMALL for a smaller workspace.
+ * Passage: tang page, "How tang works" section 3 (the combine is associative, so the key range
+ * splits and the parts recombine); tang page, "An LLM" (prefill 512).
+ */
+size_t gqa_attn_fwd_splitkv_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D);
+int gqa_attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                         size_t workspace_bytes, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                         float scale, void* stream);
+
+/*
  * Forward over a packed batch of variable-length sequences: the nseq sequences
  * lie end to end along the row axis, sequence i owning query rows
  * cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1 and key/value rows cu_seqlens_k[i] ..

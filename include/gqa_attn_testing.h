@@ -43,7 +43,8 @@ int gqa_attn_selftest_wait_timeout(int limit_us, void* stream);
 #define GQA_KERNEL_BWD_DKDV 6 /* the deterministic backward's dK/dV kernel */
 #define GQA_KERNEL_BWD_DQ 7   /* the deterministic backward's query-major dQ kernel */
 #define GQA_KERNEL_ROPE 8     /* the rotary embedding's rotation pass */
-#define GQA_KERNEL_COUNT 9
+#define GQA_KERNEL_FWD_COMBINE 9 /* the split forward's merge of its parts */
+#define GQA_KERNEL_COUNT 10
 int gqa_attn_trace_arm(void);
 int gqa_attn_trace_collect(int* launches, double* total_ms);
 

@@ -242,3 +242,97 @@ def test_split_parts_cover_every_step_once(B, Hq, Hkv, S, causal):
     lib = _lib.load()
     n = lib.gqa_attn_bwd_workspace_size(B, Hq, Hkv, S, 64)
     assert n >= B * Hkv * parts_per_group * 128 * 64 * 2 * 4
+
+
+def _kv_tiles(qt, Sq, Sk, causal):
+    if qt * 128 >= Sq:
+        return 0
+    if not causal:
+        return -(-Sk // 128)
+    return (Sk - Sq + min(Sq - 1, qt * 128 + 127)) // 128 + 1
+
+
+def _fwd_parts(nA, nB, parts):
+    n_all = max(nA, nB)
+    return [(q * nA // parts, n_all if q == parts - 1 else (q + 1) * nA // parts) for q in range(parts)]
+
+
+def _fwd_slot_floats(D):
+    return 2 * (128 * D + 2 * 128)
+
+
+def _fwd_split_plan(BH, Sq, Sk, causal, D, sms=152):
+    """The forward's key-range split, restated: query-tile pairs (tiles 2p, 2p + 1) whose tile A
+    sees more than `cap` key tiles split into ceil(nA / cap) parts. A CTA costs one unit per
+    (query tile, key tile) product plus 4, plus 2 for a part of a split pair; CTAs are dealt longest
+    first onto 152 SMs; a split adds the merge, 4 units plus one per 3 MiB of slots. The cap with
+    the shortest estimate is taken if it beats the unsplit grid by 15%. Returns (cap, slots per
+    head, split pairs); cap 0: nothing split."""
+    import heapq
+    n_pairs = -(-Sq // 256)
+
+    def makespan(cap):
+        sizes, slots = [], 0
+        for pr in range(n_pairs):
+            nA, nB = _kv_tiles(2 * pr, Sq, Sk, causal), _kv_tiles(2 * pr + 1, Sq, Sk, causal)
+            if nA == 0:
+                continue
+            parts = -(-nA // cap) if cap and nA > cap else 1
+            if parts > 1:
+                slots += parts
+            for kb, ke in _fwd_parts(nA, nB, parts):
+                sizes += [4 + (2 if parts > 1 else 0) + sum((j < nA) + (j < nB) for j in range(kb, ke))] * BH
+        load, span = [0] * sms, 0
+        for sz in sorted(sizes, reverse=True):
+            t = heapq.heappop(load) + sz
+            heapq.heappush(load, t)
+            span = max(span, t)
+        if slots:
+            span += 4 + slots * BH * _fwd_slot_floats(D) * 4 // (3 << 20)
+        return span
+
+    nA_max = max(_kv_tiles(0, Sq, Sk, causal), _kv_tiles(2 * (n_pairs - 1), Sq, Sk, causal))
+    if BH * n_pairs > 2 * sms or nA_max < 2:
+        return 0, 0, 0
+    unsplit = best = makespan(0)
+    best_cap = 0
+    for cap in range(nA_max - 1, 0, -1):
+        m = makespan(cap)
+        if m < best:
+            best, best_cap = m, cap
+    if best_cap == 0 or best * 1.15 > unsplit:
+        return 0, 0, 0
+    slots = pairs = 0
+    for pr in range(n_pairs):
+        nA = _kv_tiles(2 * pr, Sq, Sk, causal)
+        if nA > best_cap:
+            slots += -(-nA // best_cap)
+            pairs += 1
+    return best_cap, slots, pairs
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D", [(1, 4, 2, 300, 300, 64), (2, 6, 3, 700, 700, 128),
+                                              (1, 8, 2, 512, 4096, 128), (1, 32, 8, 512, 16384, 128),
+                                              (2, 32, 8, 2048, 2048, 128), (8, 32, 8, 512, 512, 64)])
+def test_forward_split_parts_and_workspace(B, Hq, Hkv, Sq, Sk, D):
+    """Host logic of the split forward: each part of a pair holds at least one key tile of tile A
+    and at most `cap` of them, the parts cover the pair's key tiles once, in order, and the
+    workspace holds one slot per part (two tiles of 128 x D floats, m and l)."""
+    from causal_gqa_attention_flash_gb300 import _lib
+    lib = _lib.load()
+    slots = 0
+    for causal in (0, 1):
+        cap, s, _ = _fwd_split_plan(B * Hq, Sq, Sk, causal, D)
+        slots = max(slots, s)
+        for pr in range(-(-Sq // 256)):
+            nA, nB = _kv_tiles(2 * pr, Sq, Sk, causal), _kv_tiles(2 * pr + 1, Sq, Sk, causal)
+            parts = _fwd_parts(nA, nB, -(-nA // cap) if cap and nA > cap else 1)
+            assert parts[0][0] == 0 and parts[-1][1] == max(nA, nB)
+            assert all(b == c for (_, b), (c, _) in zip(parts, parts[1:]))
+            assert all(min(nA, b) - a >= 1 and (not cap or min(nA, b) - a <= cap) for a, b in parts)
+    n = lib.gqa_attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Sq, Sk, D)
+    if slots == 0:
+        assert n == 0
+        return
+    assert n == -(-(B * Hq * slots * _fwd_slot_floats(D) * 4) // 256) * 256
+    assert (1, 8, 512, 4096) != (B, Hq, Sq, Sk) or n > 0

@@ -32,6 +32,7 @@ CASES = [
     "tests/test_decode_gpu.py::test_multi_token_causal",
     "tests/test_decode_gpu.py::test_split_counts_agree",
     "tests/test_fwd_cached_gpu.py::test_causal_prefill_over_cache",
+    "tests/test_fwd_cached_gpu.py::test_splitkv_forward",
     "tests/test_deterministic_gpu.py::test_deterministic_parity",
     "tests/test_rope_gpu.py::test_rope_parity",
 ]

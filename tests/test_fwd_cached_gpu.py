@@ -105,3 +105,63 @@ def test_prefill_512_over_16k_sampled_heads():
         O_ref, L_ref = oracle.forward_cached(to_f64(q[b:b + 1, h:h + 1]), to_f64(k[b:b + 1, kh:kh + 1]),
                                              to_f64(v[b:b + 1, kh:kh + 1]))
         assert_fwd_close(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], O_ref, L_ref, f"prefill512 b={b} h={h}")
+
+
+# Sizes whose grid is small enough for the forward to split key ranges: a prefill over a cache,
+# short self-attention (parts of one key tile, rows that see no key of a part), ragged lengths, a
+# single query tile, GQA groupings, D = 64 and 128.
+SPLIT_CASES = [(1, 4, 2, 257, 1000, 64), (2, 4, 4, 130, 900, 128), (1, 8, 2, 512, 4096, 128),
+               (1, 2, 2, 700, 700, 128), (2, 4, 2, 513, 2500, 64), (1, 3, 1, 129, 2000, 128)]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D", SPLIT_CASES)
+@pytest.mark.parametrize("causal", [True, False])
+def test_splitkv_forward(B, Hq, Hkv, Sq, Sk, D, causal):
+    """The split-key-range forward against the oracle; these sizes do split (a workspace is needed),
+    and the result agrees with the unsplit forward over the cache within f32 rounding."""
+    g = gqa()
+    assert g.gqa_attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Sq, Sk, D) > 0
+    q, k, v = _inputs(B, Hq, Hkv, Sq, Sk, D, seed=Sq + Sk + D)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    scale = 1.0 / np.sqrt(D)
+    o, lse = g.gqa_attn_fwd_splitkv(qd, kd, vd, causal=causal, scale=scale)
+    assert g.gqa_attn_get_error() == 0
+    O_ref, L_ref = oracle.forward_cached(to_f64(q), to_f64(k), to_f64(v), causal=causal, scale=scale)
+    assert_fwd_close(o.float().cpu().numpy(), lse.cpu().numpy(), O_ref, L_ref,
+                     f"splitkv B={B} Hq={Hq} Hkv={Hkv} Sq={Sq} Sk={Sk} D={D} causal={causal}")
+    o2, l2 = g.gqa_attn_fwd_cached(qd, kd, vd, causal=causal, scale=scale)
+    assert (o.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (lse - l2).abs().max().item() <= 1e-4
+
+
+def test_splitkv_reproducible_and_workspace_checked():
+    """Two calls give the same bits (the parts merge in part order); a short workspace is refused;
+    the split launches the forward and the merge."""
+    g = gqa()
+    B, Hq, Hkv, Sq, Sk, D = 1, 8, 2, 512, 4096, 128
+    q, k, v = (t.cuda() for t in _inputs(B, Hq, Hkv, Sq, Sk, D, seed=5))
+    need = g.gqa_attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Sq, Sk, D)
+    ws = torch.empty(need, device="cuda", dtype=torch.uint8)
+    g.gqa_attn_trace_arm()
+    r1 = g.gqa_attn_fwd_splitkv(q, k, v, workspace=ws)
+    tr = g.gqa_attn_trace_collect()
+    assert tr["fwd"][0] == 1 and tr["fwd_combine"][0] == 1
+    r2 = g.gqa_attn_fwd_splitkv(q, k, v, workspace=ws)
+    assert torch.equal(r1[0], r2[0]) and torch.equal(r1[1], r2[1])
+    with pytest.raises(g.GqaAttnError) as ei:
+        g.gqa_attn_fwd_splitkv(q, k, v, workspace=ws[:need - 256])
+    assert ei.value.code == g.GQA_ERR_WORKSPACE_TOO_SMALL
+    assert g.gqa_attn_get_error() == 0
+
+
+def test_splitkv_without_split_equals_cached_forward():
+    """Sizes the plan does not split run the ordinary forward: the same bits, no workspace."""
+    g = gqa()
+    B, Hq, Hkv, S, D = 2, 32, 8, 2048, 128
+    assert g.gqa_attn_fwd_splitkv_workspace_size(B, Hq, Hkv, S, S, D) == 0
+    q, k, v = (t.cuda() for t in _inputs(B, Hq, Hkv, S, S, D, seed=9))
+    g.gqa_attn_trace_arm()
+    o1, l1 = g.gqa_attn_fwd_splitkv(q, k, v)
+    assert g.gqa_attn_trace_collect()["fwd_combine"][0] == 0
+    o2, l2 = g.gqa_attn_fwd(q, k, v)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
