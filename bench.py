@@ -247,21 +247,25 @@ def decode_measurement(g, torch, peaks, peak_src, steps=20, warmup=3):
 
 
 PREFILL = dict(B=2, Hq=32, Hkv=8, Sq=512, Sk=16384, D=128, seed=6)
+PREFILL_B1 = dict(B=1, Hq=32, Hkv=8, Sq=512, Sk=16384, D=128, seed=7)
 
 
-def prefill_measurement(g, torch, peaks, peak_src, steps=20, warmup=3):
-    """Tensor-core forward of 512 new tokens per sequence over a 16k-token cache (bottom-right
-    causal): FLOPs are 4 D per visible (query, key) pair, against the measured bf16 burst peak."""
+def prefill_measurement(g, torch, peaks, peak_src, c=PREFILL, steps=20, warmup=3):
+    """Tensor-core forward of Sq new tokens per sequence over an Sk-token cache (bottom-right
+    causal) through gqa_attn_fwd_splitkv, which splits the key ranges when the grid is small (then
+    the forward and the merge kernel both run): FLOPs are 4 D per visible (query, key) pair,
+    against the measured bf16 burst peak."""
     from gqa_inputs import make_inputs
-    c = PREFILL
     _, k, v, _ = make_inputs(c["B"], c["Hq"], c["Hkv"], c["Sk"], c["D"], c["seed"], with_do=False)
     q = make_inputs(c["B"], c["Hq"], c["Hkv"], c["Sq"], c["D"], c["seed"] + 1, with_do=False)[0]
     q, k, v = q.cuda(), k.cuda(), v.cuda()
     o = torch.empty_like(q)
     lse = torch.empty((c["B"], c["Hq"], c["Sq"]), device="cuda", dtype=torch.float32)
+    nws = g.gqa_attn_fwd_splitkv_workspace_size(c["B"], c["Hq"], c["Hkv"], c["Sq"], c["Sk"], c["D"])
+    ws = torch.empty(max(nws, 256), device="cuda", dtype=torch.uint8)
     flush = torch.empty(256 << 20, device="cuda", dtype=torch.uint8)
     for _ in range(warmup):
-        g.gqa_attn_fwd_cached(q, k, v, o=o, lse=lse)
+        g.gqa_attn_fwd_splitkv(q, k, v, o=o, lse=lse, workspace=ws)
     torch.cuda.synchronize()
     total = 0.0
     g.gqa_attn_trace_arm()
@@ -269,7 +273,7 @@ def prefill_measurement(g, torch, peaks, peak_src, steps=20, warmup=3):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        g.gqa_attn_fwd_cached(q, k, v, o=o, lse=lse)
+        g.gqa_attn_fwd_splitkv(q, k, v, o=o, lse=lse, workspace=ws)
         e1.record()
         torch.cuda.synchronize()
         total += e0.elapsed_time(e1)
@@ -282,13 +286,18 @@ def prefill_measurement(g, torch, peaks, peak_src, steps=20, warmup=3):
     fl = 4.0 * c["D"] * pairs * c["B"] * c["Hq"]
     n, t = tr["fwd"]
     kern_ms = t / max(n, 1)
-    achieved = fl / (kern_ms * 1e-3) / 1e12
+    nc, tc = tr["fwd_combine"]
+    comb_ms = tc / max(nc, 1) if nc else 0.0
+    achieved = fl / ((kern_ms + comb_ms) * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    return {"workload": "prefill: B=2 Hq=32 Hkv=8 Sq=512 Sk=16384 D=128 (512 new tokens over a 16k cache, causal)",
+    return {"workload": (f"prefill: B={c['B']} Hq={c['Hq']} Hkv={c['Hkv']} Sq={c['Sq']} Sk={c['Sk']} D={c['D']} "
+                         f"({c['Sq']} new tokens over a {c['Sk'] // 1024}k cache, causal)"),
             "value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "us_per_call": ms * 1e3,
+            "split": {"workspace_bytes": nws, "fwd_us": kern_ms * 1e3, "combine_us": comb_ms * 1e3,
+                      "combine_launches_per_call": nc / steps},
             "l2": "256 MB buffer written between calls",
-            "roofline": {"kernel": "fwd", "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None,
+            "roofline": {"kernel": "fwd + fwd_combine" if nc else "fwd", "bound": "tensor", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
                          "peak_source": f"{peak_src} bf16 dense, burst (kernel timed alone)"}}
 
 
@@ -761,7 +770,8 @@ def main():
         line["rope"] = rope_measurement(g, torch, w, peaks, peak_src, args.steps, args.warmup,
                                         (q, k, v, dO, o, lse, dq, dk, dv, ws), peak_kind)
         line["decode"] = decode_measurement(g, torch, peaks, peak_src)
-        line["prefill"] = prefill_measurement(g, torch, peaks, peak_src)
+        line["prefill"] = prefill_measurement(g, torch, peaks, peak_src, PREFILL)
+        line["prefill_b1"] = prefill_measurement(g, torch, peaks, peak_src, PREFILL_B1)
         line["packed"] = packed_measurement(g, torch, peaks, peak_src)
     if world == 1 and not args.no_cpu_baseline:
         val, desc, cores = cpu_oracle_sample(w)

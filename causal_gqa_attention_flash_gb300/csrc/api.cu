@@ -424,7 +424,7 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
   a.dk = dk;
   a.dv = dv;
   a.dvec = reinterpret_cast<float*>(wsb + ws.dvec_off);
-  a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
+  a.nlse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
   a.dq_acc = reinterpret_cast<float*>(wsb + ws.dqacc_off);
   a.part = reinterpret_cast<float*>(wsb + ws.part_off);
   a.tickets = reinterpret_cast<unsigned*>(wsb + ws.ticket_off);
@@ -546,7 +546,7 @@ int gqa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void*
   a.dk = dk;
   a.dv = dv;
   a.dvec = reinterpret_cast<float*>(wsb + ws.dvec_off);
-  a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
+  a.nlse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
   a.dq_acc = reinterpret_cast<float*>(wsb + ws.dqacc_off);
   a.part = nullptr;  // packed batches split no key tile
   a.tickets = nullptr;

@@ -6,7 +6,7 @@
 // accumulates in f32 (the same article reports a bf16-accumulating fused
 // backward failing the f32 tolerance). Three kernels on one stream:
 //
-//   bwd_prep      D_i = sum_d dO_id O_id (f32), LSE_i * log2(e) (+inf past S),
+//   bwd_prep      D_i = sum_d dO_id O_id (f32), -LSE_i * log2(e) (-inf past S),
 //                 and a zeroed f32 dQ accumulator;                    HBM-bound
 //   bwd_main      one CTA per (batch, KV head, 128-key tile). For every query
 //                 head of the group and every query tile that can see the key
@@ -49,11 +49,11 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 // ------------------------------------------------------------------ prep
 
 // One group of D/8 threads per row: each thread reads 8 bf16 of dO and of O. Rows of the padded
-// arrays past rows_valid, or with s >= S, are padding (D = 0, LSE2 = +inf).
+// arrays past rows_valid, or with s >= S, are padding (D = 0, -LSE2 = -inf).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dO,
                                                        const float* __restrict__ lse, float* __restrict__ dvec,
-                                                       float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                       float* __restrict__ nlse2, float* __restrict__ dq_acc,
                                                        int rows_total, int rows_valid, int S, int S_pad,
                                                        float log2e, long long acc_vec4, unsigned* tickets,
                                                        int n_tickets, int* status) {
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
     if (live && sub == 0 && dbg_range(r, 1, rows_total, status)) {
       dvec[r] = acc;
-      lse2[r] = real ? lse[(size_t)bh * S + s] * log2e : INFINITY;
+      nlse2[r] = real ? -(lse[(size_t)bh * S + s] * log2e) : -INFINITY;
     }
   }
   float4* acc4 = reinterpret_cast<float4*>(dq_acc);
@@ -127,7 +127,7 @@ struct BwdCfg {
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;
   static constexpr int kDSOff = kDOOff + kStages * kTileBytes;         // dS bf16 [128 kv][128 q], MN-major
   static constexpr int kDSBytes = kTile * kTile * 2;
-  static constexpr int kRowOff = kDSOff + kDSBytes;                    // per stage: lse2, dvec rows
+  static constexpr int kRowOff = kDSOff + kDSBytes;                    // per stage: -LSE2, D rows
   static constexpr int kRowFl = 136;                                   // floats per row buffer (>= 4 + 128)
   static constexpr int kBarOff = kRowOff + kStages * 2 * kRowFl * 4;
   static constexpr int kSmemBytes = kBarOff + 256;                     // the base is checked to be 1024-aligned
@@ -155,7 +155,7 @@ static_assert(sizeof(BwdBars<BwdCfg<64>::kStages>) <= 256 && sizeof(BwdBars<BwdC
 static_assert(BwdCfg<64>::kSmemBytes <= 232448 && BwdCfg<128>::kSmemBytes <= 232448, "backward smem over the limit");
 
 struct BwdKParams {
-  const float* lse2;
+  const float* nlse2;  // -LSE * log2(e) rows
   const float* dvec;
   uint16_t* dk;
   uint16_t* dv;
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(352, 1)
         float* srow = reinterpret_cast<float*>(smem + C::kRowOff) + st * 2 * C::kRowFl;
         const size_t roff = rows_at(hl, i) & ~size_t(3);
         if (dbg_range((long long)roff, n_rowfl, p.rows_total, p.status)) {
-          bulk_load(srow, p.lse2 + roff, n_rowfl * 4, bar);
+          bulk_load(srow, p.nlse2 + roff, n_rowfl * 4, bar);
           bulk_load(srow + C::kRowFl, p.dvec + roff, n_rowfl * 4, bar);
         } else {
           mbar_complete_tx(bar, 2 * n_rowfl * 4);
@@ -474,6 +474,7 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t sp_tmem = tbase + lane_off + C::kSPCol;
     const uint32_t dp_tmem = tbase + lane_off + C::kDPCol;
     const float c = p.scale_log2;
+    const float2 c2 = make_float2(c, c);
     const int kv_row = jt * kTile + row;
     const bool kv_valid = kv_row < L;
     uint8_t* sds_half = smem + C::kDSOff + hf * kBoxBytes;  // dS columns [64hf, 64hf+64)
@@ -494,11 +495,11 @@ __global__ void __launch_bounds__(352, 1)
       const int hl = (t_begin + t) / n_i;
       const int i = i_start + (t_begin + t - hl * n_i);
       const int roff = kPacked ? (int)(rows_at(hl, i) & 3) : 0;  // the rows' offset within their widened copy
-      const float* slse = reinterpret_cast<const float*>(smem + C::kRowOff) + st * 2 * C::kRowFl + roff + hf * 64;
-      const float* sdv = slse + C::kRowFl;
+      const float* snl = reinterpret_cast<const float*>(smem + C::kRowOff) + st * 2 * C::kRowFl + roff + hf * 64;
+      const float* sdv = snl + C::kRowFl;
       // visible iff key (jt*128 + row) <= query (i*128 + col): on the diagonal tile, col >= row
       const int first_visible = (p.causal && i == jt) ? row : 0;
-      // Packed: query columns at or past q_limit lie beyond the sequence (dense: LSE2 = +inf there).
+      // Packed: query columns at or past q_limit lie beyond the sequence (dense: -LSE2 = -inf there).
       const int q_limit = kPacked ? L - i * kTile : kTile;
 
       // ---- P^T = exp2(S^T c - LSE2) for the 64 query columns of this half
@@ -520,8 +521,10 @@ __global__ void __launch_bounds__(352, 1)
           for (int x = 0; x < 32; ++x) {
             const int c0 = 2 * x;
             const int col = hf * 64 + c0;
-            const float e0 = ex2_approx(fmaf(__uint_as_float(r[c0]), c, -slse[c0]));
-            const float e1 = ex2_approx(fmaf(__uint_as_float(r[c0 + 1]), c, -slse[c0 + 1]));
+            const float2 a = ffma2(make_float2(__uint_as_float(r[c0]), __uint_as_float(r[c0 + 1])), c2,
+                                   make_float2(snl[c0], snl[c0 + 1]));
+            const float e0 = ex2_approx(a.x);
+            const float e1 = ex2_approx(a.y);
             P[c0] = (kv_valid && col >= first_visible && col < q_limit) ? e0 : 0.f;
             P[c0 + 1] = (kv_valid && col + 1 >= first_visible && col + 1 < q_limit) ? e1 : 0.f;
             pk[x] = pack_bf16(P[c0], P[c0 + 1]);
@@ -530,8 +533,10 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
             const int c0 = 2 * x;
-            P[c0] = ex2_approx(fmaf(__uint_as_float(r[c0]), c, -slse[c0]));
-            P[c0 + 1] = ex2_approx(fmaf(__uint_as_float(r[c0 + 1]), c, -slse[c0 + 1]));
+            const float2 a = ffma2(make_float2(__uint_as_float(r[c0]), __uint_as_float(r[c0 + 1])), c2,
+                                   make_float2(snl[c0], snl[c0 + 1]));
+            P[c0] = ex2_approx(a.x);
+            P[c0 + 1] = ex2_approx(a.y);
             pk[x] = pack_bf16(P[c0], P[c0 + 1]);
           }
         }
@@ -554,9 +559,10 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
           const int c0 = q * 32 + 2 * x;
-          const float ds0 = P[c0] * (__uint_as_float(d[2 * x]) - sdv[c0]);
-          const float ds1 = P[c0 + 1] * (__uint_as_float(d[2 * x + 1]) - sdv[c0 + 1]);
-          pk[x] = pack_bf16(ds0, ds1);
+          const float2 ds = fmul2(make_float2(P[c0], P[c0 + 1]),
+                                  fsub2(make_float2(__uint_as_float(d[2 * x]), __uint_as_float(d[2 * x + 1])),
+                                        make_float2(sdv[c0], sdv[c0 + 1])));
+          pk[x] = pack_bf16(ds.x, ds.y);
         }
         tmem_st_32x32b_x16(sp_tmem + hf * 64 + 32 + q * 16, pk);
         // dS[row = key][col = query] into the MN-major (query-contiguous) 128B-swizzled tile.
@@ -868,7 +874,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     const int blocks = (int)(want < (long long)sms * 8 ? (want < 1 ? 1 : want) : (long long)sms * 8);
     trace_begin(kKernelBwdPrep, stream);
     bwd_prep_kernel<D><<<blocks, threads, 0, stream>>>(
-        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse, a.dvec, a.lse2, a.dq_acc,
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse, a.dvec, a.nlse2, a.dq_acc,
         rows_total, rows_valid, a.S, S_pad, 1.4426950408889634f, acc_elems / 4, a.tickets, n_tickets, a.status);
     cudaError_t e = cudaGetLastError();
     trace_end(kKernelBwdPrep, stream);
@@ -876,7 +882,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   }
   {
     BwdKParams p;
-    p.lse2 = a.lse2;
+    p.nlse2 = a.nlse2;
     p.dvec = a.dvec;
     p.dk = static_cast<uint16_t*>(a.dk);
     p.dv = static_cast<uint16_t*>(a.dv);

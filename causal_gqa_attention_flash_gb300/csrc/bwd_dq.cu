@@ -100,7 +100,7 @@ static_assert(sizeof(DqBarsOf<64>) <= DqCfg<64>::kBarBytes && sizeof(DqBarsOf<12
 static_assert(DqCfg<64>::kSmemBytes <= 232448 && DqCfg<128>::kSmemBytes <= 232448, "dQ kernel smem over the limit");
 
 struct DqKParams {
-  const float* lse2;  // f32 [B*Hq, S_pad]: LSE * log2(e), +inf past S
+  const float* nlse2;  // f32 [B*Hq, S_pad]: -LSE * log2(e), -inf past S
   const float* dvec;  // f32 [B*Hq, S_pad]: D_i = rowsum(dO * O)
   int Hq, Hkv, S, S_pad, causal;
   float scale, scale_log2;
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(320, 1)
     const int qrow = qt * kTile + row;
     const size_t ridx = (size_t)bh * p.S_pad + qrow;  // rows past S: LSE2 = +inf, so P = 0
     const bool r_ok = dbg_range((long long)ridx, 1, (long long)heads_q * p.S_pad, p.status);
-    const float neg_lse2 = r_ok ? -p.lse2[ridx] : 0.f;
+    const float neg_lse2 = r_ok ? p.nlse2[ridx] : 0.f;
     const float dval = r_ok ? p.dvec[ridx] : 0.f;
     const float c = p.scale_log2;
     // Q (warpgroup 0) or dO (warpgroup 1) into TMEM: thread r copies row r out of the
@@ -457,7 +457,7 @@ cudaError_t launch_bwd_dq_d(const BwdArgs& a, cudaStream_t stream) {
   using C = DqCfg<D>;
   const int n_tiles = ceil_div(a.S, kTile);
   DqKParams p;
-  p.lse2 = a.lse2;
+  p.nlse2 = a.nlse2;
   p.dvec = a.dvec;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;

@@ -82,7 +82,7 @@ struct BwdArgs {
   void* dk;                    // bf16 [B, Hkv, S, D]
   void* dv;
   float* dvec;                 // f32 [B*Hq, S_pad]: D_i = rowsum(dO * O)
-  float* lse2;                 // f32 [B*Hq, S_pad]: LSE * log2(e), +inf past S
+  float* nlse2;                // f32 [B*Hq, S_pad]: -LSE * log2(e), -inf past S
   float* dq_acc;               // f32 [B*Hq, S, D]
   float* part;                 // split key tiles' f32 dK / dV partials (dense batches; see BwdSplit)
   unsigned* tickets;           // [B*Hkv*ceil(S/128)] arrival counters of the split key tiles' parts

@@ -226,36 +226,38 @@ __device__ __forceinline__ float row_max_chunked(const uint32_t (&r)[128], int l
 // P = exp2(S c - m) for one row, packed to bf16 pairs and stored into the
 // row's S columns (32 columns per tcgen05.st); returns the row sum of P. The
 // sum runs in eight independent partial sums: the pass is latency-bound, and a
-// two-accumulator chain of 64 dependent adds cost 6% of the forward.
+// two-accumulator chain of 64 dependent adds cost 6% of the forward. The
+// argument and the sums take the paired f32 instructions (two columns each).
 template <bool kMasked>
 __device__ __forceinline__ float exp_pack_store(const uint32_t (&r)[128], int last, float c, float neg_m,
                                                 uint32_t s_tmem) {
-  float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float2 sm[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t pk[16];
 #pragma unroll
     for (int x2 = 0; x2 < 16; ++x2) {
       const int i = q * 32 + 2 * x2;
-      float e0 = ex2_approx(fmaf(__uint_as_float(r[i]), c, neg_m));
-      float e1 = ex2_approx(fmaf(__uint_as_float(r[i + 1]), c, neg_m));
+      const float2 a = ffma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2, nm2);
+      float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
       if (kMasked) {
-        e0 = (i <= last) ? e0 : 0.f;
-        e1 = (i + 1 <= last) ? e1 : 0.f;
+        e.x = (i <= last) ? e.x : 0.f;
+        e.y = (i + 1 <= last) ? e.y : 0.f;
       }
-      sm[(x2 & 3) * 2] += e0;
-      sm[(x2 & 3) * 2 + 1] += e1;
-      pk[x2] = pack_bf16(e0, e1);
+      sm[x2 & 3] = fadd2(sm[x2 & 3], e);
+      pk[x2] = pack_bf16(e.x, e.y);
     }
     tmem_st_32x32b_x16(s_tmem + q * 16, pk);
   }
-  return ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+  return ((sm[0].x + sm[0].y) + (sm[1].x + sm[1].y)) + ((sm[2].x + sm[2].y) + (sm[3].x + sm[3].y));
 }
 
 // exp_pack_store for a masked tile, by 32-column chunks as row_max_chunked.
 __device__ __forceinline__ float exp_pack_store_chunked(const uint32_t (&r)[128], int last, int lo, int hi, float c,
                                                         float neg_m, uint32_t s_tmem) {
-  float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float2 sm[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t pk[16];
@@ -267,20 +269,19 @@ __device__ __forceinline__ float exp_pack_store_chunked(const uint32_t (&r)[128]
 #pragma unroll
       for (int x2 = 0; x2 < 16; ++x2) {
         const int i = q * 32 + 2 * x2;
-        float e0 = ex2_approx(fmaf(__uint_as_float(r[i]), c, neg_m));
-        float e1 = ex2_approx(fmaf(__uint_as_float(r[i + 1]), c, neg_m));
+        const float2 a = ffma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2, nm2);
+        float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
         if (!full) {
-          e0 = (i <= last) ? e0 : 0.f;
-          e1 = (i + 1 <= last) ? e1 : 0.f;
+          e.x = (i <= last) ? e.x : 0.f;
+          e.y = (i + 1 <= last) ? e.y : 0.f;
         }
-        sm[(x2 & 3) * 2] += e0;
-        sm[(x2 & 3) * 2 + 1] += e1;
-        pk[x2] = pack_bf16(e0, e1);
+        sm[x2 & 3] = fadd2(sm[x2 & 3], e);
+        pk[x2] = pack_bf16(e.x, e.y);
       }
     }
     tmem_st_32x32b_x16(s_tmem + q * 16, pk);
   }
-  return ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+  return ((sm[0].x + sm[0].y) + (sm[1].x + sm[1].y)) + ((sm[2].x + sm[2].y) + (sm[3].x + sm[3].y));
 }
 
 // Number of key tiles query tile qt visits; 0 if the tile lies past Sq.

@@ -1,6 +1,6 @@
 """GPU parity at the launch configurations bench.py times beside the main line, on the bench's own
 seeded inputs: split-KV decode (8 sequences, one new token over a 16k cache, split count from the
-cost model), prefill of 512 tokens over a 16k cache, the packed batch of 16 mixed-length
+cost model), prefill of 512 tokens over a 16k cache (B=2, and B=1 with split key ranges), the packed batch of 16 mixed-length
 sequences, the rotary-embedding step at long16k and the deterministic backward at long16k.
 
 Where the oracle cannot evaluate every element in seconds it evaluates sampled rows one by one.
@@ -38,20 +38,23 @@ def test_decode_bench_config_all_rows():
     assert_fwd_close(o.float().cpu().numpy(), lse.cpu().numpy(), O_ref, L_ref, "decode bench config")
 
 
-def test_prefill_bench_config_sampled_heads():
-    """bench.PREFILL (512 new tokens over a 16384-key cache): three (batch, head) pairs in full."""
+@pytest.mark.parametrize("name", ["PREFILL", "PREFILL_B1"])
+def test_prefill_bench_config_sampled_heads(name):
+    """bench.PREFILL (B=2) and bench.PREFILL_B1 (B=1, whose key ranges split): 512 new tokens over
+    a 16384-key cache through gqa_attn_fwd_splitkv, as the bench launches it; three (batch, head)
+    pairs in full."""
     g = gqa()
-    c = bench.PREFILL
+    c = getattr(bench, name)
     _, k, v, _ = make_inputs(c["B"], c["Hq"], c["Hkv"], c["Sk"], c["D"], c["seed"], with_do=False)
     q = make_inputs(c["B"], c["Hq"], c["Hkv"], c["Sq"], c["D"], c["seed"] + 1, with_do=False)[0]
-    o, lse = g.gqa_attn_fwd_cached(q.cuda(), k.cuda(), v.cuda())
+    o, lse = g.gqa_attn_fwd_splitkv(q.cuda(), k.cuda(), v.cuda())
     assert g.gqa_attn_get_error() == 0
     o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
-    for b, h in ((0, 0), (1, 13), (1, c["Hq"] - 1)):
+    for b, h in ((0, 0), (c["B"] - 1, 13), (c["B"] - 1, c["Hq"] - 1)):
         kh = oracle.kv_head_of(h, c["Hq"], c["Hkv"])
         O_ref, L_ref = oracle.forward_cached(to_f64(q[b:b + 1, h:h + 1]), to_f64(k[b:b + 1, kh:kh + 1]),
                                              to_f64(v[b:b + 1, kh:kh + 1]))
-        assert_fwd_close(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], O_ref, L_ref, f"prefill b={b} h={h}")
+        assert_fwd_close(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], O_ref, L_ref, f"{name} b={b} h={h}")
 
 
 def test_packed_bench_batch_sequences():
