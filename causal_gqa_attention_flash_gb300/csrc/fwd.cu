@@ -74,8 +74,8 @@ struct FwdCfg {
 template <int KST, int VST>
 struct FwdBars {
   uint64_t q_full[2];  // Q_A, Q_B (separate, so that S_A(0) need not wait for Q_B)
-  uint64_t k_full[KST];
-  uint64_t v_full[VST];
+  uint64_t kv_full[KST];  // K_j and V_j both landed (indexed by K_j's stage); for j = 0, V_0 only
+  uint64_t k0_full;       // K_0, so that the first S products need not wait for V_0
   uint64_t k_empty[KST];
   uint64_t v_empty[VST];
   uint64_t s_full[2];
@@ -357,13 +357,11 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bars->q_full[0], 1);
     mbar_init(&bars->q_full[1], 1);
     for (int s = 0; s < ST; ++s) {
-      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
     }
-    for (int s = 0; s < VST; ++s) {
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
-    }
+    for (int s = 0; s < VST; ++s) mbar_init(&bars->v_empty[s], 1);
+    mbar_init(&bars->k0_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 4);  // one arrival per softmax warp
@@ -387,12 +385,13 @@ __global__ void __launch_bounds__(384, 1)
   if (warp >= 8) {
    setmaxnreg_dec<C::kLowRegs>();
    if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer: Q, then the K ring
+    // ------------------------------------------------------------ TMA producer: Q, then the K and V rings
     if (lane == 0) {
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
-      // Q_A, then K_0, then Q_B (only when tile B has rows; its buffer is otherwise never read):
-      // the first S MMA waits for the first 64 KB, not for 96 KB.
+      tma_prefetch_desc(&map_v);
+      // Q_A, then K_0, then Q_B (only when tile B has rows; its buffer is otherwise never read),
+      // then V_0: the first S products wait for Q and K_0 only.
       auto load_q = [&](int t) {
         mbar_arrive_expect_tx(&bars->q_full[t], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
@@ -405,54 +404,40 @@ __global__ void __launch_bounds__(384, 1)
       load_q(0);
       bool q_b_issued = false;
       int issued = 0;
+      // K_j and V_j land on one barrier, kv_full[j % ST]: the MMA issuer waits once per key tile.
+      // A stage of K is reused only after both S products that read it completed, which comes
+      // after the issuer's wait on that barrier's previous phase.
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j % ST;
-        const int use = j / ST;
-        if (use > 0 && !mbar_wait(&bars->k_empty[st], (use - 1) & 1, wg)) break;
-        mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-          const int r = g.k_row0 + (kb + j) * kTile;
-          tma_load_3d_chk(smem + C::kKOff + st * C::kTileBytes + c * kBoxBytes, &map_k, &bars->k_full[st],
+        const int st = j % ST, vst = j % VST;
+        if (j >= ST && !mbar_wait(&bars->k_empty[st], ((j / ST) - 1) & 1, wg)) break;
+        if (j >= VST && !mbar_wait(&bars->v_empty[vst], ((j / VST) - 1) & 1, wg)) break;
+        uint64_t* kbar = j == 0 ? &bars->k0_full : &bars->kv_full[st];
+        mbar_arrive_expect_tx(&bars->kv_full[st], (j == 0 ? 1 : 2) * C::kTileBytes);
+        if (j == 0) mbar_arrive_expect_tx(kbar, C::kTileBytes);
+        const int r = g.k_row0 + (kb + j) * kTile;
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d_chk(smem + C::kKOff + st * C::kTileBytes + c * kBoxBytes, &map_k, kbar,
                           c * kChunk, r, g.kv_coord,
                           dbg_tile(c * kChunk, r, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv,
                                    p.status));
-        }
-        issued = j + 1;
-        if (j == 0 && nB > 0) {
+        if (j == 0 && nB > 0) {  // Q_B between K_0 and V_0
           load_q(1);
           q_b_issued = true;
         }
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d_chk(smem + C::kVOff + vst * C::kTileBytes + c * kBoxBytes, &map_v, &bars->kv_full[st],
+                          c * kChunk, r, g.kv_coord,
+                          dbg_tile(c * kChunk, r, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv,
+                                   p.status));
+        issued = j + 1;
       }
       if (bars->abort_flag) {
         // Let every copy already issued land before the CTA's shared memory goes away.
         mbar_wait_drain(&bars->q_full[0], 0, kWaitLimitNs);
         if (q_b_issued) mbar_wait_drain(&bars->q_full[1], 0, kWaitLimitNs);
+        if (issued > 0) mbar_wait_drain(&bars->k0_full, 0, kWaitLimitNs);
         for (int j = (issued > ST ? issued - ST : 0); j < issued; ++j)
-          mbar_wait_drain(&bars->k_full[j % ST], (j / ST) & 1, kWaitLimitNs);
-      }
-    }
-   } else if (warp == 10) {
-    // ------------------------------------------------------------ TMA producer: the V ring
-    if (lane == 0) {
-      tma_prefetch_desc(&map_v);
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % VST;
-        const int use = j / VST;
-        if (use > 0 && !mbar_wait(&bars->v_empty[st], (use - 1) & 1, wg)) break;
-        mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-          const int r = g.k_row0 + (kb + j) * kTile;
-          tma_load_3d_chk(smem + C::kVOff + st * C::kTileBytes + c * kBoxBytes, &map_v, &bars->v_full[st],
-                          c * kChunk, r, g.kv_coord,
-                          dbg_tile(c * kChunk, r, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv,
-                                   p.status));
-        }
-        issued = j + 1;
-      }
-      if (bars->abort_flag) {
-        for (int j = (issued > VST ? issued - VST : 0); j < issued; ++j)
-          mbar_wait_drain(&bars->v_full[j % VST], (j / VST) & 1, kWaitLimitNs);
+          mbar_wait_drain(&bars->kv_full[j % ST], (j / ST) & 1, kWaitLimitNs);
       }
     }
   } else if (warp == 9) {
@@ -480,8 +465,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         umma_commit(&bars->s_full[x]);
       };
-      // O_X += P_X(j) V_j, P_X(j) read from the S columns of tile X.
-      auto issue_pv = [=](int x, int j) {
+      // O_X += P_X(j) V_j, P_X(j) read from the S columns of tile X. O_X is signalled complete
+      // after its last product only: within the loop, S_X(j + 1) completing (issued after
+      // P_X(j) V_j by this thread) already tells the softmax warps that O_X holds P_X(j) V_j.
+      auto issue_pv = [=](int x, int j, bool last) {
         const uint64_t bv = dv0 + (uint64_t)(j % VST) * kTileDesc;
         const uint32_t p_tmem = tbase + (uint32_t)x * 128u;
         const uint32_t o_tmem = tbase + C::kOCol + (uint32_t)x * D;
@@ -489,11 +476,13 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_ts(o_tmem, p_tmem + (uint32_t)kk * 8u, bv + (uint64_t)((kk * 2048) >> 4), idesc_o,
                   (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars->o_done[x]);
+        if (last) umma_commit(&bars->o_done[x]);
       };
       // K_j is released once the last S MMA reading it completes, V_j once both P V MMAs do:
-      // the K ring refills a full key tile earlier than a shared K/V stage would.
-      bool ok = mbar_wait(&bars->q_full[0], 0, wg) && mbar_wait(&bars->k_full[0], 0, wg);
+      // the K ring refills a full key tile earlier than a shared K/V stage would. Each key tile
+      // costs one wait (kv_full) here: a wait on a barrier, even one already complete, stalls
+      // this thread for a few hundred cycles, and the tensor core holds about one MMA in its queue.
+      bool ok = mbar_wait(&bars->q_full[0], 0, wg) && mbar_wait(&bars->k0_full, 0, wg);
       if (kRope && ok) ok = mbar_wait(&bars->q_ready[0], 0, wg);  // the softmax warps rotate their queries first
       if (ok) {
         tc_fence_after();
@@ -506,18 +495,22 @@ __global__ void __launch_bounds__(384, 1)
           issue_s(1, 0);
         }
       }
+      // V_j landed with K_j, before S(j) was issued: P(j) V_j needs no wait of its own, but V_0
+      // does. Its wait comes before K_0's stage is released: the producer arms kv_full[0] again
+      // for K_ST only after that release, and arming a barrier whose phase is still open would
+      // add an arrival that phase does not expect.
+      if (ok) ok = mbar_wait(&bars->kv_full[0], 0, wg);
       if (ok) umma_commit(&bars->k_empty[0]);
       for (int j = 0; ok && j < n_kv; ++j) {
         const int vst = j % VST;
         const int j1 = j + 1;
         const int st1 = j1 % ST;
-        if (!(ok = mbar_wait(&bars->v_full[vst], (j / VST) & 1, wg))) break;
         if (j < nA) {
           if (!(ok = mbar_wait(&bars->p_full[0], j & 1, wg))) break;
           tc_fence_after();
-          issue_pv(0, j);
+          issue_pv(0, j, j1 == nA);
           if (j1 < nA) {
-            if (!(ok = mbar_wait(&bars->k_full[st1], (j1 / ST) & 1, wg))) break;
+            if (!(ok = mbar_wait(&bars->kv_full[st1], (j1 / ST) & 1, wg))) break;
             tc_fence_after();
             issue_s(0, j1);
           }
@@ -525,9 +518,9 @@ __global__ void __launch_bounds__(384, 1)
         if (j < nB) {
           if (!(ok = mbar_wait(&bars->p_full[1], j & 1, wg))) break;
           tc_fence_after();
-          issue_pv(1, j);
-          if (j1 < nB) {  // K_{j+1} was already waited for when tile A uses it too
-            if (j1 >= nA && !(ok = mbar_wait(&bars->k_full[st1], (j1 / ST) & 1, wg))) break;
+          issue_pv(1, j, j1 == nB);
+          if (j1 < nB) {  // K_{j+1} and V_{j+1} were already waited for when tile A uses them too
+            if (j1 >= nA && !(ok = mbar_wait(&bars->kv_full[st1], (j1 / ST) & 1, wg))) break;
             tc_fence_after();
             issue_s(1, j1);
           }
@@ -613,11 +606,9 @@ __global__ void __launch_bounds__(384, 1)
       l = l * alpha + rsum;
 
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O_X holds the sum up to tile j-1 against the old reference. P_X(j-1) V_{j-1} completed
-        // before S_X(j) did (same in-order MMA stream); the wait below returns at once.
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[x], (j - 1) & 1, wg));
-        if (!ok) break;
-        tc_fence_after();
+        // O_X holds the sum up to tile j-1 against the old reference: P_X(j-1) V_{j-1} completed
+        // before S_X(j) did (one thread issued both, in that order, and the commit that signalled
+        // S_X(j) tracks every MMA it issued before).
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -632,7 +623,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive_warp(&bars->p_full[x]);
     }
-    if (ok && n_x > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[x], (n_x - 1) & 1, wg));
+    if (ok && n_x > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[x], 0, wg));
     if (ok && n_x > 0 && sp.parts > 1) {
       // Split key range: this part's unnormalised O tile X and its (m, l) go to the part's slot
       // (m = -inf for a row that saw no key in the range). A warp's stores cover 32 consecutive
