@@ -140,8 +140,10 @@ struct BwdCfg {
 template <int ST>
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t qdo_full[ST];
-  uint64_t qdo_empty[ST];
+  uint64_t q_full[ST];   // Q(t) and the step's -LSE2 / D rows landed
+  uint64_t do_full[ST];  // dO(t) landed
+  uint64_t q_empty[ST];  // the Q stage may be refilled
+  uint64_t do_empty[ST]; // the dO stage may be refilled
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free, stage_full, dkv_done, drain;
   uint64_t k_ready;  // rotary embedding: the key tile rotated in shared memory
   uint64_t epi_bar;  // split key tiles: barrier of the element-wise warps around the partials' ticket
@@ -288,8 +290,10 @@ __global__ void __launch_bounds__(352, 1)
   if (tid == 0) {
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < ST; ++s) {
-      mbar_init(&bars->qdo_full[s], 1);
-      mbar_init(&bars->qdo_empty[s], 1);  // the reduce warp, once its dQ reduces have read the stage
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->do_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);   // the reduce warp, once its dQ reduces have read the stage
+      mbar_init(&bars->do_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
@@ -329,21 +333,22 @@ __global__ void __launch_bounds__(352, 1)
         tma_load_3d_chk(smem + C::kVOff + c * kBoxBytes, &map_v, &bars->kv_full, c * kChunk, row0 + jt * kTile,
                         kv_coord, kv_ok);
       }
-      int issued = 0;
+      int issued = 0, issued_do = 0;
       for (int t = 0; t < n_steps; ++t) {
         const int st = t % ST;
         const int use = t / ST;
-        if (use > 0 && !mbar_wait(&bars->qdo_empty[st], (use - 1) & 1, wg)) break;
         const int hl = (t_begin + t) / n_i;
         const int i = i_start + (t_begin + t - hl * n_i);
         const int bhq = bhq0 + hl;
-        uint64_t* bar = &bars->qdo_full[st];
-        mbar_arrive_expect_tx(bar, 2 * C::kTileBytes + 2 * n_rowfl * 4);
+        // Q(t) and the rows, then dO(t): the two stages are handed back separately (the reduce
+        // warp reads the dQ partial out of the Q stage first), so that Q(t + ST) is on its way
+        // while the dO half of the partial is still being read.
+        if (use > 0 && !mbar_wait(&bars->q_empty[st], (use - 1) & 1, wg)) break;
+        uint64_t* bar = &bars->q_full[st];
+        mbar_arrive_expect_tx(bar, C::kTileBytes + 2 * n_rowfl * 4);
         for (int c = 0; c < C::kChunks; ++c) {
           const bool q_ok = dbg_tile(c * kChunk, row0 + i * kTile, bhq, D, kChunk, row0, row0 + L, heads_q, p.status);
           tma_load_3d_chk(smem + C::kQOff + st * C::kTileBytes + c * kBoxBytes, &map_q, bar, c * kChunk,
-                          row0 + i * kTile, bhq, q_ok);
-          tma_load_3d_chk(smem + C::kDOOff + st * C::kTileBytes + c * kBoxBytes, &map_do, bar, c * kChunk,
                           row0 + i * kTile, bhq, q_ok);
         }
         float* srow = reinterpret_cast<float*>(smem + C::kRowOff) + st * 2 * C::kRowFl;
@@ -355,11 +360,22 @@ __global__ void __launch_bounds__(352, 1)
           mbar_complete_tx(bar, 2 * n_rowfl * 4);
         }
         issued = t + 1;
+        if (use > 0 && !mbar_wait(&bars->do_empty[st], (use - 1) & 1, wg)) break;
+        bar = &bars->do_full[st];
+        mbar_arrive_expect_tx(bar, C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+          const bool q_ok = dbg_tile(c * kChunk, row0 + i * kTile, bhq, D, kChunk, row0, row0 + L, heads_q, p.status);
+          tma_load_3d_chk(smem + C::kDOOff + st * C::kTileBytes + c * kBoxBytes, &map_do, bar, c * kChunk,
+                          row0 + i * kTile, bhq, q_ok);
+        }
+        issued_do = t + 1;
       }
       if (bars->abort_flag) {
         mbar_wait_drain(&bars->kv_full, 0, kWaitLimitNs);
         for (int t = (issued > ST ? issued - ST : 0); t < issued; ++t)
-          mbar_wait_drain(&bars->qdo_full[t % ST], (t / ST) & 1, kWaitLimitNs);
+          mbar_wait_drain(&bars->q_full[t % ST], (t / ST) & 1, kWaitLimitNs);
+        for (int t = (issued_do > ST ? issued_do - ST : 0); t < issued_do; ++t)
+          mbar_wait_drain(&bars->do_full[t % ST], (t / ST) & 1, kWaitLimitNs);
       }
     }
   } else if (warp == 9) {
@@ -391,12 +407,16 @@ __global__ void __launch_bounds__(352, 1)
       // TMEM column of the A operand (P^T; dS^T is 32 columns further) for query rows 16kk..16kk+15:
       // column half h = kk / 4 keeps its packed P^T in [64h, 64h+32) and dS^T in [64h+32, 64h+64).
       auto p_col = [](int kk) { return (uint32_t)(kk >> 2) * 64u + (uint32_t)(kk & 3) * 8u; };
-      bool ok = mbar_wait(&bars->kv_full, 0, wg) && mbar_wait(&bars->qdo_full[0], 0, wg);
+      bool ok = mbar_wait(&bars->kv_full, 0, wg) && mbar_wait(&bars->q_full[0], 0, wg);
       if (kRope && ok) ok = mbar_wait(&bars->k_ready, 0, wg);  // keys rotated by the element-wise warps
       if (ok) {
         tc_fence_after();
         issue_kmajor(C::kSPCol, dk_k, stage_desc(dq_k0, 0));
         umma_commit(&bars->s_full);
+      }
+      if (ok) ok = mbar_wait(&bars->do_full[0], 0, wg);
+      if (ok) {
+        tc_fence_after();
         issue_kmajor(C::kDPCol, dv_k, stage_desc(ddo_k0, 0));
         umma_commit(&bars->dp_full);
       }
@@ -420,18 +440,20 @@ __global__ void __launch_bounds__(352, 1)
                     idesc_mm, kk > 0 ? 1u : 0u);
           umma_commit(&bars->dq_full);
         } else {
-          umma_commit(&bars->qdo_empty[t % ST]);  // dK(t) and dV(t) were the last readers of Q(t), dO(t)
+          umma_commit(&bars->q_empty[t % ST]);  // dK(t) and dV(t) were the last readers of Q(t), dO(t)
+          umma_commit(&bars->do_empty[t % ST]);
         }
         if (t + 1 < n_steps) {
           const int t1 = t + 1;
-          if (!(ok = mbar_wait(&bars->qdo_full[t1 % ST], (t1 / ST) & 1, wg))) break;
+          if (!(ok = mbar_wait(&bars->q_full[t1 % ST], (t1 / ST) & 1, wg))) break;
           tc_fence_after();
           issue_kmajor(C::kSPCol, dk_k, stage_desc(dq_k0, t1));  // P^T(t), dS^T(t) were consumed by dV(t), dK(t)
           umma_commit(&bars->s_full);
           if (kDq) {  // dP(t+1) overwrites the dQ(t) partial: wait until it has been read out
             if (!(ok = mbar_wait(&bars->dq_free, t & 1, wg))) break;
-            tc_fence_after();
           }
+          if (!(ok = mbar_wait(&bars->do_full[t1 % ST], (t1 / ST) & 1, wg))) break;
+          tc_fence_after();
           issue_kmajor(C::kDPCol, dv_k, stage_desc(ddo_k0, t1));
           umma_commit(&bars->dp_full);
         }
@@ -452,16 +474,21 @@ __global__ void __launch_bounds__(352, 1)
         const int hl = (t_begin + t) / n_i;
         const int i = i_start + (t_begin + t - hl * n_i);
         const int bhq = bhq0 + hl;
+        // The slices in the Q stage go first, in their own bulk group, so that the Q stage is
+        // handed back once they have been read; then those in the dO stage.
 #pragma unroll
         for (int s2 = 0; s2 < D / 32; ++s2) {
           const uint8_t* stage = s2 < C::kChunks ? smem + C::kQOff + st * C::kTileBytes + s2 * kBoxBytes
                                                  : smem + C::kDOOff + st * C::kTileBytes + (s2 - C::kChunks) * kBoxBytes;
           if (dbg_tile(s2 * 32, row0 + i * kTile, bhq, D, 32, row0, row0 + L, heads_q, p.status))
             tma_reduce_add_3d(&map_acc, stage, s2 * 32, row0 + i * kTile, bhq);
+          if (s2 == C::kChunks - 1) bulk_commit_group();
         }
         bulk_commit_group();
+        bulk_wait_group_read<1>();
+        mbar_arrive(&bars->q_empty[st]);
         bulk_wait_group_read<0>();
-        mbar_arrive(&bars->qdo_empty[st]);
+        mbar_arrive(&bars->do_empty[st]);
       }
       bulk_wait_group<0>();
     }
