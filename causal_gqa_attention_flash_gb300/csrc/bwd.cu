@@ -839,6 +839,11 @@ BwdSplit bwd_split_plan_uncached(int B, int Hkv, int G, int n_tiles, int causal)
   long long best = unsplit;
   int best_cap = 0;
   for (int cap = steps0 - 1; cap >= 1; --cap) {
+    // Grids of more than four waves are not considered; smaller caps only add CTAs, so the
+    // search (and its host time on a first call) stops there.
+    long long ctas = 0;
+    for (int jt = 0; jt < n_tiles; ++jt) ctas += ceil_div(bwd_tile_steps(jt, n_tiles, G, causal), cap);
+    if ((long long)B * Hkv * ctas > 4ll * kPlanCtas) break;
     const long long m = bwd_plan_makespan(B, Hkv, G, n_tiles, causal, cap);
     if (m < best) {
       best = m;

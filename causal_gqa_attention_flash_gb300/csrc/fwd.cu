@@ -868,6 +868,14 @@ FwdSplit fwd_split_plan_uncached(int BH, int Sq, int Sk, int causal, int D) {
   long long best = unsplit;
   int best_cap = 0;
   for (int cap = nA_max - 1; cap >= 1; --cap) {
+    // Grids of more than four waves are not considered; smaller caps only add CTAs, so the
+    // search (and its host time on a first call) stops there.
+    long long ctas = 0;
+    for (int pr = 0; pr < n_pairs; ++pr) {
+      const int nA = dense_kv_tiles(2 * pr, Sq, Sk, causal);
+      ctas += nA > cap ? ceil_div(nA, cap) : (nA > 0 ? 1 : 0);
+    }
+    if ((long long)BH * ctas > 4ll * kPlanCtas) break;
     const long long m = fwd_plan_makespan(BH, Sq, Sk, causal, D, n_pairs, cap);
     if (m < best) {
       best = m;

@@ -205,6 +205,8 @@ def _split_plan(B, Hkv, G, n_tiles, causal):
     unsplit = best = _makespan(B, Hkv, G, n_tiles, causal, 0)
     best_cap = 0
     for cap in range(steps0 - 1, 0, -1):
+        if B * Hkv * sum(-(-_tile_steps(jt, n_tiles, G, causal) // cap) for jt in range(n_tiles)) > 4 * 152:
+            break  # grids of more than four waves are not considered
         m = _makespan(B, Hkv, G, n_tiles, causal, cap)
         if m < best:
             best, best_cap = m, cap
@@ -297,6 +299,10 @@ def _fwd_split_plan(BH, Sq, Sk, causal, D, sms=152):
     unsplit = best = makespan(0)
     best_cap = 0
     for cap in range(nA_max - 1, 0, -1):
+        ctas = sum((-(-nA // cap) if nA > cap else (1 if nA > 0 else 0))
+                   for nA in (_kv_tiles(2 * pr, Sq, Sk, causal) for pr in range(n_pairs)))
+        if BH * ctas > 4 * sms:
+            break  # grids of more than four waves are not considered
         m = makespan(cap)
         if m < best:
             best, best_cap = m, cap
@@ -336,3 +342,15 @@ def test_forward_split_parts_and_workspace(B, Hq, Hkv, Sq, Sk, D):
         return
     assert n == -(-(B * Hq * slots * _fwd_slot_floats(D) * 4) // 256) * 256
     assert (1, 8, 512, 4096) != (B, Hq, Sq, Sk) or n > 0
+
+
+def test_split_plans_are_quick_for_long_key_ranges(lib):
+    """The split plans search key-range caps on a first call for each size; the search stops at
+    four waves, so a very long cache over a small grid plans in well under a second."""
+    import time
+    t0 = time.perf_counter()
+    for B, Hq, Hkv, Sq, Sk in ((1, 1, 1, 128, 1 << 20), (1, 8, 1, 200, 1 << 19), (19, 8, 2, 256, 1 << 18)):
+        n = lib.gqa_attn_fwd_splitkv_workspace_size(B, Hq, Hkv, Sq, Sk, 128)
+        assert n % 256 == 0
+    lib.gqa_attn_bwd_workspace_size(1, 64, 1, 8192, 64)  # 64 query heads on one KV head: long key tiles
+    assert time.perf_counter() - t0 < 2.0
