@@ -456,8 +456,9 @@ CONFIG_NAMES = ("tiny", "lm101m", "block512", "qwen3_8b", "long16k")
 
 def config_measurement(g, torch, w, peaks, reps=20, warmup=3):
     """fwd, bwd and fwd+bwd of one workload, each timed alone: TFLOP/s (algorithmic flops), the
-    per-kernel averages from the library's own CUDA events, the gap between the measured time and
-    the sum of kernel times (launch and host cost), and the host time one call takes to enqueue.
+    per-kernel averages from the library's own CUDA events (a second, traced pass), the gap between
+    the measured time and the sum of kernel times (launch cost; negative where consecutive kernels
+    overlap under programmatic dependent launch), and the host time one call takes to enqueue.
     Inputs smaller than L2 get a 256 MB buffer written between timed iterations (each iteration is
     timed on its own); larger ones run back to back."""
     from gqa_inputs import make_inputs
@@ -484,12 +485,15 @@ def config_measurement(g, torch, w, peaks, reps=20, warmup=3):
     fwd_fl, bwd_fl = flops(w.B, w.Hq, w.S, w.D)
     out = {"shape": config_of(w)["workload"],
            "l2": "256 MB buffer written between timed iterations" if small else "inputs larger than L2"}
-    for label, fn, fl in (("fwd", fwd, fwd_fl), ("bwd", bwd, bwd_fl), ("fwd_bwd", both, fwd_fl + bwd_fl)):
-        for _ in range(warmup):
-            fn()
+
+    def timed(fn, traced):
+        """Mean ms per call over `reps` calls (and host seconds spent enqueueing them); with
+        `traced`, the library's per-kernel events are armed as well (they sit between the
+        kernels, so the call times come from a pass without them)."""
         torch.cuda.synchronize()
         host_s = 0.0
-        g.gqa_attn_trace_arm()
+        if traced:
+            g.gqa_attn_trace_arm()
         if small:
             total = 0.0
             for _ in range(reps):
@@ -512,15 +516,21 @@ def config_measurement(g, torch, w, peaks, reps=20, warmup=3):
             e1.record(stream)
             torch.cuda.synchronize()
             total = e0.elapsed_time(e1)
-        tr = g.gqa_attn_trace_collect()
+        tr = g.gqa_attn_trace_collect() if traced else None
+        return total / reps, host_s / reps, tr
+
+    for label, fn, fl in (("fwd", fwd, fwd_fl), ("bwd", bwd, bwd_fl), ("fwd_bwd", both, fwd_fl + bwd_fl)):
+        for _ in range(warmup):
+            fn()
+        ms, host_s, _ = timed(fn, False)
+        _, _, tr = timed(fn, True)
         rc = g.gqa_attn_get_error()
         if rc != 0:
             raise RuntimeError(f"{w.name} {label} failed: {g.gqa_attn_strerror(rc)}")
-        ms = total / reps
-        kern = {name: t_ / reps for name, (n_, t_) in tr.items() if n_}
+        kern = {name: t_ / reps for name, (n_, t_) in tr.items() if n_}  # kernel ms per call
         out[label] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                       "kernel_ms": kern, "gap_ms": ms - sum(kern.values()),
-                      "host_us_per_call": host_s / reps * 1e6}
+                      "host_us_per_call": host_s * 1e6}
     # the two contraction kernels alone, by their own events
     kf = out["fwd_bwd"]["kernel_ms"]
     out["fwd_kernel_tflops"] = fwd_fl / (kf["fwd"] * 1e-3) / 1e12

@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
                                                        int n_tickets, int* status) {
   constexpr int TPR = D / 8;            // threads per row
   constexpr int RPW = 32 / TPR;          // rows per warp and iteration
+  griddep_wait();  // O and LSE come from the forward, which may be just ahead in the stream
+  griddep_launch_dependents();
   const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
   const int nthreads = gridDim.x * blockDim.x;
   const int lane = threadIdx.x & 31;
@@ -101,6 +103,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
 
 __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq,
                                                           long long n8, float scale) {
+  griddep_wait();  // the accumulator is complete once the main kernel ahead of this one is
+  griddep_launch_dependents();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
     const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
@@ -227,6 +231,8 @@ __global__ void __launch_bounds__(352, 1)
   constexpr int ST = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   auto* bars = reinterpret_cast<BwdBars<ST>*>(smem + C::kBarOff);
+  griddep_wait();  // the D / -LSE2 rows and the zeroed accumulator come from the kernel ahead
+  griddep_launch_dependents();
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -905,10 +911,10 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     long long want = ((long long)rows_total * (D / 8) + threads - 1) / threads;
     const int blocks = (int)(want < (long long)sms * 8 ? (want < 1 ? 1 : want) : (long long)sms * 8);
     trace_begin(kKernelBwdPrep, stream);
-    bwd_prep_kernel<D><<<blocks, threads, 0, stream>>>(
+    cudaError_t e = launch_pdl(bwd_prep_kernel<D>, dim3(blocks), dim3(threads), 0, stream,
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse, a.dvec, a.nlse2, a.dq_acc,
         rows_total, rows_valid, a.S, S_pad, 1.4426950408889634f, acc_elems / 4, a.tickets, n_tickets, a.status);
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     trace_end(kKernelBwdPrep, stream);
     if (e != cudaSuccess) return e;
   }
@@ -948,8 +954,9 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     const dim3 grid = packed ? dim3((unsigned)packed_ctas)
                              : dim3((unsigned)(a.B * a.Hkv), (unsigned)(split.cap > 0 ? split.ctas_per_group : n_tiles));
     trace_begin(kind, stream);
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_do, *a.map_dqacc, p);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, stream, *a.map_q, *a.map_k, *a.map_v, *a.map_do,
+                   *a.map_dqacc, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     trace_end(kind, stream);
     if (e != cudaSuccess) return e;
   }
@@ -963,8 +970,9 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
     long long want = (n8 + threads - 1) / threads;
     const int blocks = (int)(want < (long long)sms * 8 ? (want < 1 ? 1 : want) : (long long)sms * 8);
     trace_begin(kKernelBwdConvert, stream);
-    bwd_convert_kernel<<<blocks, threads, 0, stream>>>(a.dq_acc, static_cast<uint16_t*>(a.dq), n8, a.scale);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(bwd_convert_kernel, dim3(blocks), dim3(threads), 0, stream, a.dq_acc,
+                               static_cast<uint16_t*>(a.dq), n8, a.scale);
+    if (e == cudaSuccess) e = cudaGetLastError();
     trace_end(kKernelBwdConvert, stream);
     return e;
   }

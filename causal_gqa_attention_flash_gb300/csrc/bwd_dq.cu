@@ -131,6 +131,8 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   auto* bars = reinterpret_cast<DqBarsOf<D>*>(smem + C::kBarOff);
+  griddep_wait();  // the D / -LSE2 rows come from the prep kernel, two launches ahead
+  griddep_launch_dependents();
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -471,9 +473,9 @@ cudaError_t launch_bwd_dq_d(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)(a.B * a.Hq), (unsigned)n_tiles);
   trace_begin(kKernelBwdDq, stream);
-  bwd_dq_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_do,
-                                                                 *a.map_dq, p);
-  e = cudaGetLastError();
+  e = launch_pdl(bwd_dq_kernel<D>, grid, dim3(C::kThreads), C::kSmemBytes, stream, *a.map_q, *a.map_k, *a.map_v,
+                 *a.map_do, *a.map_dq, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   trace_end(kKernelBwdDq, stream);
   return e;
 }

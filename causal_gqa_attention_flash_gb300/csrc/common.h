@@ -20,6 +20,26 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled while the kernel
+// ahead of it in the stream finishes, hiding the launch gap between them. Every kernel launched
+// this way calls griddep_wait() before anything else, so it reads nothing before its
+// predecessor has completed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 struct FwdArgs {
   const CUtensorMap* map_q;  // [B*Hq, Sq, D] bf16, box {64, 128, 1}, 128B swizzle
   const CUtensorMap* map_k;  // [B*Hkv, Sk, D]

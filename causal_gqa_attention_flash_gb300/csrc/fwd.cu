@@ -318,6 +318,8 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   auto* bars = reinterpret_cast<FwdBars<ST, VST>*>(smem + C::kBarOff);
+  griddep_wait();
+  griddep_launch_dependents();
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -734,6 +736,8 @@ struct FwdCombineParams {
 // (512 contiguous bytes); the part loops are unrolled so that a thread has many loads in flight.
 template <int D>
 __global__ void __launch_bounds__(128) fwd_combine_kernel(const FwdCombineParams p) {
+  griddep_wait();  // the parts' slots are written by the forward just ahead
+  griddep_launch_dependents();
   constexpr int kChunks = D / 8;
   const int bh = blockIdx.x;
   const int cchunk = (int)blockIdx.y % kChunks;
@@ -970,8 +974,8 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   const int rows = a.cu_q ? a.max_seqlen_q : a.Sq;
   dim3 grid((unsigned)(a.B * a.Hq), (unsigned)(split.kcap > 0 ? split.ctas_y : ceil_div(rows, 2 * kTile)));
   trace_begin(kKernelFwd, stream);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(*a.map_q, *a.map_k, *a.map_v, *a.map_o, p);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, stream, *a.map_q, *a.map_k, *a.map_v, *a.map_o, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   trace_end(kKernelFwd, stream);
   if (e != cudaSuccess || split.split_pairs == 0) return e;
   // The split pairs' slots are merged into O and LSE.
@@ -988,8 +992,8 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   cp.status = a.status;
   const dim3 cgrid((unsigned)(a.B * a.Hq), (unsigned)(split.split_pairs * 2 * (D / 8)));
   trace_begin(kKernelFwdCombine, stream);
-  fwd_combine_kernel<D><<<cgrid, 128, 0, stream>>>(cp);
-  e = cudaGetLastError();
+  e = launch_pdl(fwd_combine_kernel<D>, cgrid, dim3(128), 0, stream, cp);
+  if (e == cudaSuccess) e = cudaGetLastError();
   trace_end(kKernelFwdCombine, stream);
   return e;
 }

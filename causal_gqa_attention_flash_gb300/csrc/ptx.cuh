@@ -43,6 +43,16 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch (sm_90 and later). A kernel launched with programmatic stream
+// serialization may start before the kernel ahead of it in the stream has finished: it waits here,
+// before its first access to memory that kernel may write, until that kernel has completed and its
+// writes are visible (a no-op when the launch was an ordinary one). The trigger lets the kernel
+// behind this one be scheduled once every CTA of this grid has issued it or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
