@@ -322,6 +322,28 @@ __global__ void __launch_bounds__(352, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
+  // Q(t) and step t's -LSE2 / D rows into stage t % ST, on q_full (one thread).
+  auto load_q_rows = [&](int t) {
+    const int st = t % ST;
+    const int hl = (t_begin + t) / n_i;
+    const int i = i_start + (t_begin + t - hl * n_i);
+    const int bhq = bhq0 + hl;
+    uint64_t* bar = &bars->q_full[st];
+    mbar_arrive_expect_tx(bar, C::kTileBytes + 2 * n_rowfl * 4);
+    for (int c = 0; c < C::kChunks; ++c) {
+      const bool q_ok = dbg_tile(c * kChunk, row0 + i * kTile, bhq, D, kChunk, row0, row0 + L, heads_q, p.status);
+      tma_load_3d_chk(smem + C::kQOff + st * C::kTileBytes + c * kBoxBytes, &map_q, bar, c * kChunk, row0 + i * kTile,
+                      bhq, q_ok);
+    }
+    float* srow = reinterpret_cast<float*>(smem + C::kRowOff) + st * 2 * C::kRowFl;
+    const size_t roff = rows_at(hl, i) & ~size_t(3);
+    if (dbg_range((long long)roff, n_rowfl, p.rows_total, p.status)) {
+      bulk_load(srow, p.nlse2 + roff, n_rowfl * 4, bar);
+      bulk_load(srow + C::kRowFl, p.dvec + roff, n_rowfl * 4, bar);
+    } else {
+      mbar_complete_tx(bar, 2 * n_rowfl * 4);
+    }
+  };
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
@@ -346,28 +368,16 @@ __global__ void __launch_bounds__(352, 1)
         const int hl = (t_begin + t) / n_i;
         const int i = i_start + (t_begin + t - hl * n_i);
         const int bhq = bhq0 + hl;
-        // Q(t) and the rows, then dO(t): the two stages are handed back separately (the reduce
-        // warp reads the dQ partial out of the Q stage first), so that Q(t + ST) is on its way
-        // while the dO half of the partial is still being read.
-        if (use > 0 && !mbar_wait(&bars->q_empty[st], (use - 1) & 1, wg)) break;
-        uint64_t* bar = &bars->q_full[st];
-        mbar_arrive_expect_tx(bar, C::kTileBytes + 2 * n_rowfl * 4);
-        for (int c = 0; c < C::kChunks; ++c) {
-          const bool q_ok = dbg_tile(c * kChunk, row0 + i * kTile, bhq, D, kChunk, row0, row0 + L, heads_q, p.status);
-          tma_load_3d_chk(smem + C::kQOff + st * C::kTileBytes + c * kBoxBytes, &map_q, bar, c * kChunk,
-                          row0 + i * kTile, bhq, q_ok);
+        // Q(t) and the rows, then dO(t). The Q and dO stages are handed back separately: with the
+        // dQ partials the reduce warp reads the Q half of the staging first and then loads Q(t)
+        // itself, so that the load does not share the TMA unit with the dO half's reduce-adds.
+        if (!kDq || use == 0) {  // with the dQ partials, the reduce warp loads Q(t) for t >= ST
+          if (use > 0 && !mbar_wait(&bars->q_empty[st], (use - 1) & 1, wg)) break;
+          load_q_rows(t);
+          issued = t + 1;
         }
-        float* srow = reinterpret_cast<float*>(smem + C::kRowOff) + st * 2 * C::kRowFl;
-        const size_t roff = rows_at(hl, i) & ~size_t(3);
-        if (dbg_range((long long)roff, n_rowfl, p.rows_total, p.status)) {
-          bulk_load(srow, p.nlse2 + roff, n_rowfl * 4, bar);
-          bulk_load(srow + C::kRowFl, p.dvec + roff, n_rowfl * 4, bar);
-        } else {
-          mbar_complete_tx(bar, 2 * n_rowfl * 4);
-        }
-        issued = t + 1;
         if (use > 0 && !mbar_wait(&bars->do_empty[st], (use - 1) & 1, wg)) break;
-        bar = &bars->do_full[st];
+        uint64_t* bar = &bars->do_full[st];
         mbar_arrive_expect_tx(bar, C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
           const bool q_ok = dbg_tile(c * kChunk, row0 + i * kTile, bhq, D, kChunk, row0, row0 + L, heads_q, p.status);
@@ -470,33 +480,47 @@ __global__ void __launch_bounds__(352, 1)
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------ dQ reduce warp
-    // Issues the TMA reduce-adds of each step's staged dQ partial, waits until they have read
-    // the staging (the step's Q and dO tiles), and hands the stage back to the producer.
+    // Issues the TMA reduce-adds of each step's staged dQ partial; once the half staged in the
+    // step's Q tile has been read it loads Q(t + ST) into that stage, and once the dO half has
+    // been read it hands the dO stage back to the producer.
     if (kDq && lane == 0) {
       tma_prefetch_desc(&map_acc);
+      tma_prefetch_desc(&map_q);
+      int q_issued = ST < n_steps ? ST : n_steps;  // Q(0 .. ST-1) come from the producer
       for (int t = 0; t < n_steps; ++t) {
         if (!mbar_wait(&bars->stage_full, t & 1, wg)) break;
         const int st = t % ST;
         const int hl = (t_begin + t) / n_i;
         const int i = i_start + (t_begin + t - hl * n_i);
         const int bhq = bhq0 + hl;
-        // The slices in the Q stage go first, in their own bulk group, so that the Q stage is
-        // handed back once they have been read; then those in the dO stage.
+        // The slices staged in the Q tile go first, in their own bulk group; once they have been
+        // read, this thread loads Q(t + ST) into the stage itself, before it issues the slices
+        // staged in the dO tile, so that the load does not share the TMA unit with them.
 #pragma unroll
-        for (int s2 = 0; s2 < D / 32; ++s2) {
-          const uint8_t* stage = s2 < C::kChunks ? smem + C::kQOff + st * C::kTileBytes + s2 * kBoxBytes
-                                                 : smem + C::kDOOff + st * C::kTileBytes + (s2 - C::kChunks) * kBoxBytes;
+        for (int s2 = 0; s2 < C::kChunks; ++s2)
           if (dbg_tile(s2 * 32, row0 + i * kTile, bhq, D, 32, row0, row0 + L, heads_q, p.status))
-            tma_reduce_add_3d(&map_acc, stage, s2 * 32, row0 + i * kTile, bhq);
-          if (s2 == C::kChunks - 1) bulk_commit_group();
-        }
+            tma_reduce_add_3d(&map_acc, smem + C::kQOff + st * C::kTileBytes + s2 * kBoxBytes, s2 * 32,
+                              row0 + i * kTile, bhq);
         bulk_commit_group();
-        bulk_wait_group_read<1>();
-        mbar_arrive(&bars->q_empty[st]);
+        bulk_wait_group_read<0>();
+        if (t + ST < n_steps) {
+          load_q_rows(t + ST);
+          q_issued = t + ST + 1;
+        }
+#pragma unroll
+        for (int s2 = C::kChunks; s2 < D / 32; ++s2)
+          if (dbg_tile(s2 * 32, row0 + i * kTile, bhq, D, 32, row0, row0 + L, heads_q, p.status))
+            tma_reduce_add_3d(&map_acc, smem + C::kDOOff + st * C::kTileBytes + (s2 - C::kChunks) * kBoxBytes,
+                              s2 * 32, row0 + i * kTile, bhq);
+        bulk_commit_group();
         bulk_wait_group_read<0>();
         mbar_arrive(&bars->do_empty[st]);
       }
       bulk_wait_group<0>();
+      if (bars->abort_flag) {  // let the Q loads this thread issued land
+        for (int tt = (q_issued - ST > ST ? q_issued - ST : ST); tt < q_issued; ++tt)
+          mbar_wait_drain(&bars->q_full[tt % ST], (tt / ST) & 1, kWaitLimitNs);
+      }
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ element-wise warps 0..7
