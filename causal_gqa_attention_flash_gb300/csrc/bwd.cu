@@ -345,6 +345,21 @@ __global__ void __launch_bounds__(352, 1)
     }
   };
 
+  // dO(t) into stage t % ST, on do_full (one thread).
+  auto load_do = [&](int t) {
+    const int st = t % ST;
+    const int hl = (t_begin + t) / n_i;
+    const int i = i_start + (t_begin + t - hl * n_i);
+    const int bhq = bhq0 + hl;
+    uint64_t* bar = &bars->do_full[st];
+    mbar_arrive_expect_tx(bar, C::kTileBytes);
+    for (int c = 0; c < C::kChunks; ++c) {
+      const bool q_ok = dbg_tile(c * kChunk, row0 + i * kTile, bhq, D, kChunk, row0, row0 + L, heads_q, p.status);
+      tma_load_3d_chk(smem + C::kDOOff + st * C::kTileBytes + c * kBoxBytes, &map_do, bar, c * kChunk,
+                      row0 + i * kTile, bhq, q_ok);
+    }
+  };
+
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -362,28 +377,19 @@ __global__ void __launch_bounds__(352, 1)
                         kv_coord, kv_ok);
       }
       int issued = 0, issued_do = 0;
-      for (int t = 0; t < n_steps; ++t) {
+      // Q(t) with its rows, then dO(t). With the dQ partials only the first ST steps' tiles come
+      // from here: for later steps the reduce warp loads them into a stage as soon as it has read
+      // the half of the partial staged there, so that the loads do not share the TMA unit with
+      // the other half's reduce-adds.
+      const int n_own = kDq ? (n_steps < ST ? n_steps : ST) : n_steps;
+      for (int t = 0; t < n_own; ++t) {
         const int st = t % ST;
         const int use = t / ST;
-        const int hl = (t_begin + t) / n_i;
-        const int i = i_start + (t_begin + t - hl * n_i);
-        const int bhq = bhq0 + hl;
-        // Q(t) and the rows, then dO(t). The Q and dO stages are handed back separately: with the
-        // dQ partials the reduce warp reads the Q half of the staging first and then loads Q(t)
-        // itself, so that the load does not share the TMA unit with the dO half's reduce-adds.
-        if (!kDq || use == 0) {  // with the dQ partials, the reduce warp loads Q(t) for t >= ST
-          if (use > 0 && !mbar_wait(&bars->q_empty[st], (use - 1) & 1, wg)) break;
-          load_q_rows(t);
-          issued = t + 1;
-        }
+        if (use > 0 && !mbar_wait(&bars->q_empty[st], (use - 1) & 1, wg)) break;
+        load_q_rows(t);
+        issued = t + 1;
         if (use > 0 && !mbar_wait(&bars->do_empty[st], (use - 1) & 1, wg)) break;
-        uint64_t* bar = &bars->do_full[st];
-        mbar_arrive_expect_tx(bar, C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-          const bool q_ok = dbg_tile(c * kChunk, row0 + i * kTile, bhq, D, kChunk, row0, row0 + L, heads_q, p.status);
-          tma_load_3d_chk(smem + C::kDOOff + st * C::kTileBytes + c * kBoxBytes, &map_do, bar, c * kChunk,
-                          row0 + i * kTile, bhq, q_ok);
-        }
+        load_do(t);
         issued_do = t + 1;
       }
       if (bars->abort_flag) {
@@ -514,12 +520,14 @@ __global__ void __launch_bounds__(352, 1)
                               s2 * 32, row0 + i * kTile, bhq);
         bulk_commit_group();
         bulk_wait_group_read<0>();
-        mbar_arrive(&bars->do_empty[st]);
+        if (t + ST < n_steps) load_do(t + ST);
       }
       bulk_wait_group<0>();
-      if (bars->abort_flag) {  // let the Q loads this thread issued land
-        for (int tt = (q_issued - ST > ST ? q_issued - ST : ST); tt < q_issued; ++tt)
+      if (bars->abort_flag) {  // let the Q and dO loads this thread issued land
+        for (int tt = (q_issued - ST > ST ? q_issued - ST : ST); tt < q_issued; ++tt) {
           mbar_wait_drain(&bars->q_full[tt % ST], (tt / ST) & 1, kWaitLimitNs);
+          mbar_wait_drain(&bars->do_full[tt % ST], (tt / ST) & 1, kWaitLimitNs);
+        }
       }
     }
   } else if (warp < 8) {
