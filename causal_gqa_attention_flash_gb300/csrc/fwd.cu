@@ -114,7 +114,23 @@ struct FwdKParams {
   // kernel merges the slots of a pair with the monoid combine.
   int kcap, n_pairs, parts_per_bh;
   float* part;
+  // Division-free geometry at the start of every CTA: G = Hq / Hkv, and the multipliers of
+  // udiv_by (ceil(2^64 / d), 0 for d = 1) for Hq and G.
+  int G;
+  unsigned long long div_hq, div_g;
+  // SMs of the device: the CTA that will take this CTA's place one wave later is n_sm grid
+  // positions further on (one forward CTA per SM); its query tiles are prefetched into L2.
+  int n_sm;
 };
+
+// n / d for 0 <= n < 2^32 and 1 <= d < 2^32, with m = ceil(2^64 / d) (0 for d = 1): the high half
+// of n m is exact because n (m - 2^64 / d) < 2^-32 stays below the distance 1/d from n / d to
+// the next integer. The integer divide instruction sequence and its constant loads are not
+// cheap at the start of a CTA that runs for a few microseconds.
+__device__ __forceinline__ int udiv_by(int n, int d, unsigned long long m) {
+  return d == 1 ? n : (int)__umul64hi((unsigned long long)(unsigned)n, m);
+}
+inline unsigned long long udiv_magic(int d) { return d <= 1 ? 0ull : ~0ull / (unsigned long long)d + 1ull; }
 
 // Position of grid row y in the split forward: pair, part, parts of the pair, and the index of
 // the pair's first slot among its head's slots (only split pairs keep slots).
@@ -134,16 +150,16 @@ struct FwdGeom {
 // bounds read from cu_q / cu_k and checked; returns false (status bit set) for bounds that are
 // not a valid packing, and the CTA does nothing.
 __device__ __forceinline__ bool fwd_geom(const FwdKParams& p, int bh, FwdGeom& g) {
-  const int b = bh / p.Hq;
+  const int b = udiv_by(bh, p.Hq, p.div_hq);
   const int h = bh - b * p.Hq;
-  const int G = p.Hq / p.Hkv;
+  const int hkv = udiv_by(h, p.G, p.div_g);
   if (p.cu_q == nullptr) {
     g.Sq = p.Sq;
     g.Sk = p.Sk;
     g.q_row0 = 0;
     g.k_row0 = 0;
     g.q_coord = bh;
-    g.kv_coord = b * p.Hkv + h / G;
+    g.kv_coord = b * p.Hkv + hkv;
     g.lse_base = (size_t)bh * p.Sq;
   } else {
     const int q0 = __ldg(p.cu_q + b), q1 = __ldg(p.cu_q + b + 1);
@@ -156,7 +172,7 @@ __device__ __forceinline__ bool fwd_geom(const FwdKParams& p, int bh, FwdGeom& g
     g.q_row0 = q0;
     g.k_row0 = k0;
     g.q_coord = h;
-    g.kv_coord = h / G;
+    g.kv_coord = hkv;
     g.lse_base = (size_t)h * p.Tq + q0;
   }
   g.koff = g.Sk - g.Sq;
@@ -343,7 +359,7 @@ __global__ void __launch_bounds__(384, 1)
   // [q nA / parts, (q + 1) nA / parts), the last part up to tile B's last key tile). Below, key
   // tiles are numbered from kb: nA, nB count tile A's and tile B's tiles in the range.
   const int n_all = nA_all > nB_all ? nA_all : nB_all;
-  const int kb = (int)((long long)sp.part * nA_all / sp.parts);
+  const int kb = sp.parts == 1 ? 0 : (int)((long long)sp.part * nA_all / sp.parts);
   const int ke = sp.part == sp.parts - 1 ? n_all : (int)((long long)(sp.part + 1) * nA_all / sp.parts);
   const int nA = (nA_all < ke ? nA_all : ke) - kb;  // >= 1: every part holds a key tile of tile A
   const int nB = nB_all > 0 ? (nB_all < ke ? nB_all : ke) - kb : 0;
@@ -376,6 +392,17 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bars->q_ready[1], 4);
     bars->abort_flag = 0;
     fence_mbar_init();
+    // Q_A and K_0, which the first S product waits for, go out before the rest of the setup
+    // (TMEM allocation, the block barrier, the register split); the producer takes over from Q_B.
+    mbar_arrive_expect_tx(&bars->q_full[0], C::kTileBytes);
+    mbar_arrive_expect_tx(&bars->k0_full, C::kTileBytes);
+    const int qr = g.q_row0 + qtA * kTile, kr = g.k_row0 + kb * kTile;
+    for (int c = 0; c < C::kChunks; ++c) {
+      tma_load_3d_chk(smem + C::kQOff + c * kBoxBytes, &map_q, &bars->q_full[0], c * kChunk, qr, g.q_coord,
+                      dbg_tile(c * kChunk, qr, g.q_coord, D, kChunk, g.q_row0, g.q_row0 + g.Sq, heads_q, p.status));
+      tma_load_3d_chk(smem + C::kKOff + c * kBoxBytes, &map_k, &bars->k0_full, c * kChunk, kr, g.kv_coord,
+                      dbg_tile(c * kChunk, kr, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv, p.status));
+    }
   }
   if (warp == 9) {
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
@@ -392,8 +419,8 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      // Q_A, then K_0, then Q_B (only when tile B has rows; its buffer is otherwise never read),
-      // then V_0: the first S products wait for Q and K_0 only.
+      // Q_A and K_0 came from thread 0; then Q_B (only when tile B has rows; its buffer is
+      // otherwise never read), then V_0: the first S products wait for Q and K_0 only.
       auto load_q = [&](int t) {
         mbar_arrive_expect_tx(&bars->q_full[t], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
@@ -403,7 +430,6 @@ __global__ void __launch_bounds__(384, 1)
                           dbg_tile(c * kChunk, r, g.q_coord, D, kChunk, g.q_row0, g.q_row0 + g.Sq, heads_q, p.status));
         }
       };
-      load_q(0);
       bool q_b_issued = false;
       int issued = 0;
       // K_j and V_j land on one barrier, kv_full[j % ST]: the MMA issuer waits once per key tile.
@@ -413,15 +439,14 @@ __global__ void __launch_bounds__(384, 1)
         const int st = j % ST, vst = j % VST;
         if (j >= ST && !mbar_wait(&bars->k_empty[st], ((j / ST) - 1) & 1, wg)) break;
         if (j >= VST && !mbar_wait(&bars->v_empty[vst], ((j / VST) - 1) & 1, wg)) break;
-        uint64_t* kbar = j == 0 ? &bars->k0_full : &bars->kv_full[st];
         mbar_arrive_expect_tx(&bars->kv_full[st], (j == 0 ? 1 : 2) * C::kTileBytes);
-        if (j == 0) mbar_arrive_expect_tx(kbar, C::kTileBytes);
         const int r = g.k_row0 + (kb + j) * kTile;
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d_chk(smem + C::kKOff + st * C::kTileBytes + c * kBoxBytes, &map_k, kbar,
-                          c * kChunk, r, g.kv_coord,
-                          dbg_tile(c * kChunk, r, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv,
-                                   p.status));
+        if (j > 0)  // K_0 is on its way already
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d_chk(smem + C::kKOff + st * C::kTileBytes + c * kBoxBytes, &map_k, &bars->kv_full[st],
+                            c * kChunk, r, g.kv_coord,
+                            dbg_tile(c * kChunk, r, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv,
+                                     p.status));
         if (j == 0 && nB > 0) {  // Q_B between K_0 and V_0
           load_q(1);
           q_b_issued = true;
@@ -432,12 +457,26 @@ __global__ void __launch_bounds__(384, 1)
                           dbg_tile(c * kChunk, r, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv,
                                    p.status));
         issued = j + 1;
+        if (j == 0 && p.kcap == 0 && p.cu_q == nullptr) {
+          // The query tiles of the CTA one wave later (grid position + n_sm, where it will most
+          // likely start as this wave's CTAs finish) into L2: its own first loads then come from
+          // L2 rather than DRAM.
+          const int nxt = (int)(blockIdx.y * gridDim.x + blockIdx.x) + p.n_sm;
+          if (nxt < (int)(gridDim.x * gridDim.y)) {
+            const int y2 = nxt / (int)gridDim.x;
+            const int bh2 = nxt - y2 * (int)gridDim.x;
+            const int row2 = (2 * ((int)gridDim.y - 1 - y2)) * kTile;
+            for (int t = 0; t < 2; ++t)
+              if (row2 + t * kTile < p.Sq)
+                for (int c = 0; c < C::kChunks; ++c) tma_prefetch_l2_3d(&map_q, c * kChunk, row2 + t * kTile, bh2);
+          }
+        }
       }
       if (bars->abort_flag) {
         // Let every copy already issued land before the CTA's shared memory goes away.
         mbar_wait_drain(&bars->q_full[0], 0, kWaitLimitNs);
         if (q_b_issued) mbar_wait_drain(&bars->q_full[1], 0, kWaitLimitNs);
-        if (issued > 0) mbar_wait_drain(&bars->k0_full, 0, kWaitLimitNs);
+        mbar_wait_drain(&bars->k0_full, 0, kWaitLimitNs);  // K_0 was issued with Q_A
         for (int j = (issued > ST ? issued - ST : 0); j < issued; ++j)
           mbar_wait_drain(&bars->kv_full[j % ST], (j / ST) & 1, kWaitLimitNs);
       }
@@ -956,6 +995,10 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.causal = a.causal;
   p.n_ktiles = ceil_div(a.Sk, kTile);
   p.scale_log2 = a.scale_log2;
+  p.G = a.Hq / a.Hkv;
+  p.div_hq = udiv_magic(a.Hq);
+  p.div_g = udiv_magic(p.G);
+  p.n_sm = device_sm_count();
   p.status = a.status;
   // Dense forward given a split workspace: the key ranges of the longest pairs may be split.
   const FwdSplit split = (a.part && !a.cu_q) ? fwd_split_plan(a.B * a.Hq, a.Sq, a.Sk, a.causal, D)
