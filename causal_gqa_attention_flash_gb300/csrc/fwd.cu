@@ -13,9 +13,10 @@
 // the TMA brings in. Warp roles (384 threads, three warpgroups):
 //   warps 0..3  softmax of tile A: thread r owns row r of A (TMEM lane r);
 //   warps 4..7  softmax of tile B (same, lanes 0..127 through the lane quarter w % 4);
-//   warp 8      TMA producer: Q_A, Q_B once, then K_j into a ring of stages;
-//   warp 9      MMA issuer (one thread) and TMEM owner;
-//   warp 10     TMA producer: V_j into a ring of stages; warp 11 idle.
+//   thread 0    (of warp 0) issues Q_A and K_0 right after initialising the barriers;
+//   warp 8      TMA producer: Q_B and V_0, then K_j and V_j into their rings of
+//               stages, and an L2 prefetch of the query tiles of the CTA one wave later;
+//   warp 9      MMA issuer (one thread) and TMEM owner; warps 10, 11 idle.
 // Registers: launched at kLaunchRegs per thread; the producer warpgroup drops
 // to kLowRegs and the two softmax warpgroups rise to kHighRegs (setmaxnreg).
 // The MMA thread alternates between the tiles: while softmax A works on S_A(j)
