@@ -3,8 +3,9 @@
 import numpy as np
 import pytest
 
-from gpu_helpers import full_case, gqa
-from gqa_inputs import WORKLOADS
+import oracle
+from gpu_helpers import assert_fwd_close, assert_grad_close, full_case, gqa, run_gpu
+from gqa_inputs import WORKLOADS, make_inputs, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +44,27 @@ def test_other_scales(scale):
     """scale = 0 is uniform attention over the visible keys; 1.0 gives peaked rows."""
     g = gqa()
     full_case(g, 1, 4, 2, 257, 64, seed=55, causal=True, scale=scale, do_std=1.0)
+
+
+def test_many_heads():
+    """24,000 query heads (B = 2000, Hq = 12, Hkv = 4: G = 3), so that the kernels' head and KV-head
+    indices span a large grid: every element of 16 batch entries (the first, the last and 14
+    spread between) against the oracle, the rest checked finite."""
+    g = gqa()
+    B, Hq, Hkv, S, D = 2000, 12, 4, 130, 64
+    q, k, v, dO = make_inputs(B, Hq, Hkv, S, D, seed=77, do_std=0.1)
+    got = run_gpu(g, q, k, v, dO, True, 1.0 / np.sqrt(D))
+    for name in ("O", "LSE", "dQ", "dK", "dV"):
+        assert np.all(np.isfinite(got[name])), name
+    pick = np.unique(np.concatenate([[0, B - 1], np.linspace(1, B - 2, 14).astype(int)]))
+    qf, kf, vf, dOf = (to_f64(t[pick]) for t in (q, k, v, dO))
+    O_ref, L_ref = oracle.forward(qf, kf, vf, causal=True, scale=1.0 / np.sqrt(D))
+    where = f"(B={B},Hq={Hq},Hkv={Hkv},S={S},D={D}; entries {list(pick)})"
+    assert_fwd_close(got["O"][pick], got["LSE"][pick], O_ref, L_ref, where)
+    dQ, dK, dV = oracle.backward(qf, kf, vf, dOf, causal=True, scale=1.0 / np.sqrt(D))
+    assert_grad_close("dQ", got["dQ"][pick], dQ, where)
+    assert_grad_close("dK", got["dK"][pick], dK, where)
+    assert_grad_close("dV", got["dV"][pick], dV, where)
 
 
 def test_d128_multi_batch():
