@@ -135,6 +135,7 @@ struct SetupRec {
 std::mutex g_setup_mu;
 std::vector<SetupRec> g_setup;  // a few dozen kernel instances at most
 int g_sm_count[kMaxDevices] = {};
+int g_l2_bytes[kMaxDevices] = {};
 
 }  // namespace
 
@@ -164,6 +165,17 @@ int device_sm_count() {
   if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
     __atomic_store_n(&g_sm_count[dev], n, __ATOMIC_RELAXED);
+  }
+  return n;
+}
+
+int device_l2_bytes() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = __atomic_load_n(&g_l2_bytes[dev], __ATOMIC_RELAXED);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) return 0;
+    __atomic_store_n(&g_l2_bytes[dev], n, __ATOMIC_RELAXED);
   }
   return n;
 }

@@ -121,6 +121,8 @@ struct FwdKParams {
   unsigned long long div_hq, div_g;
   // SMs of the device: the CTA that will take this CTA's place one wave later is n_sm grid
   // positions further on (one forward CTA per SM); its query tiles are prefetched into L2.
+  // 0: no prefetch (queries larger than half the L2, where the prefetched tiles would mostly be
+  // evicted before their CTA starts and read from DRAM twice).
   int n_sm;
 };
 
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(384, 1)
                           dbg_tile(c * kChunk, r, g.kv_coord, D, kChunk, g.k_row0, g.k_row0 + g.Sk, heads_kv,
                                    p.status));
         issued = j + 1;
-        if (j == 0 && p.kcap == 0 && p.cu_q == nullptr) {
+        if (j == 0 && p.n_sm > 0 && p.kcap == 0 && p.cu_q == nullptr) {
           // The query tiles of the CTA one wave later (grid position + n_sm, where it will most
           // likely start as this wave's CTAs finish) into L2: its own first loads then come from
           // L2 rather than DRAM.
@@ -999,7 +1001,8 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.G = a.Hq / a.Hkv;
   p.div_hq = udiv_magic(a.Hq);
   p.div_g = udiv_magic(p.G);
-  p.n_sm = device_sm_count();
+  const size_t q_bytes = (size_t)a.B * a.Hq * a.Sq * a.D * 2;
+  p.n_sm = 2 * q_bytes <= (size_t)device_l2_bytes() ? device_sm_count() : 0;
   p.status = a.status;
   // Dense forward given a split workspace: the key ranges of the longest pairs may be split.
   const FwdSplit split = (a.part && !a.cu_q) ? fwd_split_plan(a.B * a.Hq, a.Sq, a.Sk, a.causal, D)
