@@ -228,8 +228,6 @@ int check_common(int B, int Hq, int Hkv, int S, int D, float scale);
 
 // Number of SMs of the current device, looked up once per device (api.cu).
 int device_sm_count();
-// The device's L2 size in bytes (0 if unknown), looked up once per device.
-int device_l2_bytes();
 
 // Host launchers (fwd.cu, bwd.cu). Return a cudaError_t.
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);

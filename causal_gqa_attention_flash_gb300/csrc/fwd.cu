@@ -135,6 +135,13 @@ __device__ __forceinline__ int udiv_by(int n, int d, unsigned long long m) {
 }
 inline unsigned long long udiv_magic(int d) { return d <= 1 ? 0ull : ~0ull / (unsigned long long)d + 1ull; }
 
+}  // namespace
+
+// The device's L2 size in bytes (0 if unknown), looked up once per device (api.cu).
+int device_l2_bytes();
+
+namespace {
+
 // Position of grid row y in the split forward: pair, part, parts of the pair, and the index of
 // the pair's first slot among its head's slots (only split pairs keep slots).
 struct FwdSplitPos {
